@@ -1,0 +1,158 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests/benchmark and the oracle tests.
+
+This module draws random numbers and rounds them to bf16; it holds none of the
+method's arithmetic.  Every tensor comes from its own ``numpy`` generator
+stream, spawned in a fixed order from ``SeedSequence(seed)``:
+
+    x_kv, z_kv, P_kv, x_I, z_I, P_I, q, qI, w, v
+
+Each bf16 tensor is ``standard_normal`` float32 rounded to bf16
+(round-to-nearest-even); the rounded values are what both the GPU and the
+oracle consume.  The compressor positional biases ``P_kv``/``P_I`` are float32
+parameters and are not rounded.
+
+Workloads follow the shapes of the DeepSeek-V4 CSA/HCA layers described in
+"DeepSeek-V4 Attention Training Systems" (§2 phase table, §4 THD packing,
+§5.1 spans and window): ratio 4 with an overlapping span of 8 tokens for CSA,
+ratio 128 with a span of 128 for HCA, a local window of 128 raw tokens.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+STREAMS = ("x_kv", "z_kv", "P_kv", "x_I", "z_I", "P_I", "q", "qI", "w", "v")
+
+
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round-to-nearest-even; NaN kept quiet."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32)
+    rounded = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    nan = np.isnan(a)
+    if nan.any():
+        rounded = np.where(nan, (u >> np.uint32(16)) | np.uint32(0x40), rounded)
+    return rounded.astype(np.uint16)
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float32 (exact)."""
+    return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def bf16_round(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 value, returned as float32."""
+    return bf16_to_f32(bf16_bits(a))
+
+
+@dataclass
+class Workload:
+    """Shape description of one synthetic workload."""
+    name: str
+    lengths: list            # per-sequence token counts
+    ratio: int               # compression ratio r (0 = window-only layer)
+    overlap: bool            # overlapping span (2r) or not (r)
+    H: int                   # query heads (one shared KV head)
+    d: int                   # head dim
+    window: int              # local window W
+    H_I: int = 0             # indexer heads (0 = no indexer)
+    d_I: int = 0             # indexer head dim
+    topk: int = 0
+    k_pad: int = 0
+    separate_v: bool = False # separate value stream (else K = V)
+    io_fp32: bool = False    # float32 I/O arrays holding bf16 values
+    kl_mode: str = "none"    # "sparse" (selected set), "dense" (all visible) or "none"
+    cap_align: int = 1       # T_cap = total rounded up to this
+    notes: str = ""
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def B(self) -> int:
+        return len(self.lengths)
+
+    @property
+    def T(self) -> int:
+        return int(sum(self.lengths))
+
+    @property
+    def T_cap(self) -> int:
+        a = self.cap_align
+        return ((self.T + a - 1) // a) * a
+
+    @property
+    def cu_seqlens(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.lengths)]).astype(np.int32)
+
+    @property
+    def span(self) -> int:
+        return (2 * self.ratio if self.overlap else self.ratio) if self.ratio > 0 else 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.d))
+
+    @property
+    def n_cmp(self) -> int:
+        return int(sum(L // self.ratio for L in self.lengths)) if self.ratio > 0 else 0
+
+
+def _thd_lengths(seed: int = 0, n: int = 16, lo: int = 1024, hi: int = 16384) -> list:
+    return [int(v) for v in np.random.default_rng(seed).integers(lo, hi + 1, n)]
+
+
+WORKLOADS = {
+    # one sequence L=512, r=4, 4 heads x 64, indexer 2 x 32, top-k 16, W=64, fp32 I/O
+    "tiny": Workload("tiny", [512], 4, True, 4, 64, 64, H_I=2, d_I=32, topk=16, k_pad=16,
+                     separate_v=True, io_fp32=True, kl_mode="sparse"),
+    # CSA sparse mode: L=8192, r=4, 64 x 128, indexer 8 x 64, top-k 512, W=128
+    "csa8k": Workload("csa8k", [8192], 4, True, 64, 128, 128, H_I=8, d_I=64, topk=512,
+                      k_pad=512, kl_mode="sparse"),
+    # HCA: L=65536, r=128 (no overlap), 64 x 128, W=128, no indexer
+    "hca64k": Workload("hca64k", [65536], 128, False, 64, 128, 128),
+    # packed THD varlen CSA: 16 sequences, lengths uniform in [1024, 16384] from seed 0
+    "thd128k": Workload("thd128k", _thd_lengths(), 4, True, 64, 128, 128, H_I=8, d_I=64,
+                        topk=1024, k_pad=1024, kl_mode="none", cap_align=128),
+    # sparse warm-up: L=32768, r=4, 64 x 128, indexer 8 x 64, top-k 2048, W=128,
+    # sparse main output + dense teacher over all visible entries
+    "warmup32k": Workload("warmup32k", [32768], 4, True, 64, 128, 128, H_I=8, d_I=64,
+                          topk=2048, k_pad=2048, kl_mode="dense"),
+}
+
+
+def custom(name="custom", **kw) -> Workload:
+    """A workload with explicit fields (tests use small ragged shapes)."""
+    return Workload(name=name, **kw)
+
+
+def generate(wl: Workload, seed: int = 0) -> dict:
+    """Draw every input stream of ``wl`` (float32 arrays holding bf16 values).
+
+    Returns a dict with the arrays and ``cu_seqlens``.  Streams the workload
+    does not use are not drawn (their generator is still spawned so that the
+    other streams do not move).
+    """
+    ss = np.random.SeedSequence(seed).spawn(len(STREAMS))
+    gens = {name: np.random.default_rng(s) for name, s in zip(STREAMS, ss)}
+    T = wl.T_cap
+    out = {"cu_seqlens": wl.cu_seqlens}
+
+    def normal(name, shape, round_bf16=True):
+        a = gens[name].standard_normal(shape, dtype=np.float32)
+        return bf16_round(a) if round_bf16 else a
+
+    out["x_kv"] = normal("x_kv", (T, wl.d))
+    if wl.ratio > 0:
+        out["z_kv"] = normal("z_kv", (T, wl.d))
+        out["P_kv"] = normal("P_kv", (wl.span, wl.d), round_bf16=False)
+    if wl.H_I > 0:
+        out["x_I"] = normal("x_I", (T, wl.d_I))
+        out["z_I"] = normal("z_I", (T, wl.d_I))
+        out["P_I"] = normal("P_I", (wl.span, wl.d_I), round_bf16=False)
+    out["q"] = normal("q", (T, wl.H, wl.d))
+    if wl.H_I > 0:
+        out["qI"] = normal("qI", (T, wl.H_I, wl.d_I))
+        out["w"] = normal("w", (T, wl.H_I))
+    if wl.separate_v:
+        out["v"] = normal("v", (T, wl.d))
+    return out

@@ -1,0 +1,391 @@
+/*
+ * csa_oracle.c -- plain CPU oracle for the compressed sparse attention
+ * forward (DeepSeek-V4 CSA / HCA / window-only layers).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct
+ * definition that the CUDA library is checked against.  Only the test suite,
+ * the package smoke check and the benchmark's CPU-baseline leg may load it.
+ * It shares no code, header, table or constant with the CUDA path.
+ *
+ * Every function evaluates the plain definition, in double precision, one
+ * query (or one compressed entry) at a time.  Inputs are the exact values the
+ * GPU receives (bf16 values widened to float, or float parameters).  Loops
+ * over independent queries are spread over OpenMP threads when the compiler
+ * supports it; the arithmetic of each query is sequential.
+ *
+ * Sources (page title, section):
+ *   "DeepSeek-V4 Attention Training Systems" (Megatron V4 notes):
+ *     §2  phase table: dense mode / sparse warm-up / sparse mode;
+ *     §3  indexer KL loss  L_I = sum_t KL(Softmax(a_{t,C_t}) || Softmax(i_{t,C_t}));
+ *     §4  THD packing, n_b = floor(L_b / r), reset list at sample boundaries;
+ *     §5.1 compression spans D_compress = 8 (overlapping r=4) and 128 (HCA),
+ *          local window D_window = 128;
+ *     §8.2 kernel map: learned-score compressor reduction, indexer score +
+ *          top-k, selected attention returning output and LSE, compressed
+ *          ids combined with window ids;
+ *     §9  precision table: FP32 compressor positional parameter, FP32
+ *          attention sink, FP32 softmax / KL math.
+ *
+ * Readings taken where the pages leave a step open (each is listed in the
+ * design notes and pinned by the CPU tests where a pin exists):
+ *   - compressor: per-channel softmax gate over the span, logits z + P[u];
+ *     overlapping entry j spans blocks j-1 and j (2r tokens), the
+ *     non-overlapping entry spans block j (r tokens); span positions before
+ *     the sequence start are left out of the softmax (parity unpinned beyond
+ *     "softmax-gated weighted sum" and the span widths);
+ *   - indexer logit i_{t,j} = sum_h w[t,h] * ReLU(qI[t,h,:] . kI[j,:]);
+ *   - top-k ties go to the smaller entry index; output ascending, -1 padded;
+ *   - attention sink is a denominator-only logit; lse includes it;
+ *   - teacher a_{t,j} = log of the head-averaged per-head softmax over C_t
+ *     (parity unpinned: the pages do not say how heads are combined).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+/* Sequence that owns packed row `row`: the b with cu[b] <= row < cu[b+1],
+ * or -1 for capacity padding (row >= cu[B]).  §4: samples are concatenated on
+ * one token axis and delimited by cu_seqlens. */
+static int owner_sequence(const int32_t* cu, int B, int64_t row) {
+  if (B <= 0 || row < cu[0] || row >= cu[B]) return -1;
+  for (int b = 0; b < B; ++b)
+    if (row >= cu[b] && row < cu[b + 1]) return b;
+  return -1;
+}
+
+/* Number of compressed entries visible to local query position t:
+ * entry j (tokens up to r(j+1)-1) is visible once r(j+1)-1 <= t  (§4 causal
+ * visibility of completed compressed groups). */
+static int64_t visible_count(int64_t t, int r) {
+  if (r <= 0) return 0;
+  return (t + 1) / r;
+}
+
+/* §4: only complete groups are compressed, n_b = floor(L_b / r).
+ * cu_cmp[b] = sum_{b' < b} n_{b'}.  Returns cu_cmp[B]. */
+int64_t oracle_compressed_offsets(const int32_t* cu, int B, int r, int32_t* cu_cmp) {
+  cu_cmp[0] = 0;
+  for (int b = 0; b < B; ++b) {
+    int64_t L = (int64_t)cu[b + 1] - cu[b];
+    int64_t n = r > 0 ? L / r : 0;
+    cu_cmp[b + 1] = (int32_t)(cu_cmp[b] + n);
+  }
+  return cu_cmp[B];
+}
+
+/* Learned-score block compression (§4, §5.1, §8.2 "C4/C128 compression",
+ * §9 FP32 positional parameter).
+ *   x, z : [T, D] packed rows (values, gate logits)
+ *   P    : [S, D] positional logit bias, S = 2r (overlap) or r
+ *   out  : [N_c, D] compressed rows, double
+ * Entry j of sequence b covers local tokens first .. first+S-1 with
+ * first = r*j + r - S; positions before the start of the sequence are not
+ * available and are left out of the per-channel softmax. */
+void oracle_compress(const float* x, const float* z, const float* P,
+                     const int32_t* cu, const int32_t* cu_cmp, int B, int D,
+                     int r, int overlap, double* out) {
+  const int S = overlap ? 2 * r : r;
+  for (int b = 0; b < B; ++b) {
+    const int64_t L = (int64_t)cu[b + 1] - cu[b];
+    const int64_t n = r > 0 ? L / r : 0;
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < n; ++j) {
+      const int64_t first = (int64_t)r * j + r - S;
+      for (int c = 0; c < D; ++c) {
+        double m = -INFINITY;
+        for (int u = 0; u < S; ++u) {
+          const int64_t t = first + u;
+          if (t < 0) continue;
+          const double logit = (double)z[(cu[b] + t) * (int64_t)D + c] + (double)P[(int64_t)u * D + c];
+          if (logit > m) m = logit;
+        }
+        double den = 0.0, num = 0.0;
+        for (int u = 0; u < S; ++u) {
+          const int64_t t = first + u;
+          if (t < 0) continue;
+          const double logit = (double)z[(cu[b] + t) * (int64_t)D + c] + (double)P[(int64_t)u * D + c];
+          const double e = exp(logit - m);
+          den += e;
+          num += e * (double)x[(cu[b] + t) * (int64_t)D + c];
+        }
+        out[((int64_t)cu_cmp[b] + j) * D + c] = num / den;
+      }
+    }
+  }
+}
+
+/* Lightning-indexer logits of one query against its visible entries
+ * (§3 i_{t,j}; form sum_h w * ReLU(qI . kI)).  logits must hold nvis values. */
+static void indexer_logits_one(const float* qI, const float* w, const float* kI,
+                               int64_t row, int64_t cmp_base, int64_t nvis,
+                               int H_I, int dI, double* logits) {
+  for (int64_t j = 0; j < nvis; ++j) {
+    double s = 0.0;
+    for (int h = 0; h < H_I; ++h) {
+      double dot = 0.0;
+      for (int c = 0; c < dI; ++c)
+        dot += (double)qI[(row * H_I + h) * (int64_t)dI + c] * (double)kI[(cmp_base + j) * dI + c];
+      const double relu = dot > 0.0 ? dot : 0.0;
+      s += (double)w[row * H_I + h] * relu;
+    }
+    logits[j] = s;
+  }
+}
+
+/* Indexer logits for a list of query rows: logits[q*max_vis + j] for
+ * j < nvis[q] (the rest left untouched). */
+void oracle_indexer_logits(const float* qI, const float* w, const float* kI,
+                           const int32_t* cu, const int32_t* cu_cmp, int B,
+                           int H_I, int dI, int r, const int64_t* rows, int nq,
+                           int64_t max_vis, double* logits, int32_t* nvis_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int q = 0; q < nq; ++q) {
+    const int64_t row = rows[q];
+    const int b = owner_sequence(cu, B, row);
+    if (b < 0) { nvis_out[q] = 0; continue; }
+    const int64_t t = row - cu[b];
+    int64_t nvis = visible_count(t, r);
+    if (nvis > max_vis) nvis = max_vis;
+    nvis_out[q] = (int32_t)nvis;
+    indexer_logits_one(qI, w, kI, row, cu_cmp[b], nvis, H_I, dI, logits + (int64_t)q * max_vis);
+  }
+}
+
+typedef struct { double s; int64_t j; } scored_entry;
+
+/* Larger score first; equal scores: smaller entry index first. */
+static int by_score_then_index(const void* pa, const void* pb) {
+  const scored_entry* a = (const scored_entry*)pa;
+  const scored_entry* b = (const scored_entry*)pb;
+  if (a->s > b->s) return -1;
+  if (a->s < b->s) return 1;
+  return (a->j > b->j) - (a->j < b->j);
+}
+
+/* Per-query top-k of the indexer logits (§8 "indexer scoring and radix
+ * top-k", §8.2 flat global index list, §8.1 top-k padding).
+ * idx[q*k_pad + i]: the min(topk, |V_t|) selected entries as global
+ * compressed rows cu_cmp[b] + j in ascending j, then -1 up to k_pad.
+ * Capacity rows (not in any sequence) get all -1. */
+void oracle_indexer_topk(const float* qI, const float* w, const float* kI,
+                         const int32_t* cu, const int32_t* cu_cmp, int B,
+                         int H_I, int dI, int r, int topk, int k_pad,
+                         const int64_t* rows, int nq, int32_t* idx) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int q = 0; q < nq; ++q) {
+    int32_t* out = idx + (int64_t)q * k_pad;
+    for (int i = 0; i < k_pad; ++i) out[i] = -1;
+    const int64_t row = rows[q];
+    const int b = owner_sequence(cu, B, row);
+    if (b < 0) continue;
+    const int64_t t = row - cu[b];
+    const int64_t nvis = visible_count(t, r);
+    if (nvis == 0) continue;
+    double* logits = (double*)malloc(sizeof(double) * nvis);
+    scored_entry* order = (scored_entry*)malloc(sizeof(scored_entry) * nvis);
+    char* chosen = (char*)calloc((size_t)nvis, 1);
+    indexer_logits_one(qI, w, kI, row, cu_cmp[b], nvis, H_I, dI, logits);
+    for (int64_t j = 0; j < nvis; ++j) { order[j].s = logits[j]; order[j].j = j; }
+    qsort(order, (size_t)nvis, sizeof(scored_entry), by_score_then_index);
+    const int64_t m = nvis < topk ? nvis : topk;
+    for (int64_t i = 0; i < m; ++i) chosen[order[i].j] = 1;
+    int64_t k = 0;
+    for (int64_t j = 0; j < nvis; ++j)
+      if (chosen[j]) out[k++] = (int32_t)(cu_cmp[b] + j);
+    free(chosen); free(order); free(logits);
+  }
+}
+
+/* Attention kinds: which compressed entries join the candidate list. */
+enum { ORACLE_CSA = 0, ORACLE_HCA = 1, ORACLE_WINDOW = 2 };
+
+/* Selected / HCA / window-only attention forward for a list of query rows
+ * (§2 phase table: top-k compressed entries + local window; HCA reads every
+ * completed compressed entry + the window; window-only has no compressed
+ * part; §8.2 FlashMLA returns output and LSE; §9 FP32 attention sink).
+ *
+ * One shared KV head (MQA): key rows kc (compressed) / kr (raw), value rows
+ * vc / vr (pass the key arrays again when K = V).  Candidate list of query t
+ * in sequence b: compressed rows (csa: the valid entries of idx row; hca: all
+ * visible entries), then the window rows cu[b] + s for s in
+ * [max(0, t-W+1), t].  Entries and window rows are distinct keys.
+ * For each head h:
+ *   s_i   = scale * q[t,h,:] . K_i
+ *   m     = max(max_i s_i, sink_h)   (sink only when given)
+ *   Z     = sum_i exp(s_i - m) + exp(sink_h - m)
+ *   o     = sum_i exp(s_i - m) V_i / Z,   lse = m + log Z
+ *   lse_cmp = logsumexp of s_i over the compressed candidates only
+ *             (no sink, no window), -inf when there are none.
+ * Capacity rows: o = 0, lse = lse_cmp = -inf.
+ * err[q] = 1 when an idx entry lies outside the query's visible entries (the
+ * entry is then skipped), else 0. */
+void oracle_attention(int kind, const float* q, const float* kc, const float* vc,
+                      const float* kr, const float* vr, const int32_t* idx,
+                      int k_pad, const float* sink, const int32_t* cu,
+                      const int32_t* cu_cmp, int B, int H, int d, int r, int W,
+                      double scale, const int64_t* rows, int nq, double* o,
+                      double* lse, double* lse_cmp, int32_t* err) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int qi = 0; qi < nq; ++qi) {
+    const int64_t row = rows[qi];
+    double* oq = o + (int64_t)qi * H * d;
+    err[qi] = 0;
+    const int b = owner_sequence(cu, B, row);
+    if (b < 0) {
+      for (int64_t e = 0; e < (int64_t)H * d; ++e) oq[e] = 0.0;
+      for (int h = 0; h < H; ++h) { lse[(int64_t)qi * H + h] = -INFINITY; lse_cmp[(int64_t)qi * H + h] = -INFINITY; }
+      continue;
+    }
+    const int64_t t = row - cu[b];
+    const int64_t nvis = kind == ORACLE_WINDOW ? 0 : visible_count(t, r);
+    /* compressed candidate rows */
+    int64_t ncmp = 0;
+    int64_t cap = kind == ORACLE_CSA ? k_pad : nvis;
+    int64_t* crow = (int64_t*)malloc(sizeof(int64_t) * (cap > 0 ? cap : 1));
+    if (kind == ORACLE_CSA) {
+      for (int i = 0; i < k_pad; ++i) {
+        const int64_t g = idx[row * (int64_t)k_pad + i];
+        if (g < 0) continue;
+        if (g < cu_cmp[b] || g >= cu_cmp[b] + nvis) { err[qi] = 1; continue; }
+        crow[ncmp++] = g;
+      }
+    } else if (kind == ORACLE_HCA) {
+      for (int64_t j = 0; j < nvis; ++j) crow[ncmp++] = cu_cmp[b] + j;
+    }
+    const int64_t w0 = t - W + 1 > 0 ? t - W + 1 : 0;
+    const int64_t nwin = t - w0 + 1;
+    const int64_t n = ncmp + nwin;
+    double* s = (double*)malloc(sizeof(double) * n);
+    for (int h = 0; h < H; ++h) {
+      const float* qh = q + (row * H + h) * (int64_t)d;
+      for (int64_t i = 0; i < n; ++i) {
+        const float* kk = i < ncmp ? kc + crow[i] * d : kr + (cu[b] + w0 + (i - ncmp)) * (int64_t)d;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += (double)qh[c] * (double)kk[c];
+        s[i] = scale * dot;
+      }
+      double m = -INFINITY;
+      for (int64_t i = 0; i < n; ++i) if (s[i] > m) m = s[i];
+      if (sink && (double)sink[h] > m) m = (double)sink[h];
+      double Z = 0.0;
+      for (int64_t i = 0; i < n; ++i) Z += exp(s[i] - m);
+      if (sink) Z += exp((double)sink[h] - m);
+      double* oh = oq + (int64_t)h * d;
+      for (int c = 0; c < d; ++c) oh[c] = 0.0;
+      for (int64_t i = 0; i < n; ++i) {
+        const double p = exp(s[i] - m) / Z;
+        const float* vv = i < ncmp ? vc + crow[i] * d : vr + (cu[b] + w0 + (i - ncmp)) * (int64_t)d;
+        for (int c = 0; c < d; ++c) oh[c] += p * (double)vv[c];
+      }
+      lse[(int64_t)qi * H + h] = m + log(Z);
+      if (ncmp == 0) {
+        lse_cmp[(int64_t)qi * H + h] = -INFINITY;
+      } else {
+        double mc = -INFINITY;
+        for (int64_t i = 0; i < ncmp; ++i) if (s[i] > mc) mc = s[i];
+        double Zc = 0.0;
+        for (int64_t i = 0; i < ncmp; ++i) Zc += exp(s[i] - mc);
+        lse_cmp[(int64_t)qi * H + h] = mc + log(Zc);
+      }
+    }
+    free(s);
+    free(crow);
+  }
+}
+
+/* Indexer KL auxiliary loss for a list of query rows (§3 equation; §2 phase
+ * table: dense warm-up teacher over every visible entry, sparse mode over the
+ * selected set; §9 FP32 loss math).
+ *   C_t     = valid entries of idx row (idx != NULL) or every visible entry
+ *   pi_h(j) = softmax over j in C_t of scale * q[t,h,:] . K_j
+ *   p(j)    = (1/H) sum_h pi_h(j)            (teacher, a_{t,j} = log p(j))
+ *   q(j)    = softmax over j in C_t of i_{t,j} (indexer logits)
+ *   KL_t    = sum_j p(j) (log p(j) - log q(j))
+ * kl[q] = KL_t (0 when C_t is empty), csize[q] = |C_t|.
+ * err[q] = 1 when an idx entry lies outside the visible entries (skipped). */
+void oracle_indexer_kl(const float* q, const float* kc, const float* qI,
+                       const float* w, const float* kI, const int32_t* idx,
+                       int k_pad, const int32_t* cu, const int32_t* cu_cmp,
+                       int B, int H, int d, int H_I, int dI, int r,
+                       double scale, const int64_t* rows, int nq, double* kl,
+                       int32_t* csize, int32_t* err) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int qi = 0; qi < nq; ++qi) {
+    const int64_t row = rows[qi];
+    kl[qi] = 0.0; csize[qi] = 0; err[qi] = 0;
+    const int b = owner_sequence(cu, B, row);
+    if (b < 0) continue;
+    const int64_t t = row - cu[b];
+    const int64_t nvis = visible_count(t, r);
+    int64_t cap = idx ? k_pad : nvis;
+    int64_t* cj = (int64_t*)malloc(sizeof(int64_t) * (cap > 0 ? cap : 1));
+    int64_t n = 0;
+    if (idx) {
+      for (int i = 0; i < k_pad; ++i) {
+        const int64_t g = idx[row * (int64_t)k_pad + i];
+        if (g < 0) continue;
+        if (g < cu_cmp[b] || g >= cu_cmp[b] + nvis) { err[qi] = 1; continue; }
+        cj[n++] = g - cu_cmp[b];
+      }
+    } else {
+      for (int64_t j = 0; j < nvis; ++j) cj[n++] = j;
+    }
+    csize[qi] = (int32_t)n;
+    if (n == 0) { free(cj); continue; }
+    /* student: indexer logits over C_t */
+    double* all_i = (double*)malloc(sizeof(double) * (nvis > 0 ? nvis : 1));
+    indexer_logits_one(qI, w, kI, row, cu_cmp[b], nvis, H_I, dI, all_i);
+    double* ilog = (double*)malloc(sizeof(double) * n);
+    for (int64_t k = 0; k < n; ++k) ilog[k] = all_i[cj[k]];
+    double mi = -INFINITY;
+    for (int64_t k = 0; k < n; ++k) if (ilog[k] > mi) mi = ilog[k];
+    double Zi = 0.0;
+    for (int64_t k = 0; k < n; ++k) Zi += exp(ilog[k] - mi);
+    const double lse_i = mi + log(Zi);
+    /* teacher: per-head softmax over C_t, then the head average */
+    double* p = (double*)calloc((size_t)n, sizeof(double));
+    double* s = (double*)malloc(sizeof(double) * n);
+    for (int h = 0; h < H; ++h) {
+      const float* qh = q + (row * H + h) * (int64_t)d;
+      for (int64_t k = 0; k < n; ++k) {
+        const float* kk = kc + (cu_cmp[b] + cj[k]) * (int64_t)d;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += (double)qh[c] * (double)kk[c];
+        s[k] = scale * dot;
+      }
+      double m = -INFINITY;
+      for (int64_t k = 0; k < n; ++k) if (s[k] > m) m = s[k];
+      double Z = 0.0;
+      for (int64_t k = 0; k < n; ++k) Z += exp(s[k] - m);
+      for (int64_t k = 0; k < n; ++k) p[k] += exp(s[k] - m) / Z;
+    }
+    double acc = 0.0;
+    for (int64_t k = 0; k < n; ++k) {
+      const double pk = p[k] / H;
+      if (pk > 0.0) acc += pk * (log(pk) - (ilog[k] - lse_i));
+    }
+    kl[qi] = acc;
+    free(s); free(p); free(ilog); free(all_i); free(cj);
+  }
+}
