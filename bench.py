@@ -1,0 +1,357 @@
+"""Benchmark: CSA forward query-tokens/s and TFLOP/s against the GB300 roofline.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+compress (main KV + indexer K), indexer score + top-k, selected attention with
+the local window, indexer KL loss.  The default workload is the sparse warm-up
+layer at L = 32768 (r = 4, 64 heads x 128, indexer 8 x 64, top-k 2048, W = 128,
+dense teacher over every visible entry), the shape of the DeepSeek-V4 CSA
+layers in "DeepSeek-V4 Attention Training Systems" (§2 phase table).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Multi-GPU: one process per GPU under
+torch.distributed.run; each rank runs its own copy of the workload (the path
+has no exchange step on one GPU: replicas only), value = all ranks' tokens /
+max-over-ranks time.  ``--impl reference`` times the CPU oracle on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from compressed_sparse_attention_compress_gb300 import inputs as I  # noqa: E402
+from compressed_sparse_attention_compress_gb300 import workload as W  # noqa: E402
+
+METRIC = "CSA fwd query-tokens/s at L=32K and TFLOP/s, % of GB300 bf16/HBM roofline"
+UNIT = "query-tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(wl, arrs, seconds_target=15.0, max_rows=None):
+    """Time the oracle on a strided sample of query rows of the same workload."""
+    import oracle
+    cu = arrs["cu_seqlens"]
+    threads = oracle.num_threads()
+    scale = wl.scale
+    t0 = time.perf_counter()
+    kv = I.bf16_round(oracle.compress(arrs["x_kv"], arrs["z_kv"], arrs["P_kv"], cu, wl.ratio, wl.overlap)
+                      .astype(np.float32)) if wl.ratio > 0 else None
+    kI = I.bf16_round(oracle.compress(arrs["x_I"], arrs["z_I"], arrs["P_I"], cu, wl.ratio, wl.overlap)
+                      .astype(np.float32)) if wl.H_I > 0 else None
+    t_comp = time.perf_counter() - t0
+    # probe cost on a few rows near the end (the most expensive queries), then size the sample
+    n = 8
+    while True:
+        stride = max(1, wl.T // n)
+        rows = np.arange(stride // 2, wl.T, stride, dtype=np.int64)[:n]
+        t1 = time.perf_counter()
+        if wl.H_I > 0:
+            idx_rows = oracle.indexer_topk(arrs["qI"], arrs["w"], kI, cu, wl.ratio, wl.topk, wl.k_pad, rows)
+            idx = np.full((wl.T_cap, wl.k_pad), -1, np.int32)
+            idx[rows] = idx_rows
+            oracle.attention(oracle.KIND_CSA, arrs["q"], kv, None, arrs["x_kv"], None, cu, wl.ratio, wl.window,
+                             scale, idx=idx, rows=rows)
+            if wl.kl_mode != "none":
+                oracle.indexer_kl(arrs["q"], kv, arrs["qI"], arrs["w"], kI, cu, wl.ratio, scale,
+                                  idx=idx if wl.kl_mode == "sparse" else None, rows=rows)
+        elif wl.ratio > 0:
+            oracle.attention(oracle.KIND_HCA, arrs["q"], kv, None, arrs["x_kv"], None, cu, wl.ratio, wl.window,
+                             scale, rows=rows)
+        else:
+            oracle.attention(oracle.KIND_WINDOW, arrs["q"], None, None, arrs["x_kv"], None, cu, 0, wl.window,
+                             scale, rows=rows)
+        dt = time.perf_counter() - t1
+        if dt >= seconds_target or n >= wl.T or (max_rows and n >= max_rows):
+            break
+        n = min(wl.T, max(n * 2, int(n * seconds_target / max(dt, 1e-3))))
+        if max_rows:
+            n = min(n, max_rows)
+    # rate: sampled rows through the per-query steps + the sample's share of compression
+    total = dt + t_comp * len(rows) / wl.T
+    return {"value": len(rows) / total, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} query rows strided over the {wl.T}-token workload (every {stride}th), "
+                      f"plus the rows' share of the full-sequence compression; fp64 C oracle, OpenMP"}
+
+
+def run_reference(args, wl):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    arrs = I.generate(wl, args.seed)
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(wl, arrs, seconds_target=2.0, max_rows=64)
+    base = None
+    t0 = time.perf_counter()
+    per_step = max(1.0, min(args.ref_seconds, 150.0 / max(args.steps, 1)))
+    for _ in range(args.steps):
+        base = cpu_baseline(wl, arrs, seconds_target=per_step)
+        vals.append(base["value"])
+    elapsed = time.perf_counter() - t0
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / max(args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "sample": base["sample"]},
+            "cpu_baseline": {**base, "value": v},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl):
+    import torch
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    from compressed_sparse_attention_compress_gb300.forward import Forward, to_device
+
+    arrs = I.generate(wl, args.seed)
+    dev_in = to_device(arrs, wl.io_fp32, local)
+    f = Forward(wl, dev_in, device=local)
+    stream = torch.cuda.current_stream()
+    counts = W.counts(wl)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    # stage boundaries for per-kernel durations (events on the launching stream)
+    stages = []
+    if wl.ratio > 0:
+        stages.append(("compress", f.compress))
+        if wl.H_I > 0:
+            stages.append(("indexer_topk", f.topk))
+    stages.append(("attention", f.attend))
+    if wl.kl_mode != "none":
+        stages.append(("indexer_kl", f.kl))
+
+    for _ in range(max(args.warmup, 3)):
+        f.run()
+    torch.cuda.synchronize()
+    assert f.h.device_status() == 0, "device status raised during warm-up"
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            for i, (_, fn) in enumerate(stages):
+                fn()
+                ev[s][i + 1].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    total_ms = sum(ev[s][0].elapsed_time(ev[s][-1]) for s in range(args.steps))
+    stage_ms = {name: sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)) / args.steps
+                for i, (name, _) in enumerate(stages)}
+    assert f.h.device_status() == 0, "device status raised during the timed steps"
+    ms_step = total_ms / args.steps
+    if ws > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = ws * wl.T / (ms_step * 1e-3)
+
+    # e2e: the same step through the public API with host buffers (pinned), inputs
+    # copied in and the loss (or lse) read back inside the timed region
+    host = {k: v.cpu().pin_memory() for k, v in dev_in.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    res = f.kl_sum if wl.kl_mode != "none" else f.lse
+    res_host = torch.empty(res.shape, dtype=res.dtype).pin_memory()
+    d2h = res_host.numel() * res_host.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        f.run()
+        res_host.copy_(res, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peaks, src = _peaks()
+    # dominant kernel: the stage with the largest share of the step
+    dom = max(stage_ms, key=stage_ms.get)
+    per_launch = {"attention": ("tensor", counts["attn_flops"]),
+                  "indexer_kl": ("tensor", counts["teacher_flops"]),
+                  "indexer_topk": ("tensor", counts["indexer_flops"]),
+                  "compress": ("hbm", counts["compress_bytes"])}
+    bound, work = per_launch[dom]
+    sec = stage_ms[dom] * 1e-3
+    if bound == "tensor":
+        achieved = work / sec / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        unit = "TFLOP/s"
+    else:
+        achieved = work / sec / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    tflops = counts["total_flops"] / (ms_step * 1e-3) / 1e12
+    traffic = _traffic(dom, wl.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "global_batch": wl.B * ws, "seq_len": max(wl.lengths),
+                   "tokens_per_gpu": wl.T, "ratio": wl.ratio, "heads": wl.H, "head_dim": wl.d, "topk": wl.topk,
+                   "window": wl.window, "kl": wl.kl_mode, "parallelism": f"replicas{ws}",
+                   "l2": "inputs larger than L2 (q alone is %.0f MB)" % (wl.T_cap * wl.H * wl.d * 2 / 1e6)},
+        "tflops": tflops,
+        "tflops_frac_of_peak": tflops / peaks["bf16_tflops_sustained"],
+        "stage_ms": stage_ms,
+        "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"},
+        "e2e": {"value": ws * wl.T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * f_launches(wl),
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and ws >= 1:
+        line["cpu_baseline"] = cpu_baseline(wl, arrs, seconds_target=args.ref_seconds)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def f_launches(wl) -> int:
+    """Kernels of ours launched per step."""
+    n = 0
+    if wl.ratio > 0:
+        n += 1 + 1 + (1 if wl.separate_v else 0) + (1 if wl.H_I > 0 else 0)   # offsets + compress calls
+        if wl.H_I > 0:
+            n += 2                                                              # top-k + capacity fill
+    n += 1                                                                      # attention
+    if wl.kl_mode != "none":
+        n += 2                                                                  # KL + finalize
+    return n
+
+
+def _traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel, if current."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    return d.get(workload, {}).get(kernel)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="warmup32k", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--ref-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = I.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,68 @@
+// launch.h -- host-side launchers of the kernels (internal to libcsa.so).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace csa {
+
+bool compress_supported(int D, int r, int S, int in_bytes);
+cudaError_t launch_compress(const void* x, const void* z, const float* P, const int32_t* cu,
+                            const int32_t* cu_cmp, int B, int T_cap, int D, int r, int S, bool fp32,
+                            void* out, int* status, cudaStream_t stream);
+cudaError_t launch_compressed_offsets(const int32_t* cu, int B, int r, int32_t* cu_cmp, int* status,
+                                      cudaStream_t stream);
+
+// Indexer scoring + top-k.
+bool indexer_topk_supported(int H_I, int d_I, int max_vis, int k_pad, int in_bytes);
+cudaError_t launch_indexer_topk(const void* qI, const void* w, const void* kI, const int32_t* cu,
+                                const int32_t* cu_cmp, int B, int T_cap, int max_vis, int H_I,
+                                int d_I, int r, int topk, int k_pad, bool fp32, int32_t* idx,
+                                int* status, cudaStream_t stream);
+
+// Attention kinds.
+enum AttnKind { kAttnCSA = 0, kAttnHCA = 1, kAttnWindow = 2 };
+
+struct AttnArgs {
+  const void* q;
+  const void* k_cmp;
+  const void* v_cmp;
+  const void* k_raw;
+  const void* v_raw;
+  const int32_t* idx;
+  int k_pad;
+  const float* sink;
+  const int32_t* cu;
+  const int32_t* cu_cmp;
+  int B, T_cap, H, d, r, window;
+  float scale;
+  void* out;
+  float* lse;
+  float* lse_cmp;
+  int* status;
+};
+cudaError_t launch_attention(AttnKind kind, const AttnArgs& a, bool fp32, cudaStream_t stream);
+
+struct KLArgs {
+  const void* q;
+  const void* k_cmp;
+  const void* qI;
+  const void* w;
+  const void* kI;
+  const int32_t* idx;   // nullptr: dense teacher over every visible entry
+  int k_pad;
+  const float* lse_cmp; // optional per-head normaliser over C_t (sparse mode)
+  const int32_t* cu;
+  const int32_t* cu_cmp;
+  int B, T_cap, H, d, H_I, d_I, r;
+  float scale;
+  float* kl_rows;       // [T_cap] per-query KL
+  int32_t* csize;       // [T_cap] |C_t|
+  float* kl_sum;
+  int32_t* n_valid;
+  int* status;
+};
+cudaError_t launch_indexer_kl(const KLArgs& a, bool fp32, cudaStream_t stream);
+
+}  // namespace csa

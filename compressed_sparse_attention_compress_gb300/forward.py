@@ -1,0 +1,114 @@
+"""One full CSA / HCA / window-only forward through the C ABI.
+
+``Forward`` holds the device buffers of one workload (capacity-sized, as the
+static-capacity contract of "DeepSeek-V4 Attention Training Systems" §4.1
+asks) and enqueues the calls in the order of the page's fused training
+forward (§8.2): compress main KV and indexer K, indexer score + top-k,
+selected attention (O, LSE), indexer KL.  HCA layers skip the indexer; window
+layers skip the compressor too.  Every step is a libcsa.so kernel; this class
+only allocates buffers and passes pointers.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import api
+
+
+class Forward:
+    def __init__(self, wl, inputs: dict, device: int = 0, handle: api.Handle | None = None):
+        """``inputs``: torch tensors on the device (bf16, or float32 when wl.io_fp32)."""
+        self.wl = wl
+        self.dev = torch.device("cuda", device)
+        self.h = handle or api.Handle(device)
+        self.x = inputs
+        dt = torch.float32 if wl.io_fp32 else torch.bfloat16
+        T, H, d = wl.T_cap, wl.H, wl.d
+        self.cu = inputs["cu_seqlens"]
+        self.max_seqlen = max(wl.lengths) if wl.lengths else 0
+        self.scale = 1.0 / math.sqrt(d)
+        B = wl.B
+        if wl.ratio > 0:
+            n_cap = max(1, T // wl.ratio)
+            self.cu_cmp = torch.zeros(B + 1, dtype=torch.int32, device=self.dev)
+            self.kv_cmp = torch.zeros(n_cap, d, dtype=dt, device=self.dev)
+            self.v_cmp = torch.zeros(n_cap, d, dtype=dt, device=self.dev) if wl.separate_v else None
+            if wl.H_I > 0:
+                self.kI = torch.zeros(n_cap, wl.d_I, dtype=dt, device=self.dev)
+                self.idx = torch.empty(T, wl.k_pad, dtype=torch.int32, device=self.dev)
+        self.out = torch.empty(T, H, d, dtype=dt, device=self.dev)
+        self.lse = torch.empty(T, H, dtype=torch.float32, device=self.dev)
+        self.lse_cmp = torch.empty(T, H, dtype=torch.float32, device=self.dev) if wl.ratio > 0 else None
+        if wl.kl_mode != "none":
+            self.kl_sum = torch.zeros(1, dtype=torch.float32, device=self.dev)
+            self.kl_rows = torch.zeros(T, dtype=torch.float32, device=self.dev)
+            self.n_valid = torch.zeros(1, dtype=torch.int32, device=self.dev)
+            self.ws = torch.empty(api.csa_indexer_kl_workspace(T), dtype=torch.uint8, device=self.dev)
+
+    # individual stages -----------------------------------------------------
+    def compress(self, stream=None):
+        wl, x = self.wl, self.x
+        api.csa_compressed_offsets(self.h, self.cu, wl.ratio, self.cu_cmp, stream)
+        api.csa_compress(self.h, x["x_kv"], x["z_kv"], x["P_kv"], self.cu, self.cu_cmp, self.max_seqlen,
+                         wl.ratio, wl.overlap, self.kv_cmp, stream)
+        if self.v_cmp is not None:
+            api.csa_compress(self.h, x["v"], x["z_kv"], x["P_kv"], self.cu, self.cu_cmp, self.max_seqlen,
+                             wl.ratio, wl.overlap, self.v_cmp, stream)
+        if wl.H_I > 0:
+            api.csa_compress(self.h, x["x_I"], x["z_I"], x["P_I"], self.cu, self.cu_cmp, self.max_seqlen,
+                             wl.ratio, wl.overlap, self.kI, stream)
+
+    def topk(self, stream=None):
+        wl, x = self.wl, self.x
+        api.csa_indexer_topk(self.h, x["qI"], x["w"], self.kI, self.cu, self.cu_cmp, self.max_seqlen, wl.ratio,
+                             wl.topk, self.idx, stream)
+
+    def attend(self, stream=None, sink=None):
+        wl, x = self.wl, self.x
+        v_raw = x.get("v") if wl.separate_v else None
+        if wl.ratio == 0:
+            api.window_attn_fwd(self.h, x["q"], x["x_kv"], self.cu, self.max_seqlen, wl.window, self.scale,
+                                self.out, self.lse, v_raw=v_raw, sink=sink, stream=stream)
+        elif wl.H_I > 0:
+            api.csa_sparse_attn_fwd(self.h, x["q"], self.kv_cmp, x["x_kv"], self.idx, self.cu, self.cu_cmp,
+                                    self.max_seqlen, wl.ratio, wl.window, self.scale, self.out, self.lse,
+                                    self.lse_cmp, v_cmp=self.v_cmp, v_raw=v_raw, sink=sink, stream=stream)
+        else:
+            api.hca_attn_fwd(self.h, x["q"], self.kv_cmp, x["x_kv"], self.cu, self.cu_cmp, self.max_seqlen,
+                             wl.ratio, wl.window, self.scale, self.out, self.lse, self.lse_cmp,
+                             v_cmp=self.v_cmp, v_raw=v_raw, sink=sink, stream=stream)
+
+    def kl(self, stream=None):
+        wl, x = self.wl, self.x
+        sparse = wl.kl_mode == "sparse"
+        api.csa_indexer_kl(self.h, x["q"], self.kv_cmp, x["qI"], x["w"], self.kI, self.cu, self.cu_cmp,
+                           self.max_seqlen, wl.ratio, self.scale, self.kl_sum, self.ws,
+                           idx=self.idx if sparse else None, lse_cmp=self.lse_cmp if sparse else None,
+                           kl_per_query=self.kl_rows, n_valid=self.n_valid, stream=stream)
+
+    def run(self, stream=None, sink=None):
+        """The whole hot path of one forward, enqueued on ``stream``."""
+        if self.wl.ratio > 0:
+            self.compress(stream)
+            if self.wl.H_I > 0:
+                self.topk(stream)
+        self.attend(stream, sink=sink)
+        if self.wl.kl_mode != "none":
+            self.kl(stream)
+
+
+def to_device(arrs: dict, io_fp32: bool, device: int = 0) -> dict:
+    """numpy float32 (bf16-valued) inputs -> device tensors in the I/O dtype."""
+    dev = torch.device("cuda", device)
+    out = {}
+    for k, v in arrs.items():
+        t = torch.from_numpy(v)
+        if k == "cu_seqlens":
+            out[k] = t.to(dev, torch.int32)
+        elif k.startswith("P_"):
+            out[k] = t.to(dev, torch.float32)
+        else:
+            out[k] = t.to(dev, torch.float32 if io_fp32 else torch.bfloat16)
+    return out

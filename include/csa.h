@@ -1,0 +1,206 @@
+/*
+ * csa.h -- C ABI of the GB300 (sm_103a) compressed sparse attention forward.
+ *
+ * The library computes the forward hot path of the DeepSeek-V4 compressed
+ * attention layers described on the page "DeepSeek-V4 Attention Training
+ * Systems" (Megatron V4 notes):
+ *   1. block compression of KV (ratio 4 overlapping for CSA, ratio 128 for HCA),
+ *   2. lightning-indexer scoring of every causally visible compressed entry and
+ *      a per-query top-k,
+ *   3. attention over the selected (CSA) or all visible (HCA) compressed
+ *      entries together with the local window of raw tokens, in one softmax,
+ *   4. the indexer KL auxiliary loss over the selected or the dense visible set.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Packing.  Tokens of B sequences are concatenated on one row axis (THD):
+ *   cu_seqlens[0..B] (int32, device) with cu_seqlens[0] = 0, non-decreasing,
+ *   cu_seqlens[B] <= T_cap.  Rows [cu_seqlens[B], T_cap) are capacity padding.
+ *   Nothing is compressed, attended or selected across a sequence boundary
+ *   (§4 "What Varlen Means In Megatron").
+ * Compression.  Sequence b of length L_b owns n_b = floor(L_b / r) compressed
+ *   entries (only complete groups, §4); cu_cmp[b] = sum of earlier n_b is the
+ *   first packed compressed row of sequence b (csa_compressed_offsets).  Entry j
+ *   is visible to local query position t once r(j+1)-1 <= t.
+ * Static capacity.  Buffers are sized for a fixed capacity and all metadata is
+ *   read on the device, so no call synchronises with the host (§4.1 "Static
+ *   capacity versus dynamic metadata").  Calls that need a bound on one
+ *   sequence's length take max_seqlen (host int, >= every L_b).
+ * Memory.  Every pointer is a device pointer unless stated.  The caller owns
+ *   every buffer; apart from csa_create the library never allocates or frees.
+ *   Arrays are dense row-major with the innermost dimension last; every array
+ *   pointer must be 16-byte aligned.
+ * Streams.  Every compute call only enqueues work on `stream` and returns.
+ * Data types.  CSA_BF16: bf16 activations in and out.  CSA_FP32: float32
+ *   arrays in and out; inputs are rounded to bf16 on load (the tensor-core
+ *   operand type), outputs are written as float32.  Positional biases, sinks,
+ *   LSE and KL values are always float32.
+ * Errors.  Argument problems that the host can see return a negative status
+ *   before anything is enqueued.  Problems only the device can see (an index
+ *   outside a query's visible entries, an inconsistent cu_seqlens, a wait that
+ *   ran out) set the handle's device status word and the offending element is
+ *   skipped; read it with csa_get_device_status.
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct csa_handle_s* csa_handle_t;
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = -1,   /* null pointer, misalignment, bad size */
+  CSA_ERR_UNSUPPORTED = -2,   /* a shape this build has no kernel for */
+  CSA_ERR_WORKSPACE = -3,     /* workspace missing or too small */
+  CSA_ERR_CUDA = -4,          /* a CUDA runtime call failed */
+  CSA_ERR_DEVICE_TIMEOUT = -5,/* a bounded device-side wait ran out */
+  CSA_ERR_DEVICE_BOUNDS = -6  /* an index or cu_seqlens value out of range */
+} csa_status_t;
+
+typedef enum { CSA_BF16 = 0, CSA_FP32 = 1 } csa_dtype_t;
+
+/* Create a handle on `device`: records device properties and allocates one
+ * int32 device status word (the only allocation the library makes).
+ * Returns CSA_ERR_INVALID_ARG for a null out pointer, CSA_ERR_CUDA when the
+ * device cannot be used. */
+csa_status_t csa_create(int device, csa_handle_t* out);
+
+/* Free the handle and its status word.  Null is accepted. */
+csa_status_t csa_destroy(csa_handle_t handle);
+
+/* Human-readable name of a status code (static string). */
+const char* csa_status_string(int status);
+
+/* Synchronise `stream`, read the device status word into *status (host
+ * pointer) and reset it to CSA_OK.  *status is CSA_OK or the first device
+ * error code raised since the last read. */
+csa_status_t csa_get_device_status(csa_handle_t handle, cudaStream_t stream, int* status);
+
+/* cu_cmp[b] = sum_{b'<b} floor(L_b' / ratio) for b = 0..B (int32, device),
+ * the packed compressed-row offsets (§4, complete groups only; §5.2 packed
+ * compressed buffer, sequence-major).  ratio 0 gives all zeros.
+ * Also checks cu_seqlens (cu[0] = 0, non-decreasing) and raises
+ * CSA_ERR_DEVICE_BOUNDS on the status word if it is not. */
+csa_status_t csa_compressed_offsets(csa_handle_t handle, const int32_t* cu_seqlens, int B,
+                                    int ratio, int32_t* cu_cmp, cudaStream_t stream);
+
+/* Learned-score block compression (§4 reset list, §5.1 spans D_compress = 8 for
+ * overlapping ratio 4 and 128 for ratio-128 HCA, §8.2 "C4/C128 compression",
+ * §9 FP32 compressor positional parameter).
+ *   x, z      [T_cap, D]  values and gate logits (dtype)
+ *   pos_bias  [S, D]      float32, S = 2*ratio (overlap = 1) or ratio
+ *   out       [cu_cmp[B], D] (dtype)
+ * Entry j of sequence b covers local tokens first .. first+S-1 with
+ * first = ratio*j + ratio - S; per channel c,
+ *   out[j,c] = sum_u softmax_u(z[t_u,c] + pos_bias[u,c]) * x[t_u,c]
+ * over the span positions u with t_u >= 0 (positions before the sequence start
+ * are left out).  The math is float32.  Rows of `out` past cu_cmp[B] are not
+ * written.  D in {32, 64, 128, 256}, ratio in 1..128, S <= 256. */
+csa_status_t csa_compress(csa_handle_t handle, const void* x, const void* z,
+                          const float* pos_bias, const int32_t* cu_seqlens,
+                          const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int D,
+                          int ratio, int overlap, csa_dtype_t dtype, void* out,
+                          cudaStream_t stream);
+
+/* Lightning-indexer scoring and per-query top-k (§3 indexer logit i_{t,j},
+ * §8 "indexer scoring and radix top-k", §8.1 top-k padding, §8.2 flat global
+ * index list).  For every packed query row t of sequence b:
+ *   i_{t,j} = sum_h w[t,h] * ReLU(qI[t,h,:] . kI[cu_cmp[b]+j,:]),  j < |V_t|
+ * and idx[t, 0..m) holds the m = min(topk, |V_t|) entries with the largest
+ * i_{t,j} (ties: smaller j first) as global compressed rows cu_cmp[b]+j in
+ * ascending order; idx[t, m..k_pad) = -1.  Capacity rows get all -1.
+ * Scores stay in shared memory; nothing but idx is written.
+ *   qI [T_cap, H_I, d_I], w [T_cap, H_I], kI [cu_cmp[B], d_I]   (dtype)
+ *   idx [T_cap, k_pad] int32
+ * H_I in {1,2,4,8}, d_I in {32,64}, 1 <= topk <= k_pad <= 8192, ratio >= 1,
+ * max_seqlen / ratio <= 16384. */
+csa_status_t csa_indexer_topk(csa_handle_t handle, const void* qI, const void* w,
+                              const void* kI, const int32_t* cu_seqlens,
+                              const int32_t* cu_cmp, int B, int T_cap, int max_seqlen,
+                              int H_I, int d_I, int ratio, int topk, int k_pad,
+                              csa_dtype_t dtype, int32_t* idx, cudaStream_t stream);
+
+/* Selected-entry attention forward, CSA (§2 phase table "top-k compressed
+ * entries + local window", §8.2 selected MQA attention returning output and
+ * LSE, compressed ids combined with window ids, §9 FP32 attention sink).
+ * One shared KV head; for query row t of sequence b and head h the candidate
+ * keys are the valid entries of idx[t,:] (global compressed rows; -1 skipped)
+ * followed by the window rows cu[b]+s, s in [max(0, t-window+1), t].
+ *   s_i = softmax_scale * q[t,h,:] . K_i
+ *   out[t,h,:] = sum_i softmax_i(s_i; sink_h) V_i,  lse[t,h] = log(sum_i e^{s_i} + e^{sink_h})
+ *   lse_cmp[t,h] = logsumexp of s_i over the compressed candidates only (no
+ *   window, no sink), -inf when there are none.
+ *   q [T_cap, H, d], kv_cmp [., d], kv_raw [T_cap, d]          (dtype)
+ *   v_cmp / v_raw: separate value rows, or NULL for K = V
+ *   sink [H] float32 or NULL; lse [T_cap, H], lse_cmp [T_cap, H] or NULL (float32)
+ * Capacity rows: out = 0, lse = lse_cmp = -inf.  An idx entry outside the
+ * query's visible entries raises CSA_ERR_DEVICE_BOUNDS and is skipped.
+ * d in {64, 128}, H in {4, 8, 16, 32, 64, 128}, window >= 1, ratio >= 1. */
+csa_status_t csa_sparse_attn_fwd(csa_handle_t handle, const void* q, const void* kv_cmp,
+                                 const void* v_cmp, const void* kv_raw, const void* v_raw,
+                                 const int32_t* idx, int k_pad, const float* sink,
+                                 const int32_t* cu_seqlens, const int32_t* cu_cmp, int B,
+                                 int T_cap, int max_seqlen, int H, int d, int ratio, int window,
+                                 float softmax_scale, csa_dtype_t dtype, void* out, float* lse,
+                                 float* lse_cmp, cudaStream_t stream);
+
+/* HCA attention forward (§2 "HCA has no indexer: it always reads every
+ * completed ratio-128 compressed entry plus the local window", §5.3).  As
+ * csa_sparse_attn_fwd with the compressed candidates = every visible entry
+ * cu_cmp[b] .. cu_cmp[b]+|V_t|-1.  Same layouts, limits and outputs. */
+csa_status_t hca_attn_fwd(csa_handle_t handle, const void* q, const void* kv_cmp,
+                          const void* v_cmp, const void* kv_raw, const void* v_raw,
+                          const float* sink, const int32_t* cu_seqlens, const int32_t* cu_cmp,
+                          int B, int T_cap, int max_seqlen, int H, int d, int ratio, int window,
+                          float softmax_scale, csa_dtype_t dtype, void* out, float* lse,
+                          float* lse_cmp, cudaStream_t stream);
+
+/* Window-only attention forward (ratio 0 layers: no compressor, no indexer;
+ * §2, §5.3).  Candidate keys are the window rows only.  lse_cmp is not
+ * produced.  Same layouts and limits as csa_sparse_attn_fwd. */
+csa_status_t window_attn_fwd(csa_handle_t handle, const void* q, const void* kv_raw,
+                             const void* v_raw, const float* sink, const int32_t* cu_seqlens,
+                             int B, int T_cap, int max_seqlen, int H, int d, int window,
+                             float softmax_scale, csa_dtype_t dtype, void* out, float* lse,
+                             cudaStream_t stream);
+
+/* Indexer KL auxiliary loss (§3 equation
+ *   L_I = sum_t KL(Softmax(a_{t,C_t}) || Softmax(i_{t,C_t})),
+ * §2 phase table: dense teacher over every visible entry in the sparse
+ * warm-up, selected-set teacher in sparse mode; §9 FP32 loss math).
+ *   C_t     = valid entries of idx[t,:] (idx != NULL) or every visible entry
+ *   pi_h(j) = softmax over C_t of softmax_scale * q[t,h,:] . kv_cmp[j,:]
+ *   p(j)    = (1/H) sum_h pi_h(j)          (teacher; a_{t,j} = log p(j))
+ *   q(j)    = softmax over C_t of i_{t,j}  (indexer logits as in csa_indexer_topk)
+ *   kl_per_query[t] = sum_j p(j) (log p(j) - log q(j)), 0 when C_t is empty
+ *   kl_sum[0]  = sum over rows of kl_per_query (float32, fixed summation order)
+ *   n_valid[0] = number of rows with a non-empty C_t
+ * lse_cmp (sparse mode only, may be NULL): the per-head log normaliser over
+ * C_t from csa_sparse_attn_fwd; when given, the teacher takes one pass over
+ * C_t instead of two.  kl_per_query and n_valid may be NULL.
+ * ws/ws_bytes: device scratch of at least csa_indexer_kl_workspace(T_cap)
+ * bytes (per-query partial results); CSA_ERR_WORKSPACE otherwise.
+ * Same layouts as csa_indexer_topk / csa_sparse_attn_fwd. */
+csa_status_t csa_indexer_kl(csa_handle_t handle, const void* q, const void* kv_cmp,
+                            const void* qI, const void* w, const void* kI, const int32_t* idx,
+                            int k_pad, const float* lse_cmp, const int32_t* cu_seqlens,
+                            const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H,
+                            int d, int H_I, int d_I, int ratio, float softmax_scale,
+                            csa_dtype_t dtype, float* kl_sum, float* kl_per_query,
+                            int32_t* n_valid, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Scratch bytes csa_indexer_kl needs for T_cap packed rows. */
+size_t csa_indexer_kl_workspace(int T_cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H_ */
