@@ -76,11 +76,13 @@ attention_kernel(int kind, const TIn* __restrict__ q, const TIn* __restrict__ k_
     *reinterpret_cast<uint4*>(sQ + h * kStride + c * 8) = v;
   }
 
+  const int cmp_limit = (kind == kAttnWindow) ? 0 : __ldg(cu_cmp + B);  // packed compressed rows
+  const int raw_limit = __ldg(cu + B);                                    // packed raw rows
   auto resolve = [&](int it, int buf) {
-    if (tid < kKeys) {
+    for (int kk = tid; kk < kKeys; kk += NW * 32) {
       int rr = -1;
       if (it < n_ctiles) {
-        const int slot = it * kKeys + tid;
+        const int slot = it * kKeys + kk;
         if (kind == kAttnCSA) {
           if (slot < k_pad) {
             const int g = __ldg(idx + (int64_t)row * k_pad + slot);
@@ -93,15 +95,15 @@ attention_kernel(int kind, const TIn* __restrict__ q, const TIn* __restrict__ k_
           rr = cmp0 + slot;
         }
       } else {
-        const int wi = (it - n_ctiles) * kKeys + tid;
+        const int wi = (it - n_ctiles) * kKeys + kk;
         if (wi < n_win) rr = seq0 + w0 + wi;
       }
-      s_rows[buf][tid] = rr;
+      s_rows[buf][kk] = rr;
     }
   };
   auto issue = [&](int it, int buf) {
     const bool cmp = it < n_ctiles;
-    gather_tile<TIn, D>(cmp ? k_cmp : k_raw, cmp ? vc : vr, separate_v, s_rows[buf],
+    gather_tile<TIn, D>(cmp ? k_cmp : k_raw, cmp ? vc : vr, separate_v, s_rows[buf], cmp ? cmp_limit : raw_limit,
                         sK + buf * kKeys * kStride, sV + buf * kKeys * kStride, tid, NW * 32);
   };
 

@@ -73,11 +73,12 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
   }
   if (tid < 8) sW[tid] = tid < H_I ? to_f32(w[(int64_t)row * H_I + tid]) : 0.f;
 
-  int count = 0;  // |C_t| seen by thread 0 .. kKeys-1 (summed at the end)
+  int count = 0;  // |C_t| entries resolved by this thread (summed at the end)
+  const int cmp_limit = __ldg(cu_cmp + B);
   auto resolve = [&](int it, int buf, bool tally) {
-    if (tid < kKeys) {
+    for (int kk = tid; kk < kKeys; kk += kThreads) {
       int rr = -1;
-      const int slot = it * kKeys + tid;
+      const int slot = it * kKeys + kk;
       if (dense) {
         if (slot < nvis) rr = cmp0 + slot;
       } else if (slot < k_pad) {
@@ -87,17 +88,18 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
           else rr = g;
         }
       }
-      s_rows[buf][tid] = rr;
+      s_rows[buf][kk] = rr;
       if (tally && rr >= 0) ++count;
     }
   };
   auto issue = [&](int buf, bool with_ki) {
-    gather_tile<TIn, D>(k_cmp, k_cmp, false, s_rows[buf], sK + buf * kKeys * kStride, nullptr, tid, kThreads);
+    gather_tile<TIn, D>(k_cmp, k_cmp, false, s_rows[buf], cmp_limit, sK + buf * kKeys * kStride, nullptr, tid,
+                        kThreads);
     if (with_ki) {
       // indexer key rows: DI bf16 = DI/8 chunks per row
       for (int i = tid; i < kKeys * (DI / 8); i += kThreads) {
         const int k = i / (DI / 8), c = i - k * (DI / 8);
-        const int rr = s_rows[buf][k];
+        const int rr = s_rows[buf][k] < cmp_limit ? s_rows[buf][k] : -1;
         __nv_bfloat16* dst = sKI + (buf * kKeys + k) * DI + c * 8;
         if constexpr (sizeof(TIn) == 2) {
           cp_async_16_zfill(smem_u32(dst), kI + (int64_t)(rr < 0 ? 0 : rr) * DI + c * 8, rr >= 0);
@@ -217,13 +219,14 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
       }
     }
     __syncthreads();
-    if (tid < kKeys && s_rows[buf][tid] >= 0) {
+    for (int kk = tid; kk < kKeys; kk += kThreads) {
+      if (s_rows[buf][kk] < 0) continue;
       float p = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < NW; ++ww) p += sPsum[ww * kKeys + tid];
+      for (int ww = 0; ww < NW; ++ww) p += sPsum[ww * kKeys + kk];
       p *= inv_h;
       float il = 0.f;
-      for (int h = 0; h < 8; ++h) il += sRed[h * kKeys + tid];
+      for (int h = 0; h < 8; ++h) il += sRed[h * kKeys + kk];
       if (p > 0.f) accA += p * __logf(p);
       accB = fmaf(p, il, accB);
       if (il > mi) { li = li * __expf(mi - il) + 1.f; mi = il; }
@@ -231,28 +234,25 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
     }
     __syncthreads();
   }
-  // block reduction (threads < kKeys hold partials)
-  if (tid < kKeys) {
-    int cnt = count;
-    sRed[tid] = accA;
-    sRed[kKeys + tid] = accB;
-    sRed[2 * kKeys + tid] = mi;
-    sRed[3 * kKeys + tid] = li;
-    reinterpret_cast<int*>(sPsum)[tid] = cnt;
-  }
+  // block reduction of the per-thread partials (kThreads <= 256 entries each)
+  sRed[tid] = accA;
+  sRed[kThreads + tid] = accB;
+  sRed[2 * kThreads + tid] = mi;
+  sRed[3 * kThreads + tid] = li;
+  reinterpret_cast<int*>(sPsum)[tid] = count;
   __syncthreads();
   if (tid == 0) {
     float A = 0.f, Bs = 0.f, M = -INFINITY;
     int n = 0;
-    for (int k = 0; k < kKeys; ++k) {
+    for (int k = 0; k < kThreads; ++k) {
       A += sRed[k];
-      Bs += sRed[kKeys + k];
-      M = fmaxf(M, sRed[2 * kKeys + k]);
+      Bs += sRed[kThreads + k];
+      M = fmaxf(M, sRed[2 * kThreads + k]);
       n += reinterpret_cast<int*>(sPsum)[k];
     }
     float Ls = 0.f;
-    for (int k = 0; k < kKeys; ++k)
-      if (sRed[2 * kKeys + k] != -INFINITY) Ls += sRed[3 * kKeys + k] * __expf(sRed[2 * kKeys + k] - M);
+    for (int k = 0; k < kThreads; ++k)
+      if (sRed[2 * kThreads + k] != -INFINITY) Ls += sRed[3 * kThreads + k] * __expf(sRed[2 * kThreads + k] - M);
     const float kl = n > 0 ? A - Bs + (M + __logf(Ls)) : 0.f;
     kl_rows[row] = kl;
     csize[row] = n;

@@ -16,15 +16,17 @@ struct AttnSmem {
 
 // Gather one tile of key (and value) rows into shared memory.  rows[k] < 0
 // leaves zeros.  bf16 sources use cp.async; float sources are converted.
+// rows outside [0, row_limit) are treated like -1 (zeros), so a bad row
+// number can never turn into an out-of-bounds load.
 template <typename TIn, int D>
 __device__ __forceinline__ void gather_tile(const TIn* __restrict__ ksrc, const TIn* __restrict__ vsrc,
-                                            bool separate_v, const int* rows, __nv_bfloat16* sk,
+                                            bool separate_v, const int* rows, int row_limit, __nv_bfloat16* sk,
                                             __nv_bfloat16* sv, int tid, int nthreads) {
   constexpr int kChunks = D / 8;  // 16-byte chunks per bf16 row
   constexpr int kStride = AttnSmem<D>::kStride;
   for (int i = tid; i < kKeys * kChunks; i += nthreads) {
     const int k = i / kChunks, c = i - k * kChunks;
-    const int row = rows[k];
+    const int row = rows[k] < row_limit ? rows[k] : -1;
     __nv_bfloat16* dk = sk + k * kStride + c * 8;
     __nv_bfloat16* dv = sv + k * kStride + c * 8;
     if constexpr (sizeof(TIn) == 2) {
