@@ -14,6 +14,7 @@ import numpy as np
 import torch
 
 import oracle
+from compressed_sparse_attention_compress_gb300.inputs import bf16_round
 
 ATOL = 1e-2
 TIE_RTOL = 1e-4
@@ -22,6 +23,12 @@ KL_RTOL = 1e-3
 
 def np32(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy()
+
+
+def operand(t: torch.Tensor) -> np.ndarray:
+    """A GPU intermediate as the next kernel consumes it: rounded to bf16 on load
+    (a no-op for bf16 tensors; float32 I/O rounds its compressed rows)."""
+    return bf16_round(np32(t))
 
 
 def check_compress(gpu_out: torch.Tensor, x, z, P, cu, ratio, overlap, n_c):

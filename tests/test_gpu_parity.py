@@ -43,11 +43,11 @@ def _check_all(f, arrs, wl, rows=None, sink=None, kl_full=True):
         assert np.array_equal(cu_cmp, oracle.compressed_offsets(cu, wl.ratio))
         n_c = int(cu_cmp[-1])
         ph.check_compress(f.kv_cmp, arrs["x_kv"], arrs["z_kv"], arrs["P_kv"], cu, wl.ratio, wl.overlap, n_c)
-        kv_cmp = ph.np32(f.kv_cmp[:n_c])
+        kv_cmp = ph.operand(f.kv_cmp[:n_c])
         v_cmp = None
         if wl.separate_v:
             ph.check_compress(f.v_cmp, arrs["v"], arrs["z_kv"], arrs["P_kv"], cu, wl.ratio, wl.overlap, n_c)
-            v_cmp = ph.np32(f.v_cmp[:n_c])
+            v_cmp = ph.operand(f.v_cmp[:n_c])
     v_raw = arrs.get("v") if wl.separate_v else None
     if wl.ratio == 0:
         ph.check_attention(oracle.KIND_WINDOW, f.out, f.lse, None, arrs["q"], None, None, arrs["x_kv"], v_raw,
@@ -55,7 +55,7 @@ def _check_all(f, arrs, wl, rows=None, sink=None, kl_full=True):
         return
     if wl.H_I > 0:
         ph.check_compress(f.kI, arrs["x_I"], arrs["z_I"], arrs["P_I"], cu, wl.ratio, wl.overlap, n_c)
-        kI = ph.np32(f.kI[:n_c])
+        kI = ph.operand(f.kI[:n_c])
         idx = f.idx.cpu().numpy()
         ph.check_topk(idx, arrs["qI"], arrs["w"], kI, cu, wl.ratio, wl.topk, rows)
         ph.check_attention(oracle.KIND_CSA, f.out, f.lse, f.lse_cmp, arrs["q"], kv_cmp, v_cmp, arrs["x_kv"],
