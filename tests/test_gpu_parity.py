@@ -152,7 +152,7 @@ def test_host_side_argument_errors():
         api.window_attn_fwd(h, q, x, cu, 64, 16, 0.1, torch.empty_like(q), torch.empty(64, 64, device="cuda"))
     assert e.value.code == -2
     q = torch.zeros(64, 64, 128, dtype=torch.bfloat16, device="cuda")
-    kv = torch.zeros(64 * 128 + 8, dtype=torch.bfloat16, device="cuda")[8:].view(64, 128)  # misaligned
+    kv = torch.zeros(64 * 128 + 1, dtype=torch.bfloat16, device="cuda")[1:].view(64, 128)  # 2-byte offset
     with pytest.raises(api.CSAError) as e:
         api.window_attn_fwd(h, q, kv, cu, 64, 16, 0.1, torch.empty_like(q), torch.empty(64, 64, device="cuda"))
     assert e.value.code == -1
