@@ -53,6 +53,7 @@ def _load():
         "hca_attn_fwd": [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P],
         "window_attn_fwd": [P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P],
         "csa_indexer_kl": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, P, Z, P],
+        "csa_indexer_kl_static_scratch": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -190,3 +191,17 @@ def csa_indexer_kl(h: Handle, q, kv_cmp, qI, w, kI, cu_seqlens, cu_cmp, max_seql
         _p(cu_cmp), cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H, d, H_I, d_I, int(ratio),
         float(softmax_scale), _dtype(q), _p(kl_sum), _p(kl_per_query), _p(n_valid), _p(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def csa_indexer_kl_static_scratch(h: Handle, q, kv_cmp, qI, w, kI, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int,
+                                  softmax_scale: float, kl_sum, idx=None, lse_cmp=None, kl_per_query=None,
+                                  n_valid=None, stream=None):
+    """csa_indexer_kl without a workspace argument: the library's own static
+    device scratch is used (for callers that cannot allocate device memory)."""
+    T_cap, H, d = q.shape
+    _, H_I, d_I = qI.shape
+    k_pad = idx.shape[1] if idx is not None else 0
+    return _check("csa_indexer_kl_static_scratch", LIB.csa_indexer_kl_static_scratch(
+        h.ptr, _p(q), _p(kv_cmp), _p(qI), _p(w), _p(kI), _p(idx), k_pad, _p(lse_cmp), _p(cu_seqlens),
+        _p(cu_cmp), cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H, d, H_I, d_I, int(ratio),
+        float(softmax_scale), _dtype(q), _p(kl_sum), _p(kl_per_query), _p(n_valid), _stream(stream)))

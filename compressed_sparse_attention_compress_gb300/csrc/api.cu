@@ -220,3 +220,8 @@ csa_status_t csa_indexer_kl(csa_handle_t h, const void* q, const void* kv_cmp, c
 }
 
 }  // extern "C"
+
+namespace csa {
+// Device of a handle (for entry points defined in other translation units).
+int handle_device(csa_handle_t h) { return h->device; }
+}  // namespace csa

@@ -199,6 +199,30 @@ csa_status_t csa_indexer_kl(csa_handle_t handle, const void* q, const void* kv_c
 /* Scratch bytes csa_indexer_kl needs for T_cap packed rows. */
 size_t csa_indexer_kl_workspace(int T_cap);
 
+/* csa_indexer_kl for callers that cannot allocate device memory (no
+ * counterpart on the page: it is a deployment convenience).  Some callers
+ * cannot provide a workspace -- code whose device memory is owned entirely by
+ * a host framework or captured into a graph it does not control, processes
+ * that forbid allocations after start-up.  This variant takes the same
+ * arguments minus ws/ws_bytes and uses a fixed 2 MiB scratch array that lives
+ * in the library's device image (held on every GPU that loads the library
+ * until the process exits).  It makes no allocation of any kind.
+ *   - T_cap must be <= 262144; larger returns CSA_ERR_WORKSPACE.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Calls share the array: calls that overlap on the GPU race on it, so the
+ *     caller serialises them.  Each call writes every scratch element it
+ *     reads, so leftover contents from an earlier call are never used.
+ * Results are identical to csa_indexer_kl with a caller workspace. */
+csa_status_t csa_indexer_kl_static_scratch(csa_handle_t handle, const void* q, const void* kv_cmp,
+                                           const void* qI, const void* w, const void* kI,
+                                           const int32_t* idx, int k_pad, const float* lse_cmp,
+                                           const int32_t* cu_seqlens, const int32_t* cu_cmp, int B,
+                                           int T_cap, int max_seqlen, int H, int d, int H_I, int d_I,
+                                           int ratio, float softmax_scale, csa_dtype_t dtype,
+                                           float* kl_sum, float* kl_per_query, int32_t* n_valid,
+                                           cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
