@@ -9,10 +9,16 @@
 
 namespace csa {
 
-// Upper bound on the polls of one bounded wait (mbarrier phase, flag).  A wait
-// that runs out raises CSA_ERR_DEVICE_TIMEOUT on the status word and the
-// caller gives up on its tile instead of spinning forever.
-constexpr uint32_t kMaxPolls = 1u << 26;
+// A bounded wait gives up after this long (nanoseconds of %globaltimer),
+// raises CSA_ERR_DEVICE_TIMEOUT on the status word and lets the caller abandon
+// its work instead of spinning forever.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ void raise_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
@@ -104,12 +110,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for phase `parity` of the barrier; false (and the status word set)
-// when the poll budget runs out.
+// when the time limit runs out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* status) {
-  for (uint32_t i = 0; i < kMaxPolls; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  raise_status(status, CSA_ERR_DEVICE_TIMEOUT);
-  return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      raise_status(status, CSA_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // Bulk (non-tensor) asynchronous copy global -> shared, completing on an

@@ -2,7 +2,9 @@
 the oracle stage by stage, compare within the tolerances the method fixes.
 
 Tolerances (bf16 inputs, fp32 accumulation):
-  compress / attention outputs / lse : max-abs 1e-2 against the fp64 oracle
+  compress / attention outputs / lse : max-abs 1e-2 against the fp64 oracle; a
+                                       bf16 output is also allowed the half-ulp
+                                       of its own storage rounding
   top-k index sets                   : bit-exact, except entries whose oracle
                                        score lies within 1e-4 relative of the
                                        oracle's k-th score (near-ties)
@@ -31,10 +33,18 @@ def operand(t: torch.Tensor) -> np.ndarray:
     return bf16_round(np32(t))
 
 
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 values at |x| (the largest round-to-nearest error)."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return np.ldexp(1.0, (e - 8).astype(np.int64))
+
+
 def check_compress(gpu_out: torch.Tensor, x, z, P, cu, ratio, overlap, n_c):
     ref = oracle.compress(x, z, P, cu, ratio, overlap)
     got = np32(gpu_out[:n_c]).astype(np.float64)
-    err = np.abs(got - ref).max() if ref.size else 0.0
+    quant = bf16_half_ulp(ref) if gpu_out.dtype == torch.bfloat16 else 0.0
+    err = (np.abs(got - ref) - quant).max() if ref.size else 0.0
     assert err <= ATOL, f"compress max-abs {err}"
     return err
 
@@ -74,7 +84,10 @@ def check_attention(kind, out, lse, lse_cmp, q, k_cmp, v_cmp, k_raw, v_raw, cu, 
                                                      scale, idx=idx, sink=sink, rows=rows)
     assert not err.any(), "oracle saw out-of-range indices"
     o = np32(out[rows]).astype(np.float64)
-    e_o = np.abs(o - o_ref).max()
+    # a bf16 output cannot be closer to the exact value than half a bf16 ulp:
+    # the tolerance applies to the fp32-accumulated value before that rounding
+    quant = bf16_half_ulp(o_ref) if out.dtype == torch.bfloat16 else 0.0
+    e_o = (np.abs(o - o_ref) - quant).max()
     l = np32(lse[rows]).astype(np.float64)
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(l), fin), "lse finiteness differs"
