@@ -326,6 +326,13 @@ static cudaError_t kl_di(const KLArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_indexer_kl(const KLArgs& a, bool fp32, cudaStream_t stream) {
+  // the dense teacher at 64 x 128 heads / 8 x 64 indexer (bf16) runs on tcgen05 with TMA-fed tiles
+  if (indexer_kl_dense_tc_supported(a, fp32)) {
+    cudaError_t err = launch_indexer_kl_dense_tc(a, stream);
+    if (err != cudaSuccess) return err;
+    kl_finalize_kernel<<<1, 1024, 0, stream>>>(a.kl_rows, a.csize, a.T_cap, a.kl_sum, a.n_valid);
+    return cudaGetLastError();
+  }
   if (fp32) return a.d == 64 ? kl_di<float, 64>(a, stream) : kl_di<float, 128>(a, stream);
   return a.d == 64 ? kl_di<__nv_bfloat16, 64>(a, stream) : kl_di<__nv_bfloat16, 128>(a, stream);
 }

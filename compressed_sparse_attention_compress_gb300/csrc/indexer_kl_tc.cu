@@ -1,0 +1,428 @@
+// indexer_kl_tc.cu -- the dense-teacher indexer KL loss on tcgen05 tensor
+// cores with TMA-fed tiles (64 heads x 128 dims, indexer 8 x 64, bf16).
+//
+// "DeepSeek-V4 Attention Training Systems": §3 (L_I = sum_t KL(Softmax(a_{t,C_t})
+// || Softmax(i_{t,C_t})) with C_t the full visible compressed history in the
+// dense-loss phase), §2 phase table (the sparse warm-up's teacher is ~O(L^2/4)
+// score work), §8.2 (dense teacher scores recomputed for the loss), §9 (FP32
+// loss math).
+//
+// In the dense phase C_t is every visible entry, a prefix of the sequence's
+// compressed rows, so consecutive queries share their keys: one CTA takes a
+// block of 4 queries (4 x 64 = 256 query-head rows) and streams the key prefix
+// through shared memory with TMA tiled loads (128 keys x 128 dims, 128-byte
+// swizzle), each tile feeding 256 rows of tensor-core work.
+//   pass 1  S = Q K^T   (two M=128 tiles of query-head rows, N=128 keys):
+//           one thread per row keeps the row's online log-sum-exp -> lse_h.
+//   pass 2  S^T = K Q^T (M=128 keys, N=256 query-heads) and the indexer tile
+//           I^T = kI qI^T (M=128 keys, N=32 = 4 queries x 8 heads): one thread
+//           per key forms, for two queries, p(j) = mean_h exp(s_h - lse_h), the
+//           indexer logit i = sum_h w_h ReLU(.), and accumulates sum p ln p,
+//           sum p i and the student's log-sum-exp;  KL = sum p ln p - sum p i + lse_i.
+// Warp roles: warps 0-7 compute (two warpgroups, one tensor-memory lane per
+// thread), warp 8 issues the TMA loads, warp 9 allocates tensor memory and
+// issues the MMAs.  Threads copy each score tile to registers and release it
+// at once, so the next tile's MMAs overlap the arithmetic.
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tcgen05.cuh"
+#include "tma.cuh"
+
+namespace csa {
+
+namespace {
+
+constexpr int kQB = 4;          // queries per block
+constexpr int kNH = 64;         // heads
+constexpr int kDim = 128;       // head dim
+constexpr int kHI = 8;          // indexer heads
+constexpr int kDI = 64;         // indexer head dim
+constexpr int kTK = 128;        // keys per tile
+constexpr int kStages = 3;
+constexpr int kComputeThreads = 256;
+constexpr int kThreads = kComputeThreads + 64;
+
+constexpr uint32_t kQRegion = kQB * kNH * 128;       // 32 KB: 256 rows x 64 dims
+constexpr uint32_t kQOff = 0;
+constexpr uint32_t kQIOff = 2 * kQRegion;            // 4 KB: 32 rows x 64 dims
+constexpr uint32_t kKRegion = kTK * 128;             // 16 KB
+constexpr uint32_t kStageK = 2 * kKRegion;           // 32 KB
+constexpr uint32_t kStageBytes = kStageK + kKRegion; // + kI tile (16 KB)
+constexpr uint32_t kStageOff = kQIOff + 4096;        // 1024-aligned
+constexpr uint32_t kSmemBytes = kStageOff + kStages * kStageBytes;
+static_assert(kStageOff % 1024 == 0, "stage alignment");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColI = 256;  // indexer tile columns in pass 2
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct Block {
+  int b, q0, nq, seq0, cmp0, nvis_max, ntiles;
+};
+
+// Blocks of kQB consecutive queries of one sequence, handed out heaviest
+// (latest in the buffer) first.  Block k counts from the end.
+__device__ __forceinline__ bool block_of(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_cmp, int B,
+                                         int r, int total, int k, Block& out) {
+  int c = total - 1 - k;
+  for (int bb = 0; bb < B; ++bb) {
+    const int L = max(0, __ldg(cu + bb + 1) - __ldg(cu + bb));
+    const int nb = (L + kQB - 1) / kQB;
+    if (c < nb) {
+      out.b = bb;
+      out.q0 = c * kQB;
+      out.nq = min(kQB, L - c * kQB);
+      out.seq0 = __ldg(cu + bb);
+      out.cmp0 = __ldg(cu_cmp + bb);
+      out.nvis_max = (out.q0 + out.nq) / r;
+      out.ntiles = (out.nvis_max + kTK - 1) / kTK;
+      return true;
+    }
+    c -= nb;
+  }
+  return false;
+}
+
+__device__ __forceinline__ int total_blocks(const int32_t* __restrict__ cu, int B) {
+  int n = 0;
+  for (int bb = 0; bb < B; ++bb) n += (max(0, __ldg(cu + bb + 1) - __ldg(cu + bb)) + kQB - 1) / kQB;
+  return n;
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                           const __grid_constant__ CUtensorMap map_qi, const __grid_constant__ CUtensorMap map_ki,
+                           const __nv_bfloat16* __restrict__ w, const int32_t* __restrict__ cu,
+                           const int32_t* __restrict__ cu_cmp, int B, int r, float scale_log2,
+                           float* __restrict__ kl_rows, int32_t* __restrict__ csize, int* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
+  __shared__ __align__(8) uint64_t s_sfull, s_sfree, s_qfull, s_qempty;
+  __shared__ float s_L[kQB][kNH];        // per (query, head) log2 normaliser over C_t
+  __shared__ float s_w[kQB][kHI];
+  __shared__ float s_red[8][2][4];       // per compute warp, per query: A, B, mI, lI
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t bar_full = smem_u32(&s_full[0]), bar_empty = smem_u32(&s_empty[0]);
+  const uint32_t bar_sfull = smem_u32(&s_sfull), bar_sfree = smem_u32(&s_sfree);
+  const uint32_t bar_qfull = smem_u32(&s_qfull), bar_qempty = smem_u32(&s_qempty);
+
+  if (warp == 9) {
+    tc::tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_sfull, 1);
+    mbar_init(bar_sfree, 8);  // one arrival per compute warp
+    mbar_init(bar_qfull, 1);
+    mbar_init(bar_qempty, 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  const int total = total_blocks(cu, B);
+
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_qi);
+      tma_prefetch_map(&map_ki);
+      uint32_t it = 0, nblk = 0;
+      for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
+        Block bk;
+        if (!block_of(cu, cu_cmp, B, r, total, k, bk) || bk.ntiles == 0) continue;
+        if (!mbar_wait_bounded(bar_qempty, (nblk & 1u) ^ 1u, status)) { s_abort = 1; break; }
+        ++nblk;
+        mbar_arrive_expect_tx(bar_qfull, 2 * kQRegion + kQB * kHI * 128);
+        for (int rg = 0; rg < 2; ++rg)
+          for (int m = 0; m < 2; ++m)
+            tma_load_2d(base + kQOff + rg * kQRegion + m * 16384, &map_q, rg * 64, (bk.seq0 + bk.q0) * kNH + m * 128,
+                        bar_qfull);
+        tma_load_2d(base + kQIOff, &map_qi, 0, (bk.seq0 + bk.q0) * kHI, bar_qfull);
+        for (int pass = 0; pass < 2; ++pass) {
+          for (int i = 0; i < bk.ntiles; ++i, ++it) {
+            const uint32_t s = it % kStages;
+            if (!mbar_wait_bounded(bar_empty + 8 * s, ((it / kStages) & 1u) ^ 1u, status)) { s_abort = 1; break; }
+            const uint32_t st = base + kStageOff + s * kStageBytes;
+            mbar_arrive_expect_tx(bar_full + 8 * s, pass == 0 ? kStageK : kStageBytes);
+            tma_load_2d(st, &map_k, 0, bk.cmp0 + i * kTK, bar_full + 8 * s);
+            tma_load_2d(st + kKRegion, &map_k, 64, bk.cmp0 + i * kTK, bar_full + 8 * s);
+            if (pass == 1) tma_load_2d(st + kStageK, &map_ki, 0, bk.cmp0 + i * kTK, bar_full + 8 * s);
+          }
+          if (s_abort) break;
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t kIdP1 = tc::idesc_bf16(128, kTK, 0, 0);
+      constexpr uint32_t kIdP2 = tc::idesc_bf16(kTK, kQB * kNH, 0, 0);
+      constexpr uint32_t kIdI = tc::idesc_bf16(kTK, kQB * kHI, 0, 0);
+      uint32_t it = 0, nblk = 0;
+      for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
+        Block bk;
+        if (!block_of(cu, cu_cmp, B, r, total, k, bk) || bk.ntiles == 0) continue;
+        if (!mbar_wait_bounded(bar_qfull, nblk & 1u, status)) { s_abort = 1; break; }
+        ++nblk;
+        for (int pass = 0; pass < 2; ++pass) {
+          for (int i = 0; i < bk.ntiles; ++i, ++it) {
+            const uint32_t s = it % kStages;
+            if (!mbar_wait_bounded(bar_full + 8 * s, (it / kStages) & 1u, status) ||
+                !mbar_wait_bounded(bar_sfree, (it & 1u) ^ 1u, status)) {
+              s_abort = 1;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t st = base + kStageOff + s * kStageBytes;
+            if (pass == 0) {
+#pragma unroll
+              for (int g = 0; g < 2; ++g)
+#pragma unroll
+                for (int ks = 0; ks < kDim / 16; ++ks) {
+                  const uint64_t a = tc::smem_desc_sw128(base + kQOff + (ks >> 2) * kQRegion + g * 16384 + (ks & 3) * 32,
+                                                         16, 1024);
+                  const uint64_t bd = tc::smem_desc_sw128(st + (ks >> 2) * kKRegion + (ks & 3) * 32, 16, 1024);
+                  tc::mma_bf16(tmem + g * kTK, a, bd, kIdP1, ks > 0 ? 1u : 0u);
+                }
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < kDim / 16; ++ks) {
+                const uint64_t a = tc::smem_desc_sw128(st + (ks >> 2) * kKRegion + (ks & 3) * 32, 16, 1024);
+                const uint64_t bd = tc::smem_desc_sw128(base + kQOff + (ks >> 2) * kQRegion + (ks & 3) * 32, 16, 1024);
+                tc::mma_bf16(tmem, a, bd, kIdP2, ks > 0 ? 1u : 0u);
+              }
+#pragma unroll
+              for (int ks = 0; ks < kDI / 16; ++ks) {
+                const uint64_t a = tc::smem_desc_sw128(st + kStageK + ks * 32, 16, 1024);
+                const uint64_t bd = tc::smem_desc_sw128(base + kQIOff + ks * 32, 16, 1024);
+                tc::mma_bf16(tmem + kColI, a, bd, kIdI, ks > 0 ? 1u : 0u);
+              }
+            }
+            tc::mma_commit(bar_sfull);
+            tc::mma_commit(bar_empty + 8 * s);
+          }
+          if (s_abort) break;
+        }
+        tc::mma_commit(bar_qempty);  // Q / qI free once this block's MMAs are done
+      }
+    }
+  } else {
+    // ---------------- compute warpgroups ----------------
+    const int g = warp >> 2;                 // warpgroup: M-tile (pass 1) / query pair (pass 2)
+    const int quad = warp & 3;               // tensor-memory lane quadrant
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int rowl = quad * 32 + lane;       // tensor-memory lane of this thread
+    uint32_t it = 0;
+    for (int k = blockIdx.x; k < total; k += gridDim.x) {
+      Block bk;
+      if (!block_of(cu, cu_cmp, B, r, total, k, bk)) continue;
+      if (bk.ntiles == 0) {
+        if (tid < bk.nq) {
+          kl_rows[bk.seq0 + bk.q0 + tid] = 0.f;
+          csize[bk.seq0 + bk.q0 + tid] = 0;
+        }
+        continue;
+      }
+      if (tid < kQB * kHI) {
+        const int q = tid / kHI, h = tid % kHI;
+        s_w[q][h] = q < bk.nq ? __bfloat162float(w[(int64_t)(bk.seq0 + bk.q0 + q) * kHI + h]) : 0.f;
+      }
+      // ---- pass 1: row (query, head) online log-sum-exp ----
+      {
+        const int q = 2 * g + (rowl >> 6), h = rowl & 63;
+        const int nvis = (bk.q0 + q + 1) / r;
+        float m = -INFINITY, l = 0.f;
+        for (int i = 0; i < bk.ntiles; ++i, ++it) {
+          if (!mbar_wait_bounded(bar_sfull, it & 1u, status)) { s_abort = 1; break; }
+          tc::fence_after_sync();
+          float x[kTK];
+#pragma unroll
+          for (int c0 = 0; c0 < kTK; c0 += 32) {
+            uint32_t rs[32];
+            tc::tmem_ld32_sync(tmem + lane_off + g * kTK + c0, rs);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[c0 + j] = __uint_as_float(rs[j]) * scale_log2;
+          }
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_sfree);
+          const int nv = nvis - i * kTK;  // valid columns of this tile
+          float tmax = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kTK; ++c) {
+            x[c] = c < nv ? x[c] : -INFINITY;
+            tmax = fmaxf(tmax, x[c]);
+          }
+          const float mn = fmaxf(m, tmax);
+          if (mn != -INFINITY) {
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < kTK; ++c) acc += ex2(x[c] - mn);
+            l = l * ex2(m - mn) + acc;
+            m = mn;
+          }
+        }
+        if (q < kQB) s_L[q][h] = (l > 0.f) ? m + __log2f(l) : INFINITY;  // +inf: contributes nothing
+      }
+      named_sync(1, kComputeThreads);
+      if (*(volatile int*)&s_abort) break;  // uniform: read after the barrier
+      // ---- pass 2: one thread per key, queries 2g and 2g+1 ----
+      float A[2] = {0.f, 0.f}, Bs[2] = {0.f, 0.f}, mI[2] = {-INFINITY, -INFINITY}, lI[2] = {0.f, 0.f};
+      for (int i = 0; i < bk.ntiles; ++i, ++it) {
+        if (!mbar_wait_bounded(bar_sfull, it & 1u, status)) { s_abort = 1; break; }
+        tc::fence_after_sync();
+        float x[kTK];
+        uint32_t ri[16];
+#pragma unroll
+        for (int c0 = 0; c0 < kTK; c0 += 32) {
+          uint32_t rs[32];
+          tc::tmem_ld32_sync(tmem + lane_off + g * kTK + c0, rs);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[c0 + j] = __uint_as_float(rs[j]);
+        }
+        tc::tmem_ld16_sync(tmem + lane_off + kColI + g * 16, ri);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfree);
+        const int j = i * kTK + rowl;  // entry index within the sequence
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const int q = 2 * g + qq;
+          const int nvis = (bk.q0 + q + 1) / r;
+          if (q < bk.nq && j < nvis) {
+            float p = 0.f;
+#pragma unroll
+            for (int h = 0; h < kNH; ++h) p += ex2(fmaf(x[qq * kNH + h], scale_log2, -s_L[q][h]));
+            p *= 1.f / kNH;
+            float iv = 0.f;
+#pragma unroll
+            for (int h = 0; h < kHI; ++h) iv = fmaf(s_w[q][h], fmaxf(__uint_as_float(ri[qq * kHI + h]), 0.f), iv);
+            if (p > 0.f) A[qq] = fmaf(p, __logf(p), A[qq]);
+            Bs[qq] = fmaf(p, iv, Bs[qq]);
+            if (iv > mI[qq]) {
+              lI[qq] = lI[qq] * __expf(mI[qq] - iv) + 1.f;
+              mI[qq] = iv;
+            } else {
+              lI[qq] += __expf(iv - mI[qq]);
+            }
+          }
+        }
+      }
+      // reduce the per-key partials over the warpgroup's 128 threads
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        float a = A[qq], bs = Bs[qq], mm = mI[qq], ll = lI[qq];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          a += __shfl_xor_sync(0xffffffffu, a, o);
+          bs += __shfl_xor_sync(0xffffffffu, bs, o);
+          const float m2 = __shfl_xor_sync(0xffffffffu, mm, o);
+          const float l2 = __shfl_xor_sync(0xffffffffu, ll, o);
+          const float mx = fmaxf(mm, m2);
+          ll = (mx == -INFINITY) ? 0.f : ll * __expf(mm - mx) + l2 * __expf(m2 - mx);
+          mm = mx;
+        }
+        if (lane == 0) {
+          s_red[warp][qq][0] = a;
+          s_red[warp][qq][1] = bs;
+          s_red[warp][qq][2] = mm;
+          s_red[warp][qq][3] = ll;
+        }
+      }
+      named_sync(1, kComputeThreads);
+      if (tid < kQB) {
+        const int q = tid, gg = q >> 1, qq = q & 1;
+        if (q < bk.nq) {
+          float a = 0.f, bs = 0.f, mm = -INFINITY;
+          for (int ww = 0; ww < 4; ++ww) {
+            a += s_red[gg * 4 + ww][qq][0];
+            bs += s_red[gg * 4 + ww][qq][1];
+            mm = fmaxf(mm, s_red[gg * 4 + ww][qq][2]);
+          }
+          float ll = 0.f;
+          for (int ww = 0; ww < 4; ++ww) {
+            const float m2 = s_red[gg * 4 + ww][qq][2];
+            if (m2 != -INFINITY) ll += s_red[gg * 4 + ww][qq][3] * __expf(m2 - mm);
+          }
+          const int nvis = (bk.q0 + q + 1) / r;
+          kl_rows[bk.seq0 + bk.q0 + q] = nvis > 0 ? a - bs + (mm + __logf(ll)) : 0.f;
+          csize[bk.seq0 + bk.q0 + q] = nvis;
+        }
+      }
+      named_sync(1, kComputeThreads);
+      if (*(volatile int*)&s_abort) break;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 9) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+bool indexer_kl_dense_tc_supported(const KLArgs& a, bool fp32) {
+  return !fp32 && a.idx == nullptr && a.H == kNH && a.d == kDim && a.H_I == kHI && a.d_I == kDI;
+}
+
+__global__ void kl_zero_rows_kernel(float* __restrict__ kl_rows, int32_t* __restrict__ csize, int T_cap) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T_cap; i += gridDim.x * blockDim.x) {
+    kl_rows[i] = 0.f;
+    csize[i] = 0;
+  }
+}
+
+cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream) {
+  if (a.T_cap <= 0) return cudaSuccess;
+  CUtensorMap mq, mk, mqi, mki;
+  // the compressed arrays hold at most T_cap / r rows
+  const uint64_t n_cmp_rows = (uint64_t)(a.T_cap / a.r > 0 ? a.T_cap / a.r : 1);
+  if (!make_tmap_bf16_sw128(&mq, a.q, (uint64_t)a.T_cap * kNH, kDim, 128) ||
+      !make_tmap_bf16_sw128(&mk, a.k_cmp, n_cmp_rows, kDim, kTK) ||
+      !make_tmap_bf16_sw128(&mqi, a.qI, (uint64_t)a.T_cap * kHI, kDI, kQB * kHI) ||
+      !make_tmap_bf16_sw128(&mki, a.kI, n_cmp_rows, kDI, kTK))
+    return cudaErrorInvalidValue;
+  kl_zero_rows_kernel<<<152, 256, 0, stream>>>(a.kl_rows, a.csize, a.T_cap);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t smem = kSmemBytes + 1024;
+  err = cudaFuncSetAttribute(indexer_kl_dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int blocks = (a.T_cap + kQB - 1) / kQB + a.B;  // upper bound on query blocks
+  const int grid = blocks < sms ? blocks : sms;
+  constexpr float kLog2e = 1.4426950408889634f;
+  indexer_kl_dense_tc_kernel<<<grid, kThreads, smem, stream>>>(
+      mq, mk, mqi, mki, static_cast<const __nv_bfloat16*>(a.w), a.cu, a.cu_cmp, a.B, a.r, a.scale * kLog2e,
+      a.kl_rows, a.csize, a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

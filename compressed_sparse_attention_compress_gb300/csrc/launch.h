@@ -66,5 +66,7 @@ struct KLArgs {
   int* status;
 };
 cudaError_t launch_indexer_kl(const KLArgs& a, bool fp32, cudaStream_t stream);
+bool indexer_kl_dense_tc_supported(const KLArgs& a, bool fp32);
+cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream);
 
 }  // namespace csa
