@@ -314,7 +314,7 @@ def run_ours(args, wl):
 
 
 def f_launches(wl) -> int:
-    """Kernels of ours launched per step."""
+    """Kernels of ours launched per step (mirrors the dispatch in csrc/)."""
     n = 0
     if wl.ratio > 0:
         n += 1 + 1 + (1 if wl.separate_v else 0) + (1 if wl.H_I > 0 else 0)   # offsets + compress calls
@@ -322,7 +322,9 @@ def f_launches(wl) -> int:
             n += 2                                                              # top-k + capacity fill
     n += 1                                                                      # attention
     if wl.kl_mode != "none":
-        n += 2                                                                  # KL + finalize
+        dense_tc = (wl.kl_mode == "dense" and not wl.io_fp32 and wl.H == 64 and wl.d == 128
+                    and wl.H_I == 8 and wl.d_I == 64)
+        n += 3 if dense_tc else 2                                               # (zero) + KL + finalize
     return n
 
 

@@ -342,6 +342,14 @@ static cudaError_t launch_topk_t(const void* qI, const void* w, const void* kI, 
 cudaError_t launch_indexer_topk(const void* qI, const void* w, const void* kI, const int32_t* cu,
                                 const int32_t* cu_cmp, int B, int T_cap, int max_vis, int H_I, int d_I, int r,
                                 int topk, int k_pad, bool fp32, int32_t* idx, int* status, cudaStream_t stream) {
+  // indexer 8 heads x 64 dims in bf16 scores on tcgen05 with TMA-fed tiles
+  if (indexer_topk_tc_supported(H_I, d_I, max_vis, fp32)) {
+    cudaError_t err = launch_indexer_topk_tc(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status,
+                                             stream);
+    if (err != cudaSuccess || T_cap <= 0) return err;
+    topk_fill_capacity_kernel<<<152, 256, 0, stream>>>(cu, B, T_cap, k_pad, idx);
+    return cudaGetLastError();
+  }
   if (fp32) {
     if (d_I == 32)
       return launch_topk_t<float, 32>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, H_I, r, topk, k_pad, idx, status,

@@ -1,0 +1,400 @@
+// indexer_topk_tc.cu -- lightning-indexer scoring on tcgen05 tensor cores with
+// TMA-fed key tiles, fused with the exact per-query top-k (indexer 8 heads x
+// 64 dims, bf16).
+//
+// "DeepSeek-V4 Attention Training Systems": §3 (indexer logit i_{t,j}; here
+// sum_h w[t,h] ReLU(qI[t,h,:] . kI[j,:])), §4 (causal visibility of completed
+// groups, reset at sample boundaries), §8 / §8.2 ("indexer scoring and radix
+// top-k": causal offsets, ragged lengths, fixed top-k capacity, alignment
+// padding and local-to-global id lowering), §8.1 (top-k padding).
+//
+// One CTA takes a block of G consecutive queries of one sequence (G = 4, or 2
+// for very long sequences).  Their visible entries are a prefix of the
+// sequence's compressed rows, so the key tiles (128 entries x 64 dims) are
+// shared: a TMA warp streams them through a 4-stage pipeline, an MMA warp
+// computes I^T = kI qI^T (M = 128 entries, N = G x 8 query-heads) into a
+// double-buffered tensor-memory tile, and 8 compute warps turn each entry's
+// head scores into sum_h w ReLU(.) for their queries and store it in shared
+// memory as an order-preserving 32-bit key.  No score reaches global memory.
+// Then, per query, an exact radix select (11/11/10-bit digits, warp-aggregated
+// shared-memory histograms) finds the k-th largest key, and an ordered
+// compaction writes the selected entries in ascending index order (ties at
+// the threshold: smaller index first) as global compressed rows, -1 padded.
+// Blocks whose queries all see at most k entries select everything without
+// scoring.
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tcgen05.cuh"
+#include "tma.cuh"
+
+namespace csa {
+
+namespace {
+
+constexpr int kHI = 8, kDI = 64;
+constexpr int kTK = 128;                 // entries per tile
+constexpr int kStages = 4;
+constexpr int kComputeThreads = 256;
+constexpr int kThreads = kComputeThreads + 64;
+constexpr int kBins = 2048;
+constexpr uint32_t kTileBytes = kTK * 128;  // 16 KB
+constexpr uint32_t kQIOff = 0;              // up to 32 rows x 128 B
+constexpr uint32_t kStageOff = 4096;
+constexpr uint32_t kKeysOff = kStageOff + kStages * kTileBytes;  // scores start here
+
+__device__ __forceinline__ uint32_t order_key(float v) {
+  if (v == 0.f) v = 0.f;  // -0 and +0 are the same score
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
+
+struct QBlock {
+  int q0, nq, seq0, cmp0, nvis_max, ntiles;
+  bool score;  // some query sees more than k entries
+};
+
+__device__ __forceinline__ int total_qblocks(const int32_t* __restrict__ cu, int B, int G) {
+  int n = 0;
+  for (int bb = 0; bb < B; ++bb) n += (max(0, __ldg(cu + bb + 1) - __ldg(cu + bb)) + G - 1) / G;
+  return n;
+}
+
+// Block k counted from the end of the buffer (latest queries, most entries, first).
+__device__ __forceinline__ bool qblock_of(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_cmp, int B,
+                                          int r, int G, int topk, int max_vis, int total, int k, QBlock& o) {
+  int c = total - 1 - k;
+  for (int bb = 0; bb < B; ++bb) {
+    const int L = max(0, __ldg(cu + bb + 1) - __ldg(cu + bb));
+    const int nb = (L + G - 1) / G;
+    if (c < nb) {
+      o.q0 = c * G;
+      o.nq = min(G, L - c * G);
+      o.seq0 = __ldg(cu + bb);
+      o.cmp0 = __ldg(cu_cmp + bb);
+      o.nvis_max = min((o.q0 + o.nq) / r, max_vis);
+      o.score = o.nvis_max > topk;
+      o.ntiles = o.score ? (o.nvis_max + kTK - 1) / kTK : 0;
+      return true;
+    }
+    c -= nb;
+  }
+  return false;
+}
+
+}  // namespace
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_constant__ CUtensorMap map_ki,
+                       const __nv_bfloat16* __restrict__ w, const int32_t* __restrict__ cu,
+                       const int32_t* __restrict__ cu_cmp, int B, int r, int topk, int k_pad, int max_vis,
+                       int32_t* __restrict__ idx, int* status) {
+  constexpr int kN = G * kHI;  // MMA N: query-head rows
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_dfull[2], s_dfree[2];
+  __shared__ __align__(8) uint64_t s_qfull, s_qempty;
+  __shared__ float s_w[G][kHI];
+  __shared__ uint32_t s_hist[kBins];
+  __shared__ int s_scan[8];
+  __shared__ int s_cnt[2][8];
+  __shared__ uint32_t s_digit;
+  __shared__ int s_need;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint32_t* sKey = reinterpret_cast<uint32_t*>(smem_raw + (base - smem_u32(smem_raw)) + kKeysOff);
+  const int vstride = (max_vis + 3) & ~3;
+  const uint32_t bar_full = smem_u32(&s_full[0]), bar_empty = smem_u32(&s_empty[0]);
+  const uint32_t bar_dfull = smem_u32(&s_dfull[0]), bar_dfree = smem_u32(&s_dfree[0]);
+  const uint32_t bar_qfull = smem_u32(&s_qfull), bar_qempty = smem_u32(&s_qempty);
+
+  if (warp == 9) {
+    tc::tmem_alloc(smem_u32(&s_tmem), 64);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_dfull + 8 * i, 1);
+      mbar_init(bar_dfree + 8 * i, 8);
+    }
+    mbar_init(bar_qfull, 1);
+    mbar_init(bar_qempty, 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  const int total = total_qblocks(cu, B, G);
+
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_map(&map_qi);
+      tma_prefetch_map(&map_ki);
+      uint32_t it = 0, nblk = 0;
+      for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
+        QBlock bk;
+        if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk) || bk.ntiles == 0) continue;
+        if (!mbar_wait_bounded(bar_qempty, (nblk & 1u) ^ 1u, status)) { s_abort = 1; break; }
+        ++nblk;
+        mbar_arrive_expect_tx(bar_qfull, kN * 128);
+        tma_load_2d(base + kQIOff, &map_qi, 0, (bk.seq0 + bk.q0) * kHI, bar_qfull);
+        for (int i = 0; i < bk.ntiles; ++i, ++it) {
+          const uint32_t s = it % kStages;
+          if (!mbar_wait_bounded(bar_empty + 8 * s, ((it / kStages) & 1u) ^ 1u, status)) { s_abort = 1; break; }
+          mbar_arrive_expect_tx(bar_full + 8 * s, kTileBytes);
+          tma_load_2d(base + kStageOff + s * kTileBytes, &map_ki, 0, bk.cmp0 + i * kTK, bar_full + 8 * s);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t kId = tc::idesc_bf16(kTK, kN, 0, 0);
+      uint32_t it = 0, nblk = 0;
+      for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
+        QBlock bk;
+        if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk) || bk.ntiles == 0) continue;
+        if (!mbar_wait_bounded(bar_qfull, nblk & 1u, status)) { s_abort = 1; break; }
+        ++nblk;
+        for (int i = 0; i < bk.ntiles; ++i, ++it) {
+          const uint32_t s = it % kStages, d = it & 1u;
+          if (!mbar_wait_bounded(bar_full + 8 * s, (it / kStages) & 1u, status) ||
+              !mbar_wait_bounded(bar_dfree + 8 * d, ((it >> 1) & 1u) ^ 1u, status)) {
+            s_abort = 1;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t st = base + kStageOff + s * kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < kDI / 16; ++ks) {
+            const uint64_t a = tc::smem_desc_sw128(st + ks * 32, 16, 1024);
+            const uint64_t bq = tc::smem_desc_sw128(base + kQIOff + ks * 32, 16, 1024);
+            tc::mma_bf16(tmem + d * 32, a, bq, kId, ks > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar_dfull + 8 * d);
+          tc::mma_commit(bar_empty + 8 * s);
+        }
+        tc::mma_commit(bar_qempty);
+      }
+    }
+  } else {
+    // ---------------- compute warps: scores, then selection ----------------
+    const int g = warp >> 2, quad = warp & 3;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int rowl = quad * 32 + lane;
+    uint32_t it = 0;
+    for (int k = blockIdx.x; k < total; k += gridDim.x) {
+      QBlock bk;
+      if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk)) continue;
+      if (tid == 0 && (bk.q0 + bk.nq) / r > max_vis) raise_status(status, CSA_ERR_DEVICE_BOUNDS);
+      if (bk.score) {
+        if (tid < G * kHI) {
+          const int q = tid / kHI, h = tid % kHI;
+          s_w[q][h] = q < bk.nq ? __bfloat162float(w[(int64_t)(bk.seq0 + bk.q0 + q) * kHI + h]) : 0.f;
+        }
+        named_sync(1, kComputeThreads);
+        for (int i = 0; i < bk.ntiles; ++i, ++it) {
+          const uint32_t d = it & 1u;
+          if (!mbar_wait_bounded(bar_dfull + 8 * d, (it >> 1) & 1u, status)) { s_abort = 1; break; }
+          tc::fence_after_sync();
+          uint32_t rv[16];
+          const bool active = 2 * g < G;  // this warpgroup's query pair exists
+          if (active) tc::tmem_ld16_sync(tmem + lane_off + d * 32 + g * 16, rv);
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dfree + 8 * d);
+          const int j = i * kTK + rowl;
+          if (active && j < bk.nvis_max) {
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+              const int q = 2 * g + qq;
+              float sc = 0.f;
+#pragma unroll
+              for (int h = 0; h < kHI; ++h) sc = fmaf(s_w[q][h], fmaxf(__uint_as_float(rv[qq * kHI + h]), 0.f), sc);
+              sKey[(size_t)q * vstride + j] = order_key(sc);
+            }
+          }
+        }
+        named_sync(1, kComputeThreads);
+        if (*(volatile int*)&s_abort) break;
+      }
+      // ---- per query: select and write ----
+      for (int q = 0; q < bk.nq; ++q) {
+        const int t = bk.q0 + q;
+        const int64_t orow = (int64_t)(bk.seq0 + t) * k_pad;
+        const int n = min((t + 1) / r, max_vis);
+        const int m = min(topk, n);
+        const uint32_t* keys = sKey + (size_t)q * vstride;
+        const bool all = n <= topk;
+        uint32_t thr = 0;
+        int need_eq = 0;
+        if (!all) {
+          uint32_t prefix = 0, pmask = 0;
+          int need = m;
+          for (int round = 0; round < 3; ++round) {
+            const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
+            const uint32_t dmask = round == 2 ? 0x3FFu : 0x7FFu;
+            for (int i = tid; i < kBins; i += kComputeThreads) s_hist[i] = 0;
+            named_sync(1, kComputeThreads);
+            for (int jb = warp * 32; jb < n; jb += kComputeThreads) {
+              const int j = jb + lane;
+              const uint32_t key = j < n ? keys[j] : 0u;
+              const bool ok = j < n && (key & pmask) == prefix;
+              const uint32_t act = __ballot_sync(0xffffffffu, ok);
+              if (ok) {
+                const uint32_t dg = (key >> shift) & dmask;
+                const uint32_t peers = __match_any_sync(act, dg);
+                if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[dg], (uint32_t)__popc(peers));
+              }
+            }
+            named_sync(1, kComputeThreads);
+            // thread tid owns 8 bins counted from the top
+            const int nb = (int)dmask + 1;
+            const int hi_bin = nb - 1 - tid * 8;
+            int local = 0;
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb)
+              if (hi_bin - kb >= 0) local += (int)s_hist[hi_bin - kb];
+            int incl = local;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int v = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += v;
+            }
+            if (lane == 31) s_scan[warp] = incl;
+            named_sync(1, kComputeThreads);
+            int above = incl - local;
+            for (int ww = 0; ww < warp; ++ww) above += s_scan[ww];
+            if (above < need && need <= above + local) {
+              int cum = above;
+              for (int kb = 0; kb < 8; ++kb) {
+                const int bin = hi_bin - kb;
+                if (bin < 0) break;
+                const int hc = (int)s_hist[bin];
+                if (need <= cum + hc) {
+                  s_digit = (uint32_t)bin;
+                  s_need = need - cum;
+                  break;
+                }
+                cum += hc;
+              }
+            }
+            named_sync(1, kComputeThreads);
+            prefix |= s_digit << shift;
+            pmask |= dmask << shift;
+            need = s_need;
+            named_sync(1, kComputeThreads);
+          }
+          thr = prefix;
+          need_eq = need;
+        }
+        // ordered compaction: warp w scans the contiguous range [w*seg, (w+1)*seg)
+        const int seg = ((n + kComputeThreads - 1) / kComputeThreads) * 32;
+        const int j_lo = warp * seg, j_hi = min(n, j_lo + seg);
+        int gt = 0, eq = 0;
+        if (!all) {
+          for (int jb = j_lo; jb < j_hi; jb += 32) {
+            const int j = jb + lane;
+            const uint32_t key = j < j_hi ? keys[j] : 0u;
+            gt += __popc(__ballot_sync(0xffffffffu, j < j_hi && key > thr));
+            eq += __popc(__ballot_sync(0xffffffffu, j < j_hi && key == thr));
+          }
+        } else {
+          gt = max(0, j_hi - j_lo);
+        }
+        if (lane == 0) { s_cnt[0][warp] = gt; s_cnt[1][warp] = eq; }
+        named_sync(1, kComputeThreads);
+        int gt_before = 0, eq_before = 0;
+        for (int ww = 0; ww < warp; ++ww) { gt_before += s_cnt[0][ww]; eq_before += s_cnt[1][ww]; }
+        for (int jb = j_lo; jb < j_hi; jb += 32) {
+          const int j = jb + lane;
+          bool fgt, feq;
+          if (all) {
+            fgt = j < j_hi;
+            feq = false;
+          } else {
+            const uint32_t key = j < j_hi ? keys[j] : 0u;
+            fgt = j < j_hi && key > thr;
+            feq = j < j_hi && key == thr;
+          }
+          const uint32_t bgt = __ballot_sync(0xffffffffu, fgt);
+          const uint32_t beq = __ballot_sync(0xffffffffu, feq);
+          const uint32_t below = (1u << lane) - 1u;
+          const int my_gt = gt_before + __popc(bgt & below);
+          const int my_eq = eq_before + __popc(beq & below);
+          if (fgt || (feq && my_eq < need_eq)) idx[orow + my_gt + min(my_eq, need_eq)] = bk.cmp0 + j;
+          gt_before += __popc(bgt);
+          eq_before += __popc(beq);
+        }
+        for (int i = m + tid; i < k_pad; i += kComputeThreads) idx[orow + i] = -1;
+        named_sync(1, kComputeThreads);
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 9) tc::tmem_dealloc(tmem, 64);
+}
+
+static int topk_tc_group(int max_vis) {
+  const size_t per_query = (size_t)((max_vis + 3) & ~3) * 4;
+  const size_t budget = 232448 - 1024 - kKeysOff - 12 * 1024;  // dynamic smem left for scores
+  if (4 * per_query <= budget) return 4;
+  if (2 * per_query <= budget) return 2;
+  return 0;
+}
+
+bool indexer_topk_tc_supported(int H_I, int d_I, int max_vis, bool fp32) {
+  return !fp32 && H_I == kHI && d_I == kDI && topk_tc_group(max_vis) > 0;
+}
+
+template <int G>
+static cudaError_t launch_topk_tc_t(const void* qI, const void* w, const void* kI, const int32_t* cu,
+                                    const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r, int topk, int k_pad,
+                                    int32_t* idx, int* status, cudaStream_t stream) {
+  CUtensorMap mqi, mki;
+  const uint64_t n_cmp_rows = (uint64_t)(T_cap / r > 0 ? T_cap / r : 1);
+  if (!make_tmap_bf16_sw128(&mqi, qI, (uint64_t)T_cap * kHI, kDI, G * kHI) ||
+      !make_tmap_bf16_sw128(&mki, kI, n_cmp_rows, kDI, kTK))
+    return cudaErrorInvalidValue;
+  const size_t smem = 1024 + kKeysOff + (size_t)G * ((max_vis + 3) & ~3) * 4;
+  auto kern = indexer_topk_tc_kernel<G>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int blocks = T_cap / G + B + 1;
+  const int grid = blocks < sms ? blocks : sms;
+  kern<<<grid, kThreads, smem, stream>>>(mqi, mki, static_cast<const __nv_bfloat16*>(w), cu, cu_cmp, B, r, topk,
+                                         k_pad, max_vis, idx, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_topk_tc(const void* qI, const void* w, const void* kI, const int32_t* cu,
+                                   const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r, int topk, int k_pad,
+                                   int32_t* idx, int* status, cudaStream_t stream) {
+  if (T_cap <= 0) return cudaSuccess;
+  if (topk_tc_group(max_vis) == 4)
+    return launch_topk_tc_t<4>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
+  return launch_topk_tc_t<2>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
+}
+
+}  // namespace csa

@@ -21,6 +21,11 @@ cudaError_t launch_indexer_topk(const void* qI, const void* w, const void* kI, c
                                 int d_I, int r, int topk, int k_pad, bool fp32, int32_t* idx,
                                 int* status, cudaStream_t stream);
 
+bool indexer_topk_tc_supported(int H_I, int d_I, int max_vis, bool fp32);
+cudaError_t launch_indexer_topk_tc(const void* qI, const void* w, const void* kI, const int32_t* cu,
+                                   const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r, int topk, int k_pad,
+                                   int32_t* idx, int* status, cudaStream_t stream);
+
 // Attention kinds.
 enum AttnKind { kAttnCSA = 0, kAttnHCA = 1, kAttnWindow = 2 };
 
