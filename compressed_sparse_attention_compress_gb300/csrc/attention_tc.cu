@@ -104,7 +104,8 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_bar[2];  // 0: S ready, 1: O (PV) done
   __shared__ int s_rows[2][kTK];
-  __shared__ float s_m[kNH], s_alpha[kNH], s_inv[kNH];
+  __shared__ __align__(16) float s_m[kNH];
+  __shared__ float s_alpha[kNH], s_inv[kNH];
   __shared__ int s_wmax[4][kNH];
   __shared__ float s_lsum[4][kNH];
 
@@ -286,24 +287,42 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       tc::fence_after_sync();
 
       // ---- softmax of tile `cur`: this thread = key (tid) ----
+      // t_h = s_h * scale*log2(e) - m_h, the log2 weight relative to the running
+      // reference; a block vote decides whether any t_h exceeds the slack.
       const bool valid = s_rows[buf][tid] >= 0;
-      float x[kNH];
-      {
+      float t[kNH];
+      auto load_t = [&]() {
         uint32_t rs[32];
         tc::tmem_ld32_sync(t_s + lane_off, rs);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = valid ? __uint_as_float(rs[j]) * scale_log2 : -INFINITY;
+        for (int j = 0; j < 32; ++j) t[j] = __uint_as_float(rs[j]);
         tc::tmem_ld32_sync(t_s + lane_off + 32, rs);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[32 + j] = valid ? __uint_as_float(rs[j]) * scale_log2 : -INFINITY;
-      }
-      float excess = -INFINITY;
+        for (int j = 0; j < 32; ++j) t[32 + j] = __uint_as_float(rs[j]);
+      };
+      auto to_log2_weights = [&]() -> float {  // t <- s*c - m; returns max_h t
+        float ex = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < kNH; ++h) excess = fmaxf(excess, x[h] - s_m[h]);
+        for (int h4 = 0; h4 < kNH / 4; ++h4) {
+          const float4 m4 = reinterpret_cast<const float4*>(s_m)[h4];
+          t[4 * h4 + 0] = fmaf(t[4 * h4 + 0], scale_log2, -m4.x);
+          t[4 * h4 + 1] = fmaf(t[4 * h4 + 1], scale_log2, -m4.y);
+          t[4 * h4 + 2] = fmaf(t[4 * h4 + 2], scale_log2, -m4.z);
+          t[4 * h4 + 3] = fmaf(t[4 * h4 + 3], scale_log2, -m4.w);
+          ex = fmaxf(ex, fmaxf(fmaxf(t[4 * h4 + 0], t[4 * h4 + 1]), fmaxf(t[4 * h4 + 2], t[4 * h4 + 3])));
+        }
+        return ex;
+      };
+      load_t();
+      float excess = -INFINITY;
+      if (valid) excess = to_log2_weights();  // m = -inf (first tile) gives +inf
       if (__syncthreads_or(excess > kTau)) {
+        // new reference: the tile's per-head column maxima (warp max-reductions)
+        load_t();
 #pragma unroll
         for (int h = 0; h < kNH; ++h) {
-          const int v = __reduce_max_sync(0xffffffffu, ord_of(x[h]));
+          const float xh = valid ? t[h] * scale_log2 : -INFINITY;
+          const int v = __reduce_max_sync(0xffffffffu, ord_of(xh));
           if (lane == 0) s_wmax[warp][h] = v;
         }
         __syncthreads();
@@ -329,21 +348,23 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
           }
           tc::tmem_wait_st();
         }
+        if (valid) to_log2_weights();
       }
-      // P^T row of this key: 64 heads -> 8 swizzled 16-byte chunks
+      // P^T row of this key: 64 heads -> 8 swizzled 16-byte chunks (zeros for a missing key)
       {
         const uint32_t prow = base + L::kPOff;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          uint32_t pk[4];
+          uint32_t pk[4] = {0u, 0u, 0u, 0u};
+          if (valid) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int h = c * 8 + 2 * j;
-            const float p0 = x[h] == -INFINITY ? 0.f : ex2(x[h] - s_m[h]);
-            const float p1 = x[h + 1] == -INFINITY ? 0.f : ex2(x[h + 1] - s_m[h + 1]);
-            l_part[h] += p0;
-            l_part[h + 1] += p1;
-            pk[j] = pack_bf16x2(p0, p1);
+            for (int j = 0; j < 4; ++j) {
+              const int h = c * 8 + 2 * j;
+              const float p0 = ex2(t[h]), p1 = ex2(t[h + 1]);
+              l_part[h] += p0;
+              l_part[h + 1] += p1;
+              pk[j] = pack_bf16x2(p0, p1);
+            }
           }
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + tc::sw128_offset(tid, c)),
                        "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])

@@ -112,7 +112,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
   __shared__ __align__(8) uint64_t s_sfull, s_sfree, s_qfull, s_qempty;
-  __shared__ float s_L[kQB][kNH];        // per (query, head) log2 normaliser over C_t
+  __shared__ __align__(16) float s_L[kQB][kNH];  // per (query, head) log2 normaliser over C_t
   __shared__ float s_w[kQB][kHI];
   __shared__ float s_red[8][2][4];       // per compute warp, per query: A, B, mI, lI
   __shared__ int s_abort;
@@ -267,24 +267,29 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
             uint32_t rs[32];
             tc::tmem_ld32_sync(tmem + lane_off + g * kTK + c0, rs);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[c0 + j] = __uint_as_float(rs[j]) * scale_log2;
+            for (int j = 0; j < 32; ++j) x[c0 + j] = __uint_as_float(rs[j]);
           }
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_sfree);
           const int nv = nvis - i * kTK;  // valid columns of this tile
+          if (nv < kTK) {                 // only the last tile of a row is partial
+#pragma unroll
+            for (int c = 0; c < kTK; ++c) x[c] = c < nv ? x[c] : -INFINITY;
+          }
           float tmax = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < kTK; ++c) {
-            x[c] = c < nv ? x[c] : -INFINITY;
-            tmax = fmaxf(tmax, x[c]);
-          }
-          const float mn = fmaxf(m, tmax);
+          for (int c = 0; c < kTK; c += 4)
+            tmax = fmaxf(tmax, fmaxf(fmaxf(x[c], x[c + 1]), fmaxf(x[c + 2], x[c + 3])));
+          const float mn = fmaxf(m, tmax * scale_log2);  // scale > 0: max commutes with it
           if (mn != -INFINITY) {
-            float acc = 0.f;
+            float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-            for (int c = 0; c < kTK; ++c) acc += ex2(x[c] - mn);
-            l = l * ex2(m - mn) + acc;
+            for (int c = 0; c < kTK; c += 2) {
+              acc0 += ex2(fmaf(x[c], scale_log2, -mn));
+              acc1 += ex2(fmaf(x[c + 1], scale_log2, -mn));
+            }
+            l = l * ex2(m - mn) + (acc0 + acc1);
             m = mn;
           }
         }
@@ -316,10 +321,17 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
           const int q = 2 * g + qq;
           const int nvis = (bk.q0 + q + 1) / r;
           if (q < bk.nq && j < nvis) {
-            float p = 0.f;
+            float p0 = 0.f, p1 = 0.f;
+            const float4* L4 = reinterpret_cast<const float4*>(&s_L[q][0]);
 #pragma unroll
-            for (int h = 0; h < kNH; ++h) p += ex2(fmaf(x[qq * kNH + h], scale_log2, -s_L[q][h]));
-            p *= 1.f / kNH;
+            for (int h4 = 0; h4 < kNH / 4; ++h4) {
+              const float4 L = L4[h4];
+              p0 += ex2(fmaf(x[qq * kNH + 4 * h4 + 0], scale_log2, -L.x));
+              p1 += ex2(fmaf(x[qq * kNH + 4 * h4 + 1], scale_log2, -L.y));
+              p0 += ex2(fmaf(x[qq * kNH + 4 * h4 + 2], scale_log2, -L.z));
+              p1 += ex2(fmaf(x[qq * kNH + 4 * h4 + 3], scale_log2, -L.w));
+            }
+            const float p = (p0 + p1) * (1.f / kNH);
             float iv = 0.f;
 #pragma unroll
             for (int h = 0; h < kHI; ++h) iv = fmaf(s_w[q][h], fmaxf(__uint_as_float(ri[qq * kHI + h]), 0.f), iv);
