@@ -160,6 +160,15 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
     const int n_ctiles = (n_cslots + kTK - 1) / kTK;
     const int ntiles = n_ctiles + (n_win + kTK - 1) / kTK;
 
+    // this thread's index-list slot of tile `it`, loaded one tile ahead of its use
+    int pre_it = -1, pre_g = -1;
+    auto prefetch = [&](int it) {
+      const int slot = it * kTK + tid;
+      if (kind == kAttnCSA && it < n_ctiles && slot < k_pad) {
+        asm volatile("ld.global.nc.b32 %0, [%1];\n" : "=r"(pre_g) : "l"(idx + (int64_t)row * k_pad + slot));
+        pre_it = it;
+      }
+    };
     // resolve the rows of tile `it` into s_rows[buf]; true if any is valid
     auto resolve = [&](int it, int buf) -> bool {
       int rr = -1;
@@ -167,7 +176,7 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
         const int slot = it * kTK + tid;
         if (kind == kAttnCSA) {
           if (slot < k_pad) {
-            const int g = __ldg(idx + (int64_t)row * k_pad + slot);
+            const int g = pre_it == it ? pre_g : __ldg(idx + (int64_t)row * k_pad + slot);
             if (g >= 0) {
               if (g < cmp0 || g >= cmp0 + nvis || g >= cmp_limit) raise_status(status, CSA_ERR_DEVICE_BOUNDS);
               else rr = g;
@@ -181,6 +190,7 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
         if (wi < n_win && seq0 + w0 + wi < raw_limit) rr = seq0 + w0 + wi;
       }
       s_rows[buf][tid] = rr;
+      prefetch(it + 1);
       return __syncthreads_or(rr >= 0) != 0;
     };
     // first tile index >= it with a valid key (window tiles always have one)
@@ -264,8 +274,10 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
 
     bool aborted = false;
     while (cur < ntiles) {
-      if (have_o && !wait(bar_o, ph_o)) { aborted = true; break; }  // PV of the previous tile done
+      // rows of the next tile (s_rows[buf ^ 1] is no longer read), then its gather
+      // into buffer buf ^ 1 once the previous tile's PV has finished reading it
       const int nxt = (cur + 1 < ntiles) ? next_tile(cur + 1, buf ^ 1) : ntiles;
+      if (have_o && !wait(bar_o, ph_o)) { aborted = true; break; }
       if (nxt < ntiles) gather(nxt, buf ^ 1);
 
       if (!snap && cur >= n_ctiles) {  // compressed candidates done: their normaliser

@@ -36,7 +36,8 @@ namespace {
 constexpr int kHI = 8, kDI = 64;
 constexpr int kTK = 128;                 // entries per tile
 constexpr int kStages = 4;
-constexpr int kComputeThreads = 256;
+constexpr int kComputeWarps = 16;
+constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kThreads = kComputeThreads + 64;
 constexpr int kBins = 2048;
 constexpr uint32_t kTileBytes = kTK * 128;  // 16 KB
@@ -102,10 +103,10 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   __shared__ __align__(8) uint64_t s_qfull, s_qempty;
   __shared__ float s_w[G][kHI];
   __shared__ uint32_t s_hist[kBins];
-  __shared__ int s_scan[8];
-  __shared__ int s_cnt[2][8];
+  __shared__ int s_scan[kComputeWarps];
+  __shared__ int s_cnt[2][kComputeWarps];
   __shared__ uint32_t s_digit;
-  __shared__ int s_need;
+  __shared__ int s_need, s_bincount;
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -116,7 +117,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   const uint32_t bar_dfull = smem_u32(&s_dfull[0]), bar_dfree = smem_u32(&s_dfree[0]);
   const uint32_t bar_qfull = smem_u32(&s_qfull), bar_qempty = smem_u32(&s_qempty);
 
-  if (warp == 9) {
+  if (warp == kComputeWarps + 1) {
     tc::tmem_alloc(smem_u32(&s_tmem), 64);
     tc::tmem_relinquish();
   }
@@ -127,7 +128,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_dfull + 8 * i, 1);
-      mbar_init(bar_dfree + 8 * i, 8);
+      mbar_init(bar_dfree + 8 * i, kComputeWarps);
     }
     mbar_init(bar_qfull, 1);
     mbar_init(bar_qempty, 1);
@@ -140,7 +141,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   const uint32_t tmem = s_tmem;
   const int total = total_qblocks(cu, B, G);
 
-  if (warp == 8) {
+  if (warp == kComputeWarps) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_map(&map_qi);
@@ -161,7 +162,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kComputeWarps + 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t kId = tc::idesc_bf16(kTK, kN, 0, 0);
@@ -194,7 +195,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
     }
   } else {
     // ---------------- compute warps: scores, then selection ----------------
-    const int g = warp >> 2, quad = warp & 3;
+    const int g = warp >> 2, quad = warp & 3;  // warpgroup g scores query g of the block
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const int rowl = quad * 32 + lane;
     uint32_t it = 0;
@@ -208,32 +209,28 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
           s_w[q][h] = q < bk.nq ? __bfloat162float(w[(int64_t)(bk.seq0 + bk.q0 + q) * kHI + h]) : 0.f;
         }
         named_sync(1, kComputeThreads);
+        const bool active = g < G;  // this warpgroup's query exists in the tile
         for (int i = 0; i < bk.ntiles; ++i, ++it) {
           const uint32_t d = it & 1u;
           if (!mbar_wait_bounded(bar_dfull + 8 * d, (it >> 1) & 1u, status)) { s_abort = 1; break; }
           tc::fence_after_sync();
-          uint32_t rv[16];
-          const bool active = 2 * g < G;  // this warpgroup's query pair exists
-          if (active) tc::tmem_ld16_sync(tmem + lane_off + d * 32 + g * 16, rv);
+          uint32_t rv[8];
+          if (active) tc::tmem_ld8_sync(tmem + lane_off + d * 32 + g * kHI, rv);
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_dfree + 8 * d);
           const int j = i * kTK + rowl;
           if (active && j < bk.nvis_max) {
+            float sc = 0.f;
 #pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
-              const int q = 2 * g + qq;
-              float sc = 0.f;
-#pragma unroll
-              for (int h = 0; h < kHI; ++h) sc = fmaf(s_w[q][h], fmaxf(__uint_as_float(rv[qq * kHI + h]), 0.f), sc);
-              sKey[(size_t)q * vstride + j] = order_key(sc);
-            }
+            for (int h = 0; h < kHI; ++h) sc = fmaf(s_w[g][h], fmaxf(__uint_as_float(rv[h]), 0.f), sc);
+            sKey[(size_t)g * vstride + j] = order_key(sc);
           }
         }
         named_sync(1, kComputeThreads);
         if (*(volatile int*)&s_abort) break;
       }
-      // ---- per query: select and write ----
+      // ---- per query: select and write (each lane takes 4 consecutive entries) ----
       for (int q = 0; q < bk.nq; ++q) {
         const int t = bk.q0 + q;
         const int64_t orow = (int64_t)(bk.seq0 + t) * k_pad;
@@ -241,35 +238,38 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
         const int m = min(topk, n);
         const uint32_t* keys = sKey + (size_t)q * vstride;
         const bool all = n <= topk;
+        // selected: key > thr, plus the first need_eq entries with key == thr
         uint32_t thr = 0;
         int need_eq = 0;
         if (!all) {
           uint32_t prefix = 0, pmask = 0;
           int need = m;
-          for (int round = 0; round < 3; ++round) {
+          bool whole_bin = false;
+          for (int round = 0; round < 3 && !whole_bin; ++round) {
             const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
             const uint32_t dmask = round == 2 ? 0x3FFu : 0x7FFu;
-            for (int i = tid; i < kBins; i += kComputeThreads) s_hist[i] = 0;
+            const int nb = (int)dmask + 1;
+            for (int b = tid; b < nb; b += kComputeThreads) s_hist[b] = 0;
             named_sync(1, kComputeThreads);
-            for (int jb = warp * 32; jb < n; jb += kComputeThreads) {
-              const int j = jb + lane;
-              const uint32_t key = j < n ? keys[j] : 0u;
-              const bool ok = j < n && (key & pmask) == prefix;
-              const uint32_t act = __ballot_sync(0xffffffffu, ok);
-              if (ok) {
-                const uint32_t dg = (key >> shift) & dmask;
-                const uint32_t peers = __match_any_sync(act, dg);
-                if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[dg], (uint32_t)__popc(peers));
+            for (int jb = warp * 128; jb < n; jb += kComputeWarps * 128) {
+              const int j0 = jb + 4 * lane;
+              uint4 k4 = make_uint4(0u, 0u, 0u, 0u);
+              if (j0 < n) k4 = *reinterpret_cast<const uint4*>(keys + j0);
+              const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const bool ok = j0 + e < n && (kk[e] & pmask) == prefix;
+                const uint32_t dg = ok ? (kk[e] >> shift) & dmask : 0xFFFFFFFFu;
+                const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+                if (ok && lane == __ffs(peers) - 1) atomicAdd(&s_hist[dg], (uint32_t)__popc(peers));
               }
             }
             named_sync(1, kComputeThreads);
-            // thread tid owns 8 bins counted from the top
-            const int nb = (int)dmask + 1;
-            const int hi_bin = nb - 1 - tid * 8;
+            // thread tid owns bpt bins counted from the top
+            const int bpt = nb / kComputeThreads;
+            const int hi_bin = nb - 1 - tid * bpt;
             int local = 0;
-#pragma unroll
-            for (int kb = 0; kb < 8; ++kb)
-              if (hi_bin - kb >= 0) local += (int)s_hist[hi_bin - kb];
+            for (int kb = 0; kb < bpt; ++kb) local += (int)s_hist[hi_bin - kb];
             int incl = local;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -282,13 +282,13 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
             for (int ww = 0; ww < warp; ++ww) above += s_scan[ww];
             if (above < need && need <= above + local) {
               int cum = above;
-              for (int kb = 0; kb < 8; ++kb) {
+              for (int kb = 0; kb < bpt; ++kb) {
                 const int bin = hi_bin - kb;
-                if (bin < 0) break;
                 const int hc = (int)s_hist[bin];
                 if (need <= cum + hc) {
                   s_digit = (uint32_t)bin;
                   s_need = need - cum;
+                  s_bincount = hc;
                   break;
                 }
                 cum += hc;
@@ -298,48 +298,76 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
             prefix |= s_digit << shift;
             pmask |= dmask << shift;
             need = s_need;
+            // the bin holds exactly the entries still needed: all of it is selected
+            whole_bin = s_bincount == need && prefix != 0u;
             named_sync(1, kComputeThreads);
           }
-          thr = prefix;
-          need_eq = need;
-        }
-        // ordered compaction: warp w scans the contiguous range [w*seg, (w+1)*seg)
-        const int seg = ((n + kComputeThreads - 1) / kComputeThreads) * 32;
-        const int j_lo = warp * seg, j_hi = min(n, j_lo + seg);
-        int gt = 0, eq = 0;
-        if (!all) {
-          for (int jb = j_lo; jb < j_hi; jb += 32) {
-            const int j = jb + lane;
-            const uint32_t key = j < j_hi ? keys[j] : 0u;
-            gt += __popc(__ballot_sync(0xffffffffu, j < j_hi && key > thr));
-            eq += __popc(__ballot_sync(0xffffffffu, j < j_hi && key == thr));
+          if (whole_bin) {
+            thr = prefix - 1u;  // every key >= prefix (lower digits free) is selected
+            need_eq = 0;
+          } else {
+            thr = prefix;
+            need_eq = need;
           }
-        } else {
-          gt = max(0, j_hi - j_lo);
         }
+        // ordered compaction: warp w scans [w*seg, (w+1)*seg), seg a multiple of 128
+        const int seg = ((n + kComputeWarps * 128 - 1) / (kComputeWarps * 128)) * 128;
+        const int j_lo = warp * seg, j_hi = min(n, j_lo + seg);
+        auto flags_of = [&](int j0, uint32_t (&kk)[4], int& cgt, int& ceq) {
+          uint4 k4 = make_uint4(0u, 0u, 0u, 0u);
+          if (!all && j0 < j_hi) k4 = *reinterpret_cast<const uint4*>(keys + j0);
+          kk[0] = k4.x; kk[1] = k4.y; kk[2] = k4.z; kk[3] = k4.w;
+          cgt = 0;
+          ceq = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const bool in = j0 + e < j_hi;
+            cgt += (in && (all || kk[e] > thr)) ? 1 : 0;
+            ceq += (in && !all && kk[e] == thr) ? 1 : 0;
+          }
+        };
+        int gt = 0, eq = 0;
+        for (int jb = j_lo; jb < j_hi; jb += 128) {
+          uint32_t kk[4];
+          int cgt, ceq;
+          flags_of(jb + 4 * lane, kk, cgt, ceq);
+          gt += cgt;
+          eq += ceq;
+        }
+        gt = __reduce_add_sync(0xffffffffu, gt);
+        eq = __reduce_add_sync(0xffffffffu, eq);
         if (lane == 0) { s_cnt[0][warp] = gt; s_cnt[1][warp] = eq; }
         named_sync(1, kComputeThreads);
         int gt_before = 0, eq_before = 0;
         for (int ww = 0; ww < warp; ++ww) { gt_before += s_cnt[0][ww]; eq_before += s_cnt[1][ww]; }
-        for (int jb = j_lo; jb < j_hi; jb += 32) {
-          const int j = jb + lane;
-          bool fgt, feq;
-          if (all) {
-            fgt = j < j_hi;
-            feq = false;
-          } else {
-            const uint32_t key = j < j_hi ? keys[j] : 0u;
-            fgt = j < j_hi && key > thr;
-            feq = j < j_hi && key == thr;
+        for (int jb = j_lo; jb < j_hi; jb += 128) {
+          const int j0 = jb + 4 * lane;
+          uint32_t kk[4];
+          int cgt, ceq;
+          flags_of(j0, kk, cgt, ceq);
+          // exclusive scan of the (gt, eq) counts over the lanes, packed 16 + 16 bits
+          const int packed = cgt | (ceq << 16);
+          int incl = packed;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
           }
-          const uint32_t bgt = __ballot_sync(0xffffffffu, fgt);
-          const uint32_t beq = __ballot_sync(0xffffffffu, feq);
-          const uint32_t below = (1u << lane) - 1u;
-          const int my_gt = gt_before + __popc(bgt & below);
-          const int my_eq = eq_before + __popc(beq & below);
-          if (fgt || (feq && my_eq < need_eq)) idx[orow + my_gt + min(my_eq, need_eq)] = bk.cmp0 + j;
-          gt_before += __popc(bgt);
-          eq_before += __popc(beq);
+          const int tot = __shfl_sync(0xffffffffu, incl, 31);
+          int my_gt = gt_before + ((incl - packed) & 0xFFFF);
+          int my_eq = eq_before + ((incl - packed) >> 16);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = j0 + e;
+            const bool in = j < j_hi;
+            const bool fgt = in && (all || kk[e] > thr);
+            const bool feq = in && !all && kk[e] == thr;
+            if (fgt || (feq && my_eq < need_eq)) idx[orow + my_gt + min(my_eq, need_eq)] = bk.cmp0 + j;
+            my_gt += fgt ? 1 : 0;
+            my_eq += feq ? 1 : 0;
+          }
+          gt_before += tot & 0xFFFF;
+          eq_before += tot >> 16;
         }
         for (int i = m + tid; i < k_pad; i += kComputeThreads) idx[orow + i] = -1;
         named_sync(1, kComputeThreads);
@@ -350,7 +378,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 9) tc::tmem_dealloc(tmem, 64);
+  if (warp == kComputeWarps + 1) tc::tmem_dealloc(tmem, 64);
 }
 
 static int topk_tc_group(int max_vis) {

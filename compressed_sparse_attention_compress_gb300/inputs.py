@@ -113,12 +113,12 @@ WORKLOADS = {
     # packed THD varlen CSA: 16 sequences, lengths uniform in [1024, 16384] from seed 0
     "thd128k": Workload("thd128k", _thd_lengths(), 4, True, 64, 128, 128, H_I=8, d_I=64,
                         topk=1024, k_pad=1024, kl_mode="none", cap_align=128),
-    # sparse warm-up: L=32768, r=4, 64 x 128, indexer 8 x 64, top-k 2048, W=128,
-    # sparse main output + dense teacher over all visible entries
     # the sparse warm-up layer at L=8192 with k=512 (a small case of the headline
     # layer for profiling and parity: every query past 2048 tokens runs the selection)
     "warmup8k": Workload("warmup8k", [8192], 4, True, 64, 128, 128, H_I=8, d_I=64,
                          topk=512, k_pad=512, kl_mode="dense"),
+    # sparse warm-up: L=32768, r=4, 64 x 128, indexer 8 x 64, top-k 2048, W=128,
+    # sparse main output + dense teacher over all visible entries
     "warmup32k": Workload("warmup32k", [32768], 4, True, 64, 128, 128, H_I=8, d_I=64,
                           topk=2048, k_pad=2048, kl_mode="dense"),
 }

@@ -21,7 +21,10 @@
  * Compression.  Sequence b of length L_b owns n_b = floor(L_b / r) compressed
  *   entries (only complete groups, §4); cu_cmp[b] = sum of earlier n_b is the
  *   first packed compressed row of sequence b (csa_compressed_offsets).  Entry j
- *   is visible to local query position t once r(j+1)-1 <= t.
+ *   is visible to local query position t once r(j+1)-1 <= t.  Compressed
+ *   arrays (kv_cmp, v_cmp, kI) are capacity buffers of floor(T_cap / r) rows:
+ *   the tensor-core kernels load whole 128-row tiles and may read rows past
+ *   cu_cmp[B] (their values are never used).
  * Static capacity.  Buffers are sized for a fixed capacity and all metadata is
  *   read on the device, so no call synchronises with the host (§4.1 "Static
  *   capacity versus dynamic metadata").  Calls that need a bound on one
