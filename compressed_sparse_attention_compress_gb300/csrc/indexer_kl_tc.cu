@@ -12,17 +12,19 @@
 // block of 4 queries (4 x 64 = 256 query-head rows) and streams the key prefix
 // through shared memory with TMA tiled loads (128 keys x 128 dims, 128-byte
 // swizzle), each tile feeding 256 rows of tensor-core work.
-//   pass 1  S = Q K^T   (two M=128 tiles of query-head rows, N=128 keys):
-//           one thread per row keeps the row's online log-sum-exp -> lse_h.
+//   pass 1  S = Q K^T   (two M=128 tiles of query-head rows, N=128 keys, two
+//           tensor-memory buffers so the next tile's MMAs run during this
+//           tile's arithmetic): each row's online log-sum-exp -> lse_h, every
+//           row split over two threads (64 key columns each), merged at the end.
 //   pass 2  S^T = K Q^T (M=128 keys, N=256 query-heads) and the indexer tile
 //           I^T = kI qI^T (M=128 keys, N=32 = 4 queries x 8 heads): one thread
-//           per key forms, for two queries, p(j) = mean_h exp(s_h - lse_h), the
-//           indexer logit i = sum_h w_h ReLU(.), and accumulates sum p ln p,
-//           sum p i and the student's log-sum-exp;  KL = sum p ln p - sum p i + lse_i.
-// Warp roles: warps 0-7 compute (two warpgroups, one tensor-memory lane per
-// thread), warp 8 issues the TMA loads, warp 9 allocates tensor memory and
-// issues the MMAs.  Threads copy each score tile to registers and release it
-// at once, so the next tile's MMAs overlap the arithmetic.
+//           per (key, query) forms p(j) = mean_h exp(s_h - lse_h), the indexer
+//           logit i = sum_h w_h ReLU(.), and accumulates sum p ln p, sum p i
+//           and the student's log-sum-exp;  KL = sum p ln p - sum p i + lse_i.
+// Warp roles: warps 0-15 compute (four warpgroups, one tensor-memory lane per
+// thread; four warps per scheduler hide the exp2 and FMA latencies), warp 16
+// issues the TMA loads, warp 17 allocates tensor memory and issues the MMAs.
+// Threads copy each score tile to registers and release it at once.
 #include <math.h>
 
 #include "common.cuh"
@@ -41,7 +43,8 @@ constexpr int kHI = 8;          // indexer heads
 constexpr int kDI = 64;         // indexer head dim
 constexpr int kTK = 128;        // keys per tile
 constexpr int kStages = 3;
-constexpr int kComputeThreads = 256;
+constexpr int kComputeWarps = 16;
+constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kThreads = kComputeThreads + 64;
 
 constexpr uint32_t kQRegion = kQB * kNH * 128;       // 32 KB: 256 rows x 64 dims
@@ -55,7 +58,8 @@ constexpr uint32_t kSmemBytes = kStageOff + kStages * kStageBytes;
 static_assert(kStageOff % 1024 == 0, "stage alignment");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColI = 256;  // indexer tile columns in pass 2
+constexpr uint32_t kBufCols = 256;  // pass 1 score buffer d at columns [256 d, 256 d + 256)
+constexpr uint32_t kColI = 256;     // indexer tile columns in pass 2 (inside buffer 1)
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -111,19 +115,20 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
-  __shared__ __align__(8) uint64_t s_sfull, s_sfree, s_qfull, s_qempty;
+  __shared__ __align__(8) uint64_t s_sfull[2], s_sfree[2], s_qfull, s_qempty;
   __shared__ __align__(16) float s_L[kQB][kNH];  // per (query, head) log2 normaliser over C_t
   __shared__ float s_w[kQB][kHI];
-  __shared__ float s_red[8][2][4];       // per compute warp, per query: A, B, mI, lI
+  __shared__ float s_red[kComputeWarps][4];  // per compute warp: A, B, mI, lI
+  __shared__ float s_ml[2][kQB * kNH][2];    // pass 1 per column half: row max, row sum
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t bar_full = smem_u32(&s_full[0]), bar_empty = smem_u32(&s_empty[0]);
-  const uint32_t bar_sfull = smem_u32(&s_sfull), bar_sfree = smem_u32(&s_sfree);
+  const uint32_t bar_sfull = smem_u32(&s_sfull[0]), bar_sfree = smem_u32(&s_sfree[0]);
   const uint32_t bar_qfull = smem_u32(&s_qfull), bar_qempty = smem_u32(&s_qempty);
 
-  if (warp == 9) {
+  if (warp == kComputeWarps + 1) {
     tc::tmem_alloc(smem_u32(&s_tmem), kTmemCols);
     tc::tmem_relinquish();
   }
@@ -132,8 +137,10 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_sfull, 1);
-    mbar_init(bar_sfree, 8);  // one arrival per compute warp
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(bar_sfull + 8 * d, 1);
+      mbar_init(bar_sfree + 8 * d, kComputeWarps);  // one arrival per compute warp
+    }
     mbar_init(bar_qfull, 1);
     mbar_init(bar_qempty, 1);
     fence_mbar_init();
@@ -145,7 +152,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
   const uint32_t tmem = s_tmem;
   const int total = total_blocks(cu, B);
 
-  if (warp == 8) {
+  if (warp == kComputeWarps) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_map(&map_q);
@@ -178,13 +185,13 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kComputeWarps + 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t kIdP1 = tc::idesc_bf16(128, kTK, 0, 0);
       constexpr uint32_t kIdP2 = tc::idesc_bf16(kTK, kQB * kNH, 0, 0);
       constexpr uint32_t kIdI = tc::idesc_bf16(kTK, kQB * kHI, 0, 0);
-      uint32_t it = 0, nblk = 0;
+      uint32_t it = 0, nblk = 0, p1 = 0, nf0 = 0, nf1 = 0;
       for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
         Block bk;
         if (!block_of(cu, cu_cmp, B, r, total, k, bk) || bk.ntiles == 0) continue;
@@ -193,8 +200,12 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         for (int pass = 0; pass < 2; ++pass) {
           for (int i = 0; i < bk.ntiles; ++i, ++it) {
             const uint32_t s = it % kStages;
+            // pass 1 alternates the two score buffers; a pass 2 tile takes both
+            const uint32_t d = p1 & 1u;
+            const bool use0 = pass == 1 || d == 0, use1 = pass == 1 || d == 1;
             if (!mbar_wait_bounded(bar_full + 8 * s, (it / kStages) & 1u, status) ||
-                !mbar_wait_bounded(bar_sfree, (it & 1u) ^ 1u, status)) {
+                (use0 && !mbar_wait_bounded(bar_sfree, (nf0 & 1u) ^ 1u, status)) ||
+                (use1 && !mbar_wait_bounded(bar_sfree + 8, (nf1 & 1u) ^ 1u, status))) {
               s_abort = 1;
               break;
             }
@@ -208,8 +219,9 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
                   const uint64_t a = tc::smem_desc_sw128(base + kQOff + (ks >> 2) * kQRegion + g * 16384 + (ks & 3) * 32,
                                                          16, 1024);
                   const uint64_t bd = tc::smem_desc_sw128(st + (ks >> 2) * kKRegion + (ks & 3) * 32, 16, 1024);
-                  tc::mma_bf16(tmem + g * kTK, a, bd, kIdP1, ks > 0 ? 1u : 0u);
+                  tc::mma_bf16(tmem + d * kBufCols + g * kTK, a, bd, kIdP1, ks > 0 ? 1u : 0u);
                 }
+              ++p1;
             } else {
 #pragma unroll
               for (int ks = 0; ks < kDim / 16; ++ks) {
@@ -224,7 +236,8 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
                 tc::mma_bf16(tmem + kColI, a, bd, kIdI, ks > 0 ? 1u : 0u);
               }
             }
-            tc::mma_commit(bar_sfull);
+            if (use0) { tc::mma_commit(bar_sfull); ++nf0; }
+            if (use1) { tc::mma_commit(bar_sfull + 8); ++nf1; }
             tc::mma_commit(bar_empty + 8 * s);
           }
           if (s_abort) break;
@@ -234,11 +247,11 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
     }
   } else {
     // ---------------- compute warpgroups ----------------
-    const int g = warp >> 2;                 // warpgroup: M-tile (pass 1) / query pair (pass 2)
+    const int wg = warp >> 2;                // warpgroup 0..3
     const int quad = warp & 3;               // tensor-memory lane quadrant
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const int rowl = quad * 32 + lane;       // tensor-memory lane of this thread
-    uint32_t it = 0;
+    uint32_t p1 = 0, nf0 = 0, nf1 = 0;       // score-buffer uses, as counted by the MMA warp
     for (int k = blockIdx.x; k < total; k += gridDim.x) {
       Block bk;
       if (!block_of(cu, cu_cmp, B, r, total, k, bk)) continue;
@@ -253,39 +266,42 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         const int q = tid / kHI, h = tid % kHI;
         s_w[q][h] = q < bk.nq ? __bfloat162float(w[(int64_t)(bk.seq0 + bk.q0 + q) * kHI + h]) : 0.f;
       }
-      // ---- pass 1: row (query, head) online log-sum-exp ----
+      // ---- pass 1: row (query, head) online log-sum-exp; warpgroup = (M-tile, column half) ----
       {
-        const int q = 2 * g + (rowl >> 6), h = rowl & 63;
+        const int mt = wg >> 1, half = wg & 1;
+        const int q = 2 * mt + (rowl >> 6), h = rowl & 63;
         const int nvis = (bk.q0 + q + 1) / r;
         float m = -INFINITY, l = 0.f;
-        for (int i = 0; i < bk.ntiles; ++i, ++it) {
-          if (!mbar_wait_bounded(bar_sfull, it & 1u, status)) { s_abort = 1; break; }
+        for (int i = 0; i < bk.ntiles; ++i) {
+          const uint32_t d = p1++ & 1u;
+          if (!mbar_wait_bounded(bar_sfull + 8 * d, (d ? nf1 : nf0) & 1u, status)) { s_abort = 1; break; }
           tc::fence_after_sync();
-          float x[kTK];
+          float x[kTK / 2];
 #pragma unroll
-          for (int c0 = 0; c0 < kTK; c0 += 32) {
+          for (int c0 = 0; c0 < kTK / 2; c0 += 32) {
             uint32_t rs[32];
-            tc::tmem_ld32_sync(tmem + lane_off + g * kTK + c0, rs);
+            tc::tmem_ld32_sync(tmem + lane_off + d * kBufCols + mt * kTK + half * (kTK / 2) + c0, rs);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[c0 + j] = __uint_as_float(rs[j]);
+            for (int jj = 0; jj < 32; ++jj) x[c0 + jj] = __uint_as_float(rs[jj]);
           }
           tc::fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_sfree);
-          const int nv = nvis - i * kTK;  // valid columns of this tile
-          if (nv < kTK) {                 // only the last tile of a row is partial
+          if (lane == 0) mbar_arrive(bar_sfree + 8 * d);
+          if (d) ++nf1; else ++nf0;
+          const int nv = nvis - i * kTK - half * (kTK / 2);  // valid columns of this thread's half
+          if (nv < kTK / 2) {               // only the last tile of a row is partial
 #pragma unroll
-            for (int c = 0; c < kTK; ++c) x[c] = c < nv ? x[c] : -INFINITY;
+            for (int c = 0; c < kTK / 2; ++c) x[c] = c < nv ? x[c] : -INFINITY;
           }
           float tmax = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < kTK; c += 4)
+          for (int c = 0; c < kTK / 2; c += 4)
             tmax = fmaxf(tmax, fmaxf(fmaxf(x[c], x[c + 1]), fmaxf(x[c + 2], x[c + 3])));
           const float mn = fmaxf(m, tmax * scale_log2);  // scale > 0: max commutes with it
           if (mn != -INFINITY) {
             float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-            for (int c = 0; c < kTK; c += 2) {
+            for (int c = 0; c < kTK / 2; c += 2) {
               acc0 += ex2(fmaf(x[c], scale_log2, -mn));
               acc1 += ex2(fmaf(x[c + 1], scale_log2, -mn));
             }
@@ -293,63 +309,76 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
             m = mn;
           }
         }
-        if (q < kQB) s_L[q][h] = (l > 0.f) ? m + __log2f(l) : INFINITY;  // +inf: contributes nothing
+        s_ml[half][mt * kTK + rowl][0] = m;
+        s_ml[half][mt * kTK + rowl][1] = l;
+        named_sync(1, kComputeThreads);
+        if (half == 0 && q < kQB) {  // merge the two column halves of the row
+          const float m2 = s_ml[1][mt * kTK + rowl][0], l2 = s_ml[1][mt * kTK + rowl][1];
+          const float mx = fmaxf(m, m2);
+          const float ls = (mx == -INFINITY) ? 0.f : l * ex2(m - mx) + l2 * ex2(m2 - mx);
+          s_L[q][h] = (ls > 0.f) ? mx + __log2f(ls) : INFINITY;  // +inf: contributes nothing
+        }
       }
       named_sync(1, kComputeThreads);
       if (*(volatile int*)&s_abort) break;  // uniform: read after the barrier
-      // ---- pass 2: one thread per key, queries 2g and 2g+1 ----
-      float A[2] = {0.f, 0.f}, Bs[2] = {0.f, 0.f}, mI[2] = {-INFINITY, -INFINITY}, lI[2] = {0.f, 0.f};
-      for (int i = 0; i < bk.ntiles; ++i, ++it) {
-        if (!mbar_wait_bounded(bar_sfull, it & 1u, status)) { s_abort = 1; break; }
-        tc::fence_after_sync();
-        float x[kTK];
-        uint32_t ri[16];
-#pragma unroll
-        for (int c0 = 0; c0 < kTK; c0 += 32) {
-          uint32_t rs[32];
-          tc::tmem_ld32_sync(tmem + lane_off + g * kTK + c0, rs);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x[c0 + j] = __uint_as_float(rs[j]);
+      // ---- pass 2: one thread per key, warpgroup q = query q ----
+      const int q = wg;
+      const int nvis_q = (bk.q0 + q + 1) / r;
+      const bool q_ok = q < bk.nq;
+      float A = 0.f, Bs = 0.f, mI = -INFINITY, lI = 0.f;
+      for (int i = 0; i < bk.ntiles; ++i) {
+        if (!mbar_wait_bounded(bar_sfull, nf0 & 1u, status) || !mbar_wait_bounded(bar_sfull + 8, nf1 & 1u, status)) {
+          s_abort = 1;
+          break;
         }
-        tc::tmem_ld16_sync(tmem + lane_off + kColI + g * 16, ri);
+        tc::fence_after_sync();
+        float x[kNH];
+        uint32_t ri[8];
+#pragma unroll
+        for (int c0 = 0; c0 < kNH; c0 += 32) {
+          uint32_t rs[32];
+          tc::tmem_ld32_sync(tmem + lane_off + q * kNH + c0, rs);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) x[c0 + jj] = __uint_as_float(rs[jj]);
+        }
+        tc::tmem_ld8_sync(tmem + lane_off + kColI + q * kHI, ri);
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfree);
+        if (lane == 0) {
+          mbar_arrive(bar_sfree);
+          mbar_arrive(bar_sfree + 8);
+        }
+        ++nf0;
+        ++nf1;
         const int j = i * kTK + rowl;  // entry index within the sequence
+        if (q_ok && j < nvis_q) {
+          float pa = 0.f, pb = 0.f;
+          const float4* L4 = reinterpret_cast<const float4*>(&s_L[q][0]);
 #pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          const int q = 2 * g + qq;
-          const int nvis = (bk.q0 + q + 1) / r;
-          if (q < bk.nq && j < nvis) {
-            float p0 = 0.f, p1 = 0.f;
-            const float4* L4 = reinterpret_cast<const float4*>(&s_L[q][0]);
+          for (int h4 = 0; h4 < kNH / 4; ++h4) {
+            const float4 L = L4[h4];
+            pa += ex2(fmaf(x[4 * h4 + 0], scale_log2, -L.x));
+            pb += ex2(fmaf(x[4 * h4 + 1], scale_log2, -L.y));
+            pa += ex2(fmaf(x[4 * h4 + 2], scale_log2, -L.z));
+            pb += ex2(fmaf(x[4 * h4 + 3], scale_log2, -L.w));
+          }
+          const float p = (pa + pb) * (1.f / kNH);
+          float iv = 0.f;
 #pragma unroll
-            for (int h4 = 0; h4 < kNH / 4; ++h4) {
-              const float4 L = L4[h4];
-              p0 += ex2(fmaf(x[qq * kNH + 4 * h4 + 0], scale_log2, -L.x));
-              p1 += ex2(fmaf(x[qq * kNH + 4 * h4 + 1], scale_log2, -L.y));
-              p0 += ex2(fmaf(x[qq * kNH + 4 * h4 + 2], scale_log2, -L.z));
-              p1 += ex2(fmaf(x[qq * kNH + 4 * h4 + 3], scale_log2, -L.w));
-            }
-            const float p = (p0 + p1) * (1.f / kNH);
-            float iv = 0.f;
-#pragma unroll
-            for (int h = 0; h < kHI; ++h) iv = fmaf(s_w[q][h], fmaxf(__uint_as_float(ri[qq * kHI + h]), 0.f), iv);
-            if (p > 0.f) A[qq] = fmaf(p, __logf(p), A[qq]);
-            Bs[qq] = fmaf(p, iv, Bs[qq]);
-            if (iv > mI[qq]) {
-              lI[qq] = lI[qq] * __expf(mI[qq] - iv) + 1.f;
-              mI[qq] = iv;
-            } else {
-              lI[qq] += __expf(iv - mI[qq]);
-            }
+          for (int hh = 0; hh < kHI; ++hh) iv = fmaf(s_w[q][hh], fmaxf(__uint_as_float(ri[hh]), 0.f), iv);
+          if (p > 0.f) A = fmaf(p, __logf(p), A);
+          Bs = fmaf(p, iv, Bs);
+          if (iv > mI) {
+            lI = lI * __expf(mI - iv) + 1.f;
+            mI = iv;
+          } else {
+            lI += __expf(iv - mI);
           }
         }
       }
       // reduce the per-key partials over the warpgroup's 128 threads
-#pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        float a = A[qq], bs = Bs[qq], mm = mI[qq], ll = lI[qq];
+      {
+        float a = A, bs = Bs, mm = mI, ll = lI;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
           a += __shfl_xor_sync(0xffffffffu, a, o);
@@ -361,31 +390,29 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
           mm = mx;
         }
         if (lane == 0) {
-          s_red[warp][qq][0] = a;
-          s_red[warp][qq][1] = bs;
-          s_red[warp][qq][2] = mm;
-          s_red[warp][qq][3] = ll;
+          s_red[warp][0] = a;
+          s_red[warp][1] = bs;
+          s_red[warp][2] = mm;
+          s_red[warp][3] = ll;
         }
       }
       named_sync(1, kComputeThreads);
-      if (tid < kQB) {
-        const int q = tid, gg = q >> 1, qq = q & 1;
-        if (q < bk.nq) {
-          float a = 0.f, bs = 0.f, mm = -INFINITY;
-          for (int ww = 0; ww < 4; ++ww) {
-            a += s_red[gg * 4 + ww][qq][0];
-            bs += s_red[gg * 4 + ww][qq][1];
-            mm = fmaxf(mm, s_red[gg * 4 + ww][qq][2]);
-          }
-          float ll = 0.f;
-          for (int ww = 0; ww < 4; ++ww) {
-            const float m2 = s_red[gg * 4 + ww][qq][2];
-            if (m2 != -INFINITY) ll += s_red[gg * 4 + ww][qq][3] * __expf(m2 - mm);
-          }
-          const int nvis = (bk.q0 + q + 1) / r;
-          kl_rows[bk.seq0 + bk.q0 + q] = nvis > 0 ? a - bs + (mm + __logf(ll)) : 0.f;
-          csize[bk.seq0 + bk.q0 + q] = nvis;
+      if (tid < kQB && tid < bk.nq) {
+        const int qq = tid;
+        float a = 0.f, bs = 0.f, mm = -INFINITY;
+        for (int ww = 0; ww < 4; ++ww) {
+          a += s_red[qq * 4 + ww][0];
+          bs += s_red[qq * 4 + ww][1];
+          mm = fmaxf(mm, s_red[qq * 4 + ww][2]);
         }
+        float ll = 0.f;
+        for (int ww = 0; ww < 4; ++ww) {
+          const float m2 = s_red[qq * 4 + ww][2];
+          if (m2 != -INFINITY) ll += s_red[qq * 4 + ww][3] * __expf(m2 - mm);
+        }
+        const int nvis = (bk.q0 + qq + 1) / r;
+        kl_rows[bk.seq0 + bk.q0 + qq] = nvis > 0 ? a - bs + (mm + __logf(ll)) : 0.f;
+        csize[bk.seq0 + bk.q0 + qq] = nvis;
       }
       named_sync(1, kComputeThreads);
       if (*(volatile int*)&s_abort) break;
@@ -395,7 +422,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 9) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kComputeWarps + 1) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 bool indexer_kl_dense_tc_supported(const KLArgs& a, bool fp32) {
