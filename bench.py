@@ -320,7 +320,8 @@ def f_launches(wl) -> int:
         n += 1 + 1 + (1 if wl.separate_v else 0) + (1 if wl.H_I > 0 else 0)   # offsets + compress calls
         if wl.H_I > 0:
             n += 2                                                              # top-k + capacity fill
-    n += 1                                                                      # attention
+    ws_attn = not wl.io_fp32 and wl.H == 64 and wl.d == 128 and not wl.separate_v
+    n += 2 if ws_attn else 1                                                    # (capacity rows) + attention
     if wl.kl_mode != "none":
         dense_tc = (wl.kl_mode == "dense" and not wl.io_fp32 and wl.H == 64 and wl.d == 128
                     and wl.H_I == 8 and wl.d_I == 64)

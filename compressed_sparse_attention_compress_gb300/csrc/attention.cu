@@ -287,6 +287,7 @@ static cudaError_t dispatch_heads(AttnKind kind, const AttnArgs& a, cudaStream_t
 cudaError_t launch_attention(AttnKind kind, const AttnArgs& a, bool fp32, cudaStream_t stream) {
   // 64 heads x 128 dims in bf16 (every workload of the pages) run on tcgen05;
   // other head counts / dims and float32 I/O use the warp-level kernel above.
+  if (attention_ws_supported(a, fp32)) return launch_attention_ws(kind, a, stream);
   if (attention_tc_supported(a, fp32)) return launch_attention_tc(kind, a, stream);
   if (fp32) {
     if (a.d == 64) return dispatch_heads<float, float, 64>(kind, a, stream);

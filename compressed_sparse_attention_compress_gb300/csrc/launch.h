@@ -48,6 +48,8 @@ struct AttnArgs {
   int* status;
 };
 cudaError_t launch_attention(AttnKind kind, const AttnArgs& a, bool fp32, cudaStream_t stream);
+bool attention_ws_supported(const AttnArgs& a, bool fp32);
+cudaError_t launch_attention_ws(AttnKind kind, const AttnArgs& a, cudaStream_t stream);
 bool attention_tc_supported(const AttnArgs& a, bool fp32);
 cudaError_t launch_attention_tc(AttnKind kind, const AttnArgs& a, cudaStream_t stream);
 
