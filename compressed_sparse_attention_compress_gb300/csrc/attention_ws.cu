@@ -342,7 +342,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
     }
     cp_async_wait<0>();
   } else if (warp >= kMmaWarp) {
-    // =================== MMA issuer of group g: QK(n), then PV(n-1) ===================
+    // =================== MMA issuer of group g: whatever is ready, PV first ===================
     const int g = warp - kMmaWarp;
     if (lane == 0) {
       constexpr uint32_t kIdQK = tc::idesc_bf16(kTK, kNH, 0, 0);
@@ -354,64 +354,67 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       const uint64_t dv0 = tc::smem_desc_sw128(base + kStageOff + (g * 2) * kTileBytes, kTileRegion, 1024);
       constexpr uint64_t kStageStep = kTileBytes >> 4;
       const uint32_t t_s = tmem + g * 128, t_o = tmem + g * 128 + kNH;
-      uint32_t nq = 0, nqp = 0;
-      int prev_flags = 0;
-      bool ok = true;
-      for (uint32_t n = 0; ok; ++n) {
-        // ---- QK(n) ----
-        const uint32_t st = n & 1u;
-        WS_T0(m_full);
-        ok = mbar_wait_bounded(full_bar(g, st), (n >> 1) & 1u, status);
-        WS_ADD(0, m_full);
-        if (!ok) break;
-        const int flags = s_meta[g][st].flags;
-        const bool done = (flags & kDone) != 0;
-        if (!done) {
-          WS_T0(m_sfree);
-          if (n > 0) ok = mbar_wait_bounded(smem_u32(&s_sfree[g]), (n - 1) & 1u, status);
-          WS_ADD(1, m_sfree);
-          WS_T0(m_qfull);
-          if (ok && (flags & kFirst)) ok = mbar_wait_bounded(smem_u32(&s_qfull[g]), nq++ & 1u, status);
-          WS_ADD(2, m_qfull);
-          if (!ok) break;
-          tc::fence_after_sync();
-          const uint64_t dk = dk0 + st * kStageStep;
+      uint32_t kq = 0, kp = 0, nqq = 0, nqp = 0;  // QKs / PVs issued, queries started by QK / PV
+      bool end = false;                           // the end-of-stream tile was seen
+      uint64_t last = globaltimer_ns();
+      while (!(end && kp == kq)) {
+        bool progress = false;
+        // PV(kp): frees the stage for the producer as early as possible
+        if (kp < kq && mbar_test(smem_u32(&s_pfull[g]), kp & 1u)) {
+          const uint32_t sp = kp & 1u;
+          const bool first = (s_meta[g][sp].flags & kFirst) != 0;
+          if (!first || nqp == 0 || mbar_test(smem_u32(&s_ofree[g]), (nqp - 1) & 1u)) {
+            if (first) ++nqp;
+            tc::fence_after_sync();
+            const uint64_t dv = dv0 + sp * kStageStep;
 #pragma unroll
-          for (int ks = 0; ks < kDim / 16; ++ks) {
-            const uint32_t off = ((ks >> 2) * kTileRegion + (ks & 3) * 32) >> 4;
-            const uint32_t offq = ((ks >> 2) * kQRegion + (ks & 3) * 32) >> 4;
-            tc::mma_bf16(t_s, dk + off, dq + offq, kIdQK, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < kTK / 16; ++ks) {
+              const uint32_t off = (ks * 2048) >> 4;
+              tc::mma_bf16(t_o, dv + off, dp + off, kIdPV, (first && ks == 0) ? 0u : 1u);
+            }
+            tc::mma_commit(smem_u32(&s_odone[g]));
+            tc::mma_commit(empty_bar(g, sp));
+            ++kp;
+            progress = true;
           }
-          tc::mma_commit(smem_u32(&s_sfull[g]));
-          if (flags & kLast) tc::mma_commit(smem_u32(&s_qempty[g]));
         }
-        // ---- PV(n-1) ----
-        if (n > 0) {
-          const uint32_t sp = (n - 1) & 1u;
-          const bool first = (prev_flags & kFirst) != 0;
-          WS_T0(m_pfull);
-          ok = mbar_wait_bounded(smem_u32(&s_pfull[g]), (n - 1) & 1u, status);
-          WS_ADD(3, m_pfull);
-          WS_T0(m_ofree);
-          if (ok && first && nqp > 0) ok = mbar_wait_bounded(smem_u32(&s_ofree[g]), (nqp - 1) & 1u, status);
-          WS_ADD(4, m_ofree);
-          if (!ok) break;
-          if (first) ++nqp;
-          tc::fence_after_sync();
-          const uint64_t dv = dv0 + sp * kStageStep;
+        // QK(kq): its tile is gathered and the softmax has read S^T(kq - 1)
+        if (!end && kq < kp + 2 && mbar_test(full_bar(g, kq & 1u), (kq >> 1) & 1u)) {
+          const uint32_t st = kq & 1u;
+          const int flags = s_meta[g][st].flags;
+          if (flags & kDone) {
+            end = true;
+            progress = true;
+          } else if ((kq == 0 || mbar_test(smem_u32(&s_sfree[g]), (kq - 1) & 1u)) &&
+                     (!(flags & kFirst) || mbar_test(smem_u32(&s_qfull[g]), nqq & 1u))) {
+            if (flags & kFirst) ++nqq;
+            tc::fence_after_sync();
+            const uint64_t dk = dk0 + st * kStageStep;
 #pragma unroll
-          for (int ks = 0; ks < kTK / 16; ++ks) {
-            const uint32_t off = (ks * 2048) >> 4;
-            tc::mma_bf16(t_o, dv + off, dp + off, kIdPV, (first && ks == 0) ? 0u : 1u);
+            for (int ks = 0; ks < kDim / 16; ++ks) {
+              const uint32_t off = ((ks >> 2) * kTileRegion + (ks & 3) * 32) >> 4;
+              const uint32_t offq = ((ks >> 2) * kQRegion + (ks & 3) * 32) >> 4;
+              tc::mma_bf16(t_s, dk + off, dq + offq, kIdQK, ks > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(smem_u32(&s_sfull[g]));
+            if (flags & kLast) tc::mma_commit(smem_u32(&s_qempty[g]));
+            ++kq;
+            progress = true;
           }
-          tc::mma_commit(smem_u32(&s_odone[g]));
-          tc::mma_commit(empty_bar(g, sp));
         }
-        WS_CNT(6);
-        if (done) break;
-        prev_flags = flags;
+        if (progress) {
+          WS_CNT(6);
+          last = globaltimer_ns();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer_ns() - last > kWaitLimitNs) {
+            raise_status(status, CSA_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          __nanosleep(20);
+        }
       }
-      if (!ok) *abort_flag = 1;
     }
   } else {
     // =================== softmax: group g, warp sw = (head half, lane quadrant) ===================
@@ -514,12 +517,10 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       if (k > 0) ok = ok && mbar_wait_bounded(smem_u32(&s_odone[g]), (k - 1) & 1u, status);
       WS_ADD(3, s_od);
       WS_T0(s_vote);
-      if (bar_or(gbar, kSoftThreads, !ok)) {
-        *abort_flag = 1;
-        break;
-      }
-      tc::fence_after_sync();
-      if (bar_or(gbar, kSoftThreads, excess > kTau)) {
+      // one vote per tile: a score above the reference by more than the slack, or a
+      // failed wait (the abort is then decided uniformly inside)
+      const bool bad = !ok || *abort_flag != 0;
+      if (bar_or(gbar, kSoftThreads, excess > kTau || bad)) {
         // new reference: the tile's per-head column maxima (t + m is the scaled score)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -527,7 +528,11 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
           const int v = __reduce_max_sync(0xffffffffu, ord_of(valid ? sc : -INFINITY));
           if (lane == 0) s_wmax[g][quad][hh * 32 + j] = v;
         }
-        bar_sync(gbar, kSoftThreads);
+        if (bar_or(gbar, kSoftThreads, bad)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc::fence_after_sync();
         if (tig < kNH) {
           const float mo = fresh ? -INFINITY : m_g[tig];
           float mn = mo;
@@ -568,33 +573,36 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       // ---- this thread's half of the key's P^T row: 32 heads -> 4 swizzled 16-byte chunks ----
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t pk[4] = {0u, 0u, 0u, 0u};
-        uint32_t lv[8];
-        if (fresh) {
+        uint32_t pk[4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) lv[j] = 0u;
-        } else {
-          tc::tmem_ld8_sync(t_l + c * 8, lv);
+        for (int j = 0; j < 4; ++j) {
+          const int h = c * 8 + 2 * j;
+          t[h] = valid ? ex2(t[h]) : 0.f;  // t now holds p
+          t[h + 1] = valid ? ex2(t[h + 1]) : 0.f;
+          pk[j] = pack_bf16x2(t[h], t[h + 1]);
         }
-        if (valid) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int h = c * 8 + 2 * j;
-            const float p0 = ex2(t[h]), p1 = ex2(t[h + 1]);
-            lv[2 * j] = __float_as_uint(__uint_as_float(lv[2 * j]) + p0);
-            lv[2 * j + 1] = __float_as_uint(__uint_as_float(lv[2 * j + 1]) + p1);
-            pk[j] = pack_bf16x2(p0, p1);
-          }
-        }
-        tc::tmem_st8(t_l + c * 8, lv);
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + tc::sw128_offset(key, hh * 4 + c)),
                      "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]));
       }
-      tc::tmem_wait_st();
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s_pfull[g]));
+      // running sums (off the P^T -> PV path)
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t lv[16];
+        if (fresh) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) lv[j] = __float_as_uint(t[c2 * 16 + j]);
+        } else {
+          tc::tmem_ld16_sync(t_l + c2 * 16, lv);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) lv[j] = __float_as_uint(__uint_as_float(lv[j]) + t[c2 * 16 + j]);
+        }
+        tc::tmem_st16(t_l + c2 * 16, lv);
+      }
+      tc::tmem_wait_st();
       WS_ADD(5, s_p);
       WS_CNT(7);
       have_o = true;
