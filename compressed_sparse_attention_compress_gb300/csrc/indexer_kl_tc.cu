@@ -116,7 +116,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
   __shared__ __align__(8) uint64_t s_sfull[2], s_sfree[2], s_qfull, s_qempty;
-  __shared__ __align__(16) float s_L[kQB][kNH];  // per (query, head) log2 normaliser over C_t
+  __shared__ __align__(16) float s_L[kQB][kNH];  // per (query, head) minus the log2 normaliser over C_t
   __shared__ float s_w[kQB][kHI];
   __shared__ float s_red[kComputeWarps][4];  // per compute warp: A, B, mI, lI
   __shared__ float s_ml[2][kQB * kNH][2];    // pass 1 per column half: row max, row sum
@@ -299,13 +299,21 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
             tmax = fmaxf(tmax, fmaxf(fmaxf(x[c], x[c + 1]), fmaxf(x[c + 2], x[c + 3])));
           const float mn = fmaxf(m, tmax * scale_log2);  // scale > 0: max commutes with it
           if (mn != -INFINITY) {
-            float acc0 = 0.f, acc1 = 0.f;
+            // packed pairs: one f32x2 FMA and one f32x2 add per two columns
+            const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-mn, -mn);
+            uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-            for (int c = 0; c < kTK / 2; c += 2) {
-              acc0 += ex2(fmaf(x[c], scale_log2, -mn));
-              acc1 += ex2(fmaf(x[c + 1], scale_log2, -mn));
+            for (int c = 0; c < kTK / 2; c += 4) {
+              float a0, a1, a2, a3;
+              f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sc2, nm2), a0, a1);
+              f2_unpack(f2_fma(f2_pack(x[c + 2], x[c + 3]), sc2, nm2), a2, a3);
+              acc0 = f2_add(acc0, f2_pack(ex2(a0), ex2(a1)));
+              acc1 = f2_add(acc1, f2_pack(ex2(a2), ex2(a3)));
             }
-            l = l * ex2(m - mn) + (acc0 + acc1);
+            float s0, s1, s2, s3;
+            f2_unpack(acc0, s0, s1);
+            f2_unpack(acc1, s2, s3);
+            l = l * ex2(m - mn) + ((s0 + s1) + (s2 + s3));
             m = mn;
           }
         }
@@ -316,7 +324,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
           const float m2 = s_ml[1][mt * kTK + rowl][0], l2 = s_ml[1][mt * kTK + rowl][1];
           const float mx = fmaxf(m, m2);
           const float ls = (mx == -INFINITY) ? 0.f : l * ex2(m - mx) + l2 * ex2(m2 - mx);
-          s_L[q][h] = (ls > 0.f) ? mx + __log2f(ls) : INFINITY;  // +inf: contributes nothing
+          s_L[q][h] = (ls > 0.f) ? -(mx + __log2f(ls)) : -INFINITY;  // negated; -inf: contributes nothing
         }
       }
       named_sync(1, kComputeThreads);
@@ -352,17 +360,22 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         ++nf1;
         const int j = i * kTK + rowl;  // entry index within the sequence
         if (q_ok && j < nvis_q) {
-          float pa = 0.f, pb = 0.f;
-          const float4* L4 = reinterpret_cast<const float4*>(&s_L[q][0]);
+          const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+          uint64_t pa = f2_pack(0.f, 0.f), pb = pa;
+          const float4* L4 = reinterpret_cast<const float4*>(&s_L[q][0]);  // -lse_h
 #pragma unroll
           for (int h4 = 0; h4 < kNH / 4; ++h4) {
             const float4 L = L4[h4];
-            pa += ex2(fmaf(x[4 * h4 + 0], scale_log2, -L.x));
-            pb += ex2(fmaf(x[4 * h4 + 1], scale_log2, -L.y));
-            pa += ex2(fmaf(x[4 * h4 + 2], scale_log2, -L.z));
-            pb += ex2(fmaf(x[4 * h4 + 3], scale_log2, -L.w));
+            float a0, a1, a2, a3;
+            f2_unpack(f2_fma(f2_pack(x[4 * h4 + 0], x[4 * h4 + 1]), sc2, f2_pack(L.x, L.y)), a0, a1);
+            f2_unpack(f2_fma(f2_pack(x[4 * h4 + 2], x[4 * h4 + 3]), sc2, f2_pack(L.z, L.w)), a2, a3);
+            pa = f2_add(pa, f2_pack(ex2(a0), ex2(a1)));
+            pb = f2_add(pb, f2_pack(ex2(a2), ex2(a3)));
           }
-          const float p = (pa + pb) * (1.f / kNH);
+          float p0, p1, p2, p3;
+          f2_unpack(pa, p0, p1);
+          f2_unpack(pb, p2, p3);
+          const float p = ((p0 + p1) + (p2 + p3)) * (1.f / kNH);
           float iv = 0.f;
 #pragma unroll
           for (int hh = 0; hh < kHI; ++hh) iv = fmaf(s_w[q][hh], fmaxf(__uint_as_float(ri[hh]), 0.f), iv);
