@@ -35,15 +35,22 @@ namespace {
 
 constexpr int kHI = 8, kDI = 64;
 constexpr int kTK = 128;                 // entries per tile
-constexpr int kStages = 4;
-constexpr int kComputeWarps = 16;
-constexpr int kComputeThreads = 32 * kComputeWarps;
-constexpr int kThreads = kComputeThreads + 64;
 constexpr int kBins = 2048;
 constexpr uint32_t kTileBytes = kTK * 128;  // 16 KB
 constexpr uint32_t kQIOff = 0;              // up to 32 rows x 128 B
 constexpr uint32_t kStageOff = 4096;
-constexpr uint32_t kKeysOff = kStageOff + kStages * kTileBytes;  // scores start here
+
+// Two shapes: 16 compute warps and a 4-stage ring, one CTA per SM; or 8 compute
+// warps and a 2-stage ring, two CTAs per SM (one CTA selects while the other
+// scores).
+template <int CW>
+struct TopkCfg {
+  static constexpr int kWarps = CW;
+  static constexpr int kStages = CW == 8 ? 2 : 4;
+  static constexpr int kCtasPerSm = CW == 8 ? 2 : 1;
+  static constexpr int kThreads = 32 * CW + 64;
+  static constexpr uint32_t kKeysOff = kStageOff + kStages * kTileBytes;  // scores start here
+};
 
 __device__ __forceinline__ uint32_t order_key(float v) {
   if (v == 0.f) v = 0.f;  // -0 and +0 are the same score
@@ -90,13 +97,18 @@ __device__ __forceinline__ bool qblock_of(const int32_t* __restrict__ cu, const 
 
 }  // namespace
 
-template <int G>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int G, int CW>
+__global__ void __launch_bounds__(TopkCfg<CW>::kThreads, TopkCfg<CW>::kCtasPerSm)
 indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_constant__ CUtensorMap map_ki,
                        const __nv_bfloat16* __restrict__ w, const int32_t* __restrict__ cu,
                        const int32_t* __restrict__ cu_cmp, int B, int r, int topk, int k_pad, int max_vis,
                        int32_t* __restrict__ idx, int* status) {
   constexpr int kN = G * kHI;  // MMA N: query-head rows
+  constexpr int kComputeWarps = CW;
+  constexpr int kComputeThreads = 32 * CW;
+  constexpr int kStages = TopkCfg<CW>::kStages;
+  constexpr uint32_t kKeysOff = TopkCfg<CW>::kKeysOff;
+  constexpr int kQPW = G * 4 / CW > 1 ? G * 4 / CW : 1;  // queries scored per warpgroup
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_dfull[2], s_dfree[2];
@@ -195,7 +207,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
     }
   } else {
     // ---------------- compute warps: scores, then selection ----------------
-    const int g = warp >> 2, quad = warp & 3;  // warpgroup g scores query g of the block
+    const int g = warp >> 2, quad = warp & 3;  // warpgroup g scores queries kQPW g ... of the block
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const int rowl = quad * 32 + lane;
     uint32_t it = 0;
@@ -209,22 +221,29 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
           s_w[q][h] = q < bk.nq ? __bfloat162float(w[(int64_t)(bk.seq0 + bk.q0 + q) * kHI + h]) : 0.f;
         }
         named_sync(1, kComputeThreads);
-        const bool active = g < G;  // this warpgroup's query exists in the tile
+        const bool active = g * kQPW < G;  // this warpgroup's queries exist in the tile
         for (int i = 0; i < bk.ntiles; ++i, ++it) {
           const uint32_t d = it & 1u;
           if (!mbar_wait_bounded(bar_dfull + 8 * d, (it >> 1) & 1u, status)) { s_abort = 1; break; }
           tc::fence_after_sync();
-          uint32_t rv[8];
-          if (active) tc::tmem_ld8_sync(tmem + lane_off + d * 32 + g * kHI, rv);
+          uint32_t rv[8 * kQPW];
+          if (active) {
+            if constexpr (kQPW == 2) tc::tmem_ld16_sync(tmem + lane_off + d * 32 + g * kQPW * kHI, rv);
+            else tc::tmem_ld8_sync(tmem + lane_off + d * 32 + g * kQPW * kHI, rv);
+          }
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_dfree + 8 * d);
           const int j = i * kTK + rowl;
           if (active && j < bk.nvis_max) {
-            float sc = 0.f;
 #pragma unroll
-            for (int h = 0; h < kHI; ++h) sc = fmaf(s_w[g][h], fmaxf(__uint_as_float(rv[h]), 0.f), sc);
-            sKey[(size_t)g * vstride + j] = order_key(sc);
+            for (int qq = 0; qq < kQPW; ++qq) {
+              const int q = g * kQPW + qq;
+              float sc = 0.f;
+#pragma unroll
+              for (int h = 0; h < kHI; ++h) sc = fmaf(s_w[q][h], fmaxf(__uint_as_float(rv[qq * kHI + h]), 0.f), sc);
+              sKey[(size_t)q * vstride + j] = order_key(sc);
+            }
           }
         }
         named_sync(1, kComputeThreads);
@@ -381,19 +400,33 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   if (warp == kComputeWarps + 1) tc::tmem_dealloc(tmem, 64);
 }
 
-static int topk_tc_group(int max_vis) {
+// Shared memory a CTA may use for scores: per-SM capacity split over the CTAs
+// resident on it, less static arrays (about 10 KB), the 1 KB every block
+// reserves, alignment slack and the fixed front part.
+template <int CW>
+static size_t topk_key_budget() {
+  const size_t per_cta = 233472 / TopkCfg<CW>::kCtasPerSm;
+  return per_cta - 10 * 1024 - 1024 - 1024 - TopkCfg<CW>::kKeysOff;
+}
+
+struct TopkShape {
+  int G, CW;  // queries per block, compute warps (0: unsupported)
+};
+
+static TopkShape topk_tc_shape(int max_vis) {
   const size_t per_query = (size_t)((max_vis + 3) & ~3) * 4;
-  const size_t budget = 232448 - 1024 - kKeysOff - 12 * 1024;  // dynamic smem left for scores
-  if (4 * per_query <= budget) return 4;
-  if (2 * per_query <= budget) return 2;
-  return 0;
+  if (4 * per_query <= topk_key_budget<8>()) return {4, 8};
+  if (2 * per_query <= topk_key_budget<8>()) return {2, 8};
+  if (4 * per_query <= topk_key_budget<16>()) return {4, 16};
+  if (2 * per_query <= topk_key_budget<16>()) return {2, 16};
+  return {0, 0};
 }
 
 bool indexer_topk_tc_supported(int H_I, int d_I, int max_vis, bool fp32) {
-  return !fp32 && H_I == kHI && d_I == kDI && topk_tc_group(max_vis) > 0;
+  return !fp32 && H_I == kHI && d_I == kDI && topk_tc_shape(max_vis).G > 0;
 }
 
-template <int G>
+template <int G, int CW>
 static cudaError_t launch_topk_tc_t(const void* qI, const void* w, const void* kI, const int32_t* cu,
                                     const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r, int topk, int k_pad,
                                     int32_t* idx, int* status, cudaStream_t stream) {
@@ -402,17 +435,18 @@ static cudaError_t launch_topk_tc_t(const void* qI, const void* w, const void* k
   if (!make_tmap_bf16_sw128(&mqi, qI, (uint64_t)T_cap * kHI, kDI, G * kHI) ||
       !make_tmap_bf16_sw128(&mki, kI, n_cmp_rows, kDI, kTK))
     return cudaErrorInvalidValue;
-  const size_t smem = 1024 + kKeysOff + (size_t)G * ((max_vis + 3) & ~3) * 4;
-  auto kern = indexer_topk_tc_kernel<G>;
+  const size_t smem = 1024 + TopkCfg<CW>::kKeysOff + (size_t)G * ((max_vis + 3) & ~3) * 4;
+  auto kern = indexer_topk_tc_kernel<G, CW>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int blocks = T_cap / G + B + 1;
-  const int grid = blocks < sms ? blocks : sms;
-  kern<<<grid, kThreads, smem, stream>>>(mqi, mki, static_cast<const __nv_bfloat16*>(w), cu, cu_cmp, B, r, topk,
-                                         k_pad, max_vis, idx, status);
+  const int slots = sms * TopkCfg<CW>::kCtasPerSm;
+  const int grid = blocks < slots ? blocks : slots;
+  kern<<<grid, TopkCfg<CW>::kThreads, smem, stream>>>(mqi, mki, static_cast<const __nv_bfloat16*>(w), cu, cu_cmp, B,
+                                                      r, topk, k_pad, max_vis, idx, status);
   return cudaGetLastError();
 }
 
@@ -420,9 +454,14 @@ cudaError_t launch_indexer_topk_tc(const void* qI, const void* w, const void* kI
                                    const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r, int topk, int k_pad,
                                    int32_t* idx, int* status, cudaStream_t stream) {
   if (T_cap <= 0) return cudaSuccess;
-  if (topk_tc_group(max_vis) == 4)
-    return launch_topk_tc_t<4>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
-  return launch_topk_tc_t<2>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
+  const TopkShape sh = topk_tc_shape(max_vis);
+  if (sh.G == 4 && sh.CW == 8)
+    return launch_topk_tc_t<4, 8>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
+  if (sh.G == 2 && sh.CW == 8)
+    return launch_topk_tc_t<2, 8>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
+  if (sh.G == 4)
+    return launch_topk_tc_t<4, 16>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
+  return launch_topk_tc_t<2, 16>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
 }
 
 }  // namespace csa
