@@ -34,6 +34,24 @@
 
 namespace csa {
 
+#ifdef CSA_KL_PROFILE
+// Profiling build only: cycles per (role, site), summed over warps.
+__device__ unsigned long long g_kl_prof[48];
+#define KL_T0(v) const long long v = clock64()
+#define KL_ADD(site, v) \
+  do {                  \
+    if (lane == 0) s_prof[warp][site] += (unsigned long long)(clock64() - (v)); \
+  } while (0)
+#define KL_CNT(site) \
+  do {               \
+    if (lane == 0) s_prof[warp][site] += 1ull; \
+  } while (0)
+#else
+#define KL_T0(v)
+#define KL_ADD(site, v)
+#define KL_CNT(site)
+#endif
+
 namespace {
 
 constexpr int kQB = 4;          // queries per block
@@ -121,8 +139,15 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
   __shared__ float s_red[kComputeWarps][4];  // per compute warp: A, B, mI, lI
   __shared__ float s_ml[2][kQB * kNH][2];    // pass 1 per column half: row max, row sum
   __shared__ int s_abort;
+#ifdef CSA_KL_PROFILE
+  __shared__ unsigned long long s_prof[kThreads / 32][16];
+#endif
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#ifdef CSA_KL_PROFILE
+  if (lane == 0)
+    for (int i = 0; i < 16; ++i) s_prof[warp][i] = 0;
+#endif
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t bar_full = smem_u32(&s_full[0]), bar_empty = smem_u32(&s_empty[0]);
   const uint32_t bar_sfull = smem_u32(&s_sfull[0]), bar_sfree = smem_u32(&s_sfree[0]);
@@ -174,7 +199,10 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         for (int pass = 0; pass < 2; ++pass) {
           for (int i = 0; i < bk.ntiles; ++i, ++it) {
             const uint32_t s = it % kStages;
+            KL_T0(t_e);
             if (!mbar_wait_bounded(bar_empty + 8 * s, ((it / kStages) & 1u) ^ 1u, status)) { s_abort = 1; break; }
+            KL_ADD(0, t_e);
+            KL_CNT(1);
             const uint32_t st = base + kStageOff + s * kStageBytes;
             mbar_arrive_expect_tx(bar_full + 8 * s, pass == 0 ? kStageK : kStageBytes);
             tma_load_2d(st, &map_k, 0, bk.cmp0 + i * kTK, bar_full + 8 * s);
@@ -203,12 +231,17 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
             // pass 1 alternates the two score buffers; a pass 2 tile takes both
             const uint32_t d = p1 & 1u;
             const bool use0 = pass == 1 || d == 0, use1 = pass == 1 || d == 1;
-            if (!mbar_wait_bounded(bar_full + 8 * s, (it / kStages) & 1u, status) ||
-                (use0 && !mbar_wait_bounded(bar_sfree, (nf0 & 1u) ^ 1u, status)) ||
+            KL_T0(m_f);
+            const bool okf = mbar_wait_bounded(bar_full + 8 * s, (it / kStages) & 1u, status);
+            KL_ADD(0, m_f);
+            KL_T0(m_s);
+            if (!okf || (use0 && !mbar_wait_bounded(bar_sfree, (nf0 & 1u) ^ 1u, status)) ||
                 (use1 && !mbar_wait_bounded(bar_sfree + 8, (nf1 & 1u) ^ 1u, status))) {
               s_abort = 1;
               break;
             }
+            KL_ADD(1, m_s);
+            KL_CNT(2);
             tc::fence_after_sync();
             const uint32_t st = base + kStageOff + s * kStageBytes;
             if (pass == 0) {
@@ -274,7 +307,10 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         float m = -INFINITY, l = 0.f;
         for (int i = 0; i < bk.ntiles; ++i) {
           const uint32_t d = p1++ & 1u;
+          KL_T0(c_w1);
           if (!mbar_wait_bounded(bar_sfull + 8 * d, (d ? nf1 : nf0) & 1u, status)) { s_abort = 1; break; }
+          KL_ADD(0, c_w1);
+          KL_T0(c_l1);
           tc::fence_after_sync();
           float x[kTK / 2];
 #pragma unroll
@@ -288,6 +324,8 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_sfree + 8 * d);
           if (d) ++nf1; else ++nf0;
+          KL_ADD(1, c_l1);
+          KL_T0(c_c1);
           const int nv = nvis - i * kTK - half * (kTK / 2);  // valid columns of this thread's half
           if (nv < kTK / 2) {               // only the last tile of a row is partial
 #pragma unroll
@@ -316,7 +354,10 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
             l = l * ex2(m - mn) + ((s0 + s1) + (s2 + s3));
             m = mn;
           }
+          KL_ADD(2, c_c1);
+          KL_CNT(7);
         }
+        KL_T0(c_m);
         s_ml[half][mt * kTK + rowl][0] = m;
         s_ml[half][mt * kTK + rowl][1] = l;
         named_sync(1, kComputeThreads);
@@ -326,6 +367,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
           const float ls = (mx == -INFINITY) ? 0.f : l * ex2(m - mx) + l2 * ex2(m2 - mx);
           s_L[q][h] = (ls > 0.f) ? -(mx + __log2f(ls)) : -INFINITY;  // negated; -inf: contributes nothing
         }
+        KL_ADD(9, c_m);
       }
       named_sync(1, kComputeThreads);
       if (*(volatile int*)&s_abort) break;  // uniform: read after the barrier
@@ -335,10 +377,13 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
       const bool q_ok = q < bk.nq;
       float A = 0.f, Bs = 0.f, mI = -INFINITY, lI = 0.f;
       for (int i = 0; i < bk.ntiles; ++i) {
+        KL_T0(c_w2);
         if (!mbar_wait_bounded(bar_sfull, nf0 & 1u, status) || !mbar_wait_bounded(bar_sfull + 8, nf1 & 1u, status)) {
           s_abort = 1;
           break;
         }
+        KL_ADD(3, c_w2);
+        KL_T0(c_l2);
         tc::fence_after_sync();
         float x[kNH];
         uint32_t ri[8];
@@ -358,6 +403,8 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         }
         ++nf0;
         ++nf1;
+        KL_ADD(4, c_l2);
+        KL_T0(c_c2);
         const int j = i * kTK + rowl;  // entry index within the sequence
         if (q_ok && j < nvis_q) {
           const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
@@ -388,7 +435,10 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
             lI += __expf(iv - mI);
           }
         }
+        KL_ADD(5, c_c2);
+        KL_CNT(8);
       }
+      KL_T0(c_end);
       // reduce the per-key partials over the warpgroup's 128 threads
       {
         float a = A, bs = Bs, mm = mI, ll = lI;
@@ -428,15 +478,30 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         csize[bk.seq0 + bk.q0 + qq] = nvis;
       }
       named_sync(1, kComputeThreads);
+      KL_ADD(6, c_end);
       if (*(volatile int*)&s_abort) break;
     }
   }
+#ifdef CSA_KL_PROFILE
+  if (lane == 0) {
+    const int role = warp < kComputeWarps ? 0 : (warp == kComputeWarps + 1 ? 1 : 2);
+    for (int i = 0; i < 16; ++i) atomicAdd(&g_kl_prof[role * 16 + i], s_prof[warp][i]);
+  }
+#endif
 
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (warp == kComputeWarps + 1) tc::tmem_dealloc(tmem, kTmemCols);
 }
+
+#ifdef CSA_KL_PROFILE
+extern "C" int csa_kl_profile(unsigned long long* out48) {
+  if (cudaMemcpyFromSymbol(out48, g_kl_prof, sizeof(unsigned long long) * 48) != cudaSuccess) return -1;
+  static const unsigned long long zeros[48] = {};
+  return cudaMemcpyToSymbol(g_kl_prof, zeros, sizeof(zeros)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 bool indexer_kl_dense_tc_supported(const KLArgs& a, bool fp32) {
   return !fp32 && a.idx == nullptr && a.H == kNH && a.d == kDim && a.H_I == kHI && a.d_I == kDI;

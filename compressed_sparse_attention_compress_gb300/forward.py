@@ -99,6 +99,50 @@ class Forward:
             self.kl(stream)
 
 
+    # inputs each stage needs first, in the order the stages run
+    _STAGE_INPUTS = (("cu_seqlens", "x_kv", "z_kv", "P_kv", "x_I", "z_I", "P_I", "v"), ("qI", "w"), ("q",))
+
+    def run_from_host(self, host: dict, stream=None, copy_stream=None):
+        """The forward with its inputs still in (pinned) host memory.
+
+        The inputs are copied into this object's device buffers on
+        ``copy_stream`` in the order the stages need them, and each stage
+        waits only for its own inputs, so the 537 MB of queries at the headline
+        size arrive while the compressor and the top-k run.  The previous
+        forward on ``stream`` must be done with the buffers before they are
+        overwritten: the copy stream waits for it first.
+        """
+        main = stream if stream is not None else torch.cuda.current_stream()
+        cs = copy_stream if copy_stream is not None else self._copy_stream()
+        cs.wait_stream(main)
+        ready = []
+        with torch.cuda.stream(cs):
+            for names in self._STAGE_INPUTS:
+                for k in names:
+                    if k in host and k in self.x:
+                        self.x[k].copy_(host[k], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                ready.append(ev)
+        with torch.cuda.stream(main):
+            main.wait_event(ready[0])
+            if self.wl.ratio > 0:
+                self.compress(main)
+                if self.wl.H_I > 0:
+                    main.wait_event(ready[1])
+                    self.topk(main)
+            main.wait_event(ready[1])
+            main.wait_event(ready[2])
+            self.attend(main)
+            if self.wl.kl_mode != "none":
+                self.kl(main)
+
+    def _copy_stream(self):
+        if getattr(self, "_cs", None) is None:
+            self._cs = torch.cuda.Stream(device=self.dev)
+        return self._cs
+
+
 def to_device(arrs: dict, io_fp32: bool, device: int = 0) -> dict:
     """numpy float32 (bf16-valued) inputs -> device tensors in the I/O dtype."""
     dev = torch.device("cuda", device)

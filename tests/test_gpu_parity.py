@@ -205,3 +205,24 @@ def test_packed_equals_separate_sequences():
         gi = g.idx.clone()
         gi[gi >= 0] += cmp0
         assert torch.equal(gi, f.idx[s])
+
+
+def test_run_from_host_matches_device_run():
+    """Inputs copied from pinned host memory stage by stage give the same outputs
+    as a forward on inputs already on the device; a second call reuses the buffers."""
+    wl = I.custom("host", lengths=[700, 1300], ratio=4, overlap=True, H=64, d=128, window=128, H_I=8, d_I=64,
+                  topk=64, k_pad=64, kl_mode="dense")
+    arrs = I.generate(wl, 5)
+    ref = Forward(wl, to_device(arrs, False))
+    ref.run()
+    zeros = {k: torch.zeros_like(v) for k, v in to_device(arrs, False).items()}
+    g = Forward(wl, zeros)
+    host = {k: v.cpu().pin_memory() for k, v in to_device(arrs, False).items()}
+    for _ in range(2):
+        g.run_from_host(host)
+        torch.cuda.synchronize()
+        assert g.h.device_status() == 0
+        assert torch.equal(g.out, ref.out)
+        assert torch.equal(g.lse, ref.lse)
+        assert torch.equal(g.idx, ref.idx)
+        assert torch.equal(g.kl_sum, ref.kl_sum)
