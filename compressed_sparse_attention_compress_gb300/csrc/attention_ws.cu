@@ -160,6 +160,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
   __shared__ Meta s_meta[2][2];
   __shared__ int s_rows[2][2][kTK];
   __shared__ __align__(16) float s_m[2][kNH];
+  __shared__ __align__(16) float s_nm[2][kNH];  // -s_m
   __shared__ float s_alpha[2][kNH], s_dm[2][kNH], s_inv[2][kNH];
   __shared__ int s_wmax[2][4][kNH];
   __shared__ float s_lsum[2][4][kNH];
@@ -500,13 +501,14 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
           for (int j = 0; j < 32; ++j) t[j] *= scale_log2;
           excess = INFINITY;
         } else {
+          const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 m4 = reinterpret_cast<const float4*>(m_g + hh * 32)[j4];
-            t[4 * j4 + 0] = fmaf(t[4 * j4 + 0], scale_log2, -m4.x);
-            t[4 * j4 + 1] = fmaf(t[4 * j4 + 1], scale_log2, -m4.y);
-            t[4 * j4 + 2] = fmaf(t[4 * j4 + 2], scale_log2, -m4.z);
-            t[4 * j4 + 3] = fmaf(t[4 * j4 + 3], scale_log2, -m4.w);
+          for (int j4 = 0; j4 < 8; ++j4) {  // packed pairs against -m (kept negated in shared memory)
+            const float4 nm4 = reinterpret_cast<const float4*>(s_nm[g] + hh * 32)[j4];
+            f2_unpack(f2_fma(f2_pack(t[4 * j4 + 0], t[4 * j4 + 1]), sc2, f2_pack(nm4.x, nm4.y)), t[4 * j4 + 0],
+                      t[4 * j4 + 1]);
+            f2_unpack(f2_fma(f2_pack(t[4 * j4 + 2], t[4 * j4 + 3]), sc2, f2_pack(nm4.z, nm4.w)), t[4 * j4 + 2],
+                      t[4 * j4 + 3]);
             excess = fmaxf(excess, fmaxf(fmaxf(t[4 * j4 + 0], t[4 * j4 + 1]), fmaxf(t[4 * j4 + 2], t[4 * j4 + 3])));
           }
         }
@@ -541,6 +543,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
           s_alpha[g][tig] = (mo == -INFINITY) ? 1.f : ex2(mo - mn);
           s_dm[g][tig] = (fresh ? 0.f : mo) - mn;
           m_g[tig] = mn;
+          s_nm[g][tig] = -mn;
         }
         bar_sync(gbar, kSoftThreads);
 #pragma unroll
@@ -598,7 +601,13 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
         } else {
           tc::tmem_ld16_sync(t_l + c2 * 16, lv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) lv[j] = __float_as_uint(__uint_as_float(lv[j]) + t[c2 * 16 + j]);
+          for (int j = 0; j < 16; j += 2) {
+            float a, b;
+            f2_unpack(f2_add(f2_pack(__uint_as_float(lv[j]), __uint_as_float(lv[j + 1])),
+                             f2_pack(t[c2 * 16 + j], t[c2 * 16 + j + 1])), a, b);
+            lv[j] = __float_as_uint(a);
+            lv[j + 1] = __float_as_uint(b);
+          }
         }
         tc::tmem_st16(t_l + c2 * 16, lv);
       }
