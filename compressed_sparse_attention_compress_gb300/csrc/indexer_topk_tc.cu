@@ -31,6 +31,24 @@
 
 namespace csa {
 
+#ifdef CSA_TOPK_PROFILE
+// Profiling build only: cycles per site, summed over compute warps.
+__device__ unsigned long long g_topk_prof[16];
+#define TK_T0(v) const long long v = clock64()
+#define TK_ADD(site, v) \
+  do {                  \
+    if (lane == 0) atomicAdd(&g_topk_prof[site], (unsigned long long)(clock64() - (v))); \
+  } while (0)
+#define TK_CNT(site) \
+  do {               \
+    if (lane == 0) atomicAdd(&g_topk_prof[site], 1ull); \
+  } while (0)
+#else
+#define TK_T0(v)
+#define TK_ADD(site, v)
+#define TK_CNT(site)
+#endif
+
 namespace {
 
 constexpr int kHI = 8, kDI = 64;
@@ -215,6 +233,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
       QBlock bk;
       if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk)) continue;
       if (tid == 0 && (bk.q0 + bk.nq) / r > max_vis) raise_status(status, CSA_ERR_DEVICE_BOUNDS);
+      TK_T0(tk_sc);
       if (bk.score) {
         if (tid < G * kHI) {
           const int q = tid / kHI, h = tid % kHI;
@@ -249,6 +268,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
         named_sync(1, kComputeThreads);
         if (*(volatile int*)&s_abort) break;
       }
+      TK_ADD(5, tk_sc);
       // ---- per query: select and write (each lane takes 4 consecutive entries) ----
       for (int q = 0; q < bk.nq; ++q) {
         const int t = bk.q0 + q;
@@ -268,22 +288,26 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
             const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
             const uint32_t dmask = round == 2 ? 0x3FFu : 0x7FFu;
             const int nb = (int)dmask + 1;
+            TK_T0(tk_clr);
             for (int b = tid; b < nb; b += kComputeThreads) s_hist[b] = 0;
             named_sync(1, kComputeThreads);
+            TK_ADD(4, tk_clr);
+            TK_CNT(6);
+            TK_T0(tk_h);
             for (int jb = warp * 128; jb < n; jb += kComputeWarps * 128) {
               const int j0 = jb + 4 * lane;
               uint4 k4 = make_uint4(0u, 0u, 0u, 0u);
               if (j0 < n) k4 = *reinterpret_cast<const uint4*>(keys + j0);
               const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
+              for (int e = 0; e < 4; ++e) {  // plain shared atomics: cheaper here than warp-aggregating them
                 const bool ok = j0 + e < n && (kk[e] & pmask) == prefix;
-                const uint32_t dg = ok ? (kk[e] >> shift) & dmask : 0xFFFFFFFFu;
-                const uint32_t peers = __match_any_sync(0xffffffffu, dg);
-                if (ok && lane == __ffs(peers) - 1) atomicAdd(&s_hist[dg], (uint32_t)__popc(peers));
+                if (ok) atomicAdd(&s_hist[(kk[e] >> shift) & dmask], 1u);
               }
             }
             named_sync(1, kComputeThreads);
+            TK_ADD(0, tk_h);
+            TK_T0(tk_s);
             // thread tid owns bpt bins counted from the top
             const int bpt = nb / kComputeThreads;
             const int hi_bin = nb - 1 - tid * bpt;
@@ -320,6 +344,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
             // the bin holds exactly the entries still needed: all of it is selected
             whole_bin = s_bincount == need && prefix != 0u;
             named_sync(1, kComputeThreads);
+            TK_ADD(1, tk_s);
           }
           if (whole_bin) {
             thr = prefix - 1u;  // every key >= prefix (lower digits free) is selected
@@ -345,6 +370,8 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
             ceq += (in && !all && kk[e] == thr) ? 1 : 0;
           }
         };
+        TK_T0(tk_c);
+        TK_CNT(7);
         int gt = 0, eq = 0;
         for (int jb = j_lo; jb < j_hi; jb += 128) {
           uint32_t kk[4];
@@ -357,39 +384,28 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
         eq = __reduce_add_sync(0xffffffffu, eq);
         if (lane == 0) { s_cnt[0][warp] = gt; s_cnt[1][warp] = eq; }
         named_sync(1, kComputeThreads);
+        TK_ADD(2, tk_c);
+        TK_T0(tk_w);
         int gt_before = 0, eq_before = 0;
         for (int ww = 0; ww < warp; ++ww) { gt_before += s_cnt[0][ww]; eq_before += s_cnt[1][ww]; }
-        for (int jb = j_lo; jb < j_hi; jb += 128) {
-          const int j0 = jb + 4 * lane;
-          uint32_t kk[4];
-          int cgt, ceq;
-          flags_of(j0, kk, cgt, ceq);
-          // exclusive scan of the (gt, eq) counts over the lanes, packed 16 + 16 bits
-          const int packed = cgt | (ceq << 16);
-          int incl = packed;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-          }
-          const int tot = __shfl_sync(0xffffffffu, incl, 31);
-          int my_gt = gt_before + ((incl - packed) & 0xFFFF);
-          int my_eq = eq_before + ((incl - packed) >> 16);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = j0 + e;
-            const bool in = j < j_hi;
-            const bool fgt = in && (all || kk[e] > thr);
-            const bool feq = in && !all && kk[e] == thr;
-            if (fgt || (feq && my_eq < need_eq)) idx[orow + my_gt + min(my_eq, need_eq)] = bk.cmp0 + j;
-            my_gt += fgt ? 1 : 0;
-            my_eq += feq ? 1 : 0;
-          }
-          gt_before += tot & 0xFFFF;
-          eq_before += tot >> 16;
+        // write pass, 32 consecutive entries per step: ballots give each lane its output slot
+        const uint32_t lt = (1u << lane) - 1u;
+        for (int jb = j_lo; jb < j_hi; jb += 32) {
+          const int j = jb + lane;
+          const bool in = j < j_hi;
+          const uint32_t key = (!all && in) ? keys[j] : 0u;
+          const bool fgt = in && (all || key > thr);
+          const bool feq = in && !all && key == thr;
+          const uint32_t bgt = __ballot_sync(0xffffffffu, fgt);
+          const uint32_t beq = __ballot_sync(0xffffffffu, feq);
+          const int my_eq = eq_before + __popc(beq & lt);
+          if (fgt || (feq && my_eq < need_eq)) idx[orow + gt_before + __popc(bgt & lt) + min(my_eq, need_eq)] = bk.cmp0 + j;
+          gt_before += __popc(bgt);
+          eq_before += __popc(beq);
         }
         for (int i = m + tid; i < k_pad; i += kComputeThreads) idx[orow + i] = -1;
         named_sync(1, kComputeThreads);
+        TK_ADD(3, tk_w);
       }
     }
   }
@@ -399,6 +415,14 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   tc::fence_after_sync();
   if (warp == kComputeWarps + 1) tc::tmem_dealloc(tmem, 64);
 }
+
+#ifdef CSA_TOPK_PROFILE
+extern "C" int csa_topk_profile(unsigned long long* out16) {
+  if (cudaMemcpyFromSymbol(out16, g_topk_prof, sizeof(unsigned long long) * 16) != cudaSuccess) return -1;
+  static const unsigned long long zeros[16] = {};
+  return cudaMemcpyToSymbol(g_topk_prof, zeros, sizeof(zeros)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 // Shared memory a CTA may use for scores: per-SM capacity split over the CTAs
 // resident on it, less static arrays (about 10 KB), the 1 KB every block
