@@ -7,6 +7,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -36,8 +37,15 @@ def _deps_mtime() -> float:
     return max((os.path.getmtime(f) for f in files), default=0.0)
 
 
+def _obj_dir(extra: list) -> str:
+    """Objects built with different extra flags live apart, so a flag change rebuilds."""
+    if not extra:
+        return BUILD
+    return os.path.join(BUILD, hashlib.sha1(" ".join(extra).encode()).hexdigest()[:12])
+
+
 def _compile(nvcc: str, src: str, extra: list) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+    obj = os.path.join(_obj_dir(extra), os.path.basename(src).replace(".cu", ".o"))
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _deps_mtime()):
         return obj
     cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj + ".tmp"]
@@ -50,20 +58,24 @@ def _compile(nvcc: str, src: str, extra: list) -> str:
 
 def build(verbose: bool = False, extra: list | None = None) -> str:
     """Compile every csrc/*.cu and link libcsa.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+    extra = list(extra or [])
+    os.makedirs(_obj_dir(extra), exist_ok=True)
     nvcc = _nvcc()
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    extra = list(extra or [])
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(lambda s: _compile(nvcc, s, extra), srcs))
     newest = max(os.path.getmtime(o) for o in objs)
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
+    stamp = os.path.join(BUILD, "last_link")  # which object set the library was linked from
+    linked_from = open(stamp).read() if os.path.exists(stamp) else ""
+    if not os.path.exists(LIB) or os.path.getmtime(LIB) < newest or linked_from != _obj_dir(extra):
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]  # static cudart (nvcc default)
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:
             raise RuntimeError(f"link failed:\n{p.stdout}\n{p.stderr}")
         os.replace(tmp, LIB)
+        with open(stamp, "w") as fh:
+            fh.write(_obj_dir(extra))
     if verbose:
         print(LIB)
     return LIB
