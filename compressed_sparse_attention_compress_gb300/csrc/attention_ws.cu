@@ -116,6 +116,13 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Sleep on a barrier phase for at most about `ns` nanoseconds (returns either way).
+__device__ __forceinline__ void mbar_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%0], %1, %2;\n}\n" ::"r"(bar), "r"(parity),
+      "r"(ns)
+      : "memory");
+}
 __device__ __forceinline__ void arrive_cp_async(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
@@ -413,7 +420,17 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
             *abort_flag = 1;
             break;
           }
-          __nanosleep(20);
+          // sleep on the barrier the next issue waits for, instead of spinning on the
+          // scheduler the softmax warps share: the next QK's if one is due, else the PV's
+          if (!end && kq < kp + 2) {
+            const uint32_t sf = smem_u32(&s_sfree[g]);
+            if (kq > 0 && !mbar_test(sf, (kq - 1) & 1u)) mbar_sleep(sf, (kq - 1) & 1u, 500);
+            else mbar_sleep(full_bar(g, kq & 1u), (kq >> 1) & 1u, 500);
+          } else if (kp < kq) {
+            mbar_sleep(smem_u32(&s_pfull[g]), kp & 1u, 500);
+          } else {
+            __nanosleep(64);
+          }
         }
       }
     }
