@@ -11,12 +11,36 @@
 // thread stages both spans into shared memory with bulk asynchronous copies
 // (cp.async.bulk, completion on an mbarrier); every input byte is read from
 // HBM once per CTA and the overlap between neighbouring entries is served from
-// shared memory.  Threads then walk (entry, channel) pairs with a one-pass
-// online softmax over the span in float32 and store coalesced rows.
+// shared memory.  A thread owns a pair of adjacent channels and walks the
+// run's entries; per entry it takes the span in chunks of 8 positions: the
+// chunk's logits z + P (log2 domain) in registers, one max, one rescale of the
+// running sums, then ex2 (MUFU) weights -- a float32 softmax over the span,
+// stored as a coalesced pair of the output row.
 #include "common.cuh"
 #include "launch.h"
 
 namespace csa {
+
+namespace {
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
+  const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+  return make_float2(bf16_lo(v), bf16_hi(v));
+}
+__device__ __forceinline__ float2 load_pair(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ void store_pair(__nv_bfloat16* p, float a, float b) {
+  *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(a, b);
+}
+__device__ __forceinline__ void store_pair(float* p, float a, float b) {
+  *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+
+}  // namespace
 
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(256)
@@ -74,27 +98,56 @@ compress_kernel(const TIn* __restrict__ x, const TIn* __restrict__ z, const floa
   if (!mbar_wait_bounded(bar_a, 0, status)) return;
 
   const int64_t out0 = (int64_t)__ldg(cu_cmp + b);
-  const int work = (j1 - j0) * D;
-  for (int i = threadIdx.x; i < work; i += blockDim.x) {
-    const int e = i / D, c = i - e * D;
+  constexpr float kLog2e = 1.4426950408889634f;
+  const int pairs = D >> 1;                        // D is even (checked on the host)
+  const int groups = (int)blockDim.x / pairs;      // entries worked on side by side
+  const int cpair = (int)threadIdx.x % pairs, eg = (int)threadIdx.x / pairs;
+  if (eg >= groups) return;
+  const int c = 2 * cpair;
+  for (int e = eg; e < j1 - j0; e += groups) {
     const int j = j0 + e;
-    const int first = r * j + r - S;
-    float m = -INFINITY, den = 0.f, num = 0.f;
-    for (int u = max(0, -first); u < S; ++u) {
-      const int srow = first + u - tok0;
-      const float lg = to_f32(sz[(size_t)srow * D + c]) + __ldg(P + (size_t)u * D + c);
-      const float xv = to_f32(sx[(size_t)srow * D + c]);
-      if (lg > m) {
-        const float sc = expf(m - lg);
-        den *= sc;
-        num *= sc;
-        m = lg;
+    const int first = r * j + r - S;               // span position u reads local token first + u
+    float m0 = -INFINITY, m1 = -INFINITY, den0 = 0.f, den1 = 0.f, num0 = 0.f, num1 = 0.f;
+    for (int u0 = max(0, -first); u0 < S; u0 += 8) {
+      float lg0[8], lg1[8], xv0[8], xv1[8];
+      float cm0 = -INFINITY, cm1 = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int u = u0 + k;
+        lg0[k] = -INFINITY;
+        lg1[k] = -INFINITY;
+        xv0[k] = 0.f;
+        xv1[k] = 0.f;
+        if (u < S) {
+          const size_t sofs = (size_t)(first + u - tok0) * D + c;
+          const float2 zz = load_pair(sz + sofs), xx = load_pair(sx + sofs);
+          const float2 pp = __ldg(reinterpret_cast<const float2*>(P + (size_t)u * D + c));
+          lg0[k] = (zz.x + pp.x) * kLog2e;
+          lg1[k] = (zz.y + pp.y) * kLog2e;
+          xv0[k] = xx.x;
+          xv1[k] = xx.y;
+          cm0 = fmaxf(cm0, lg0[k]);
+          cm1 = fmaxf(cm1, lg1[k]);
+        }
       }
-      const float ex = expf(lg - m);
-      den += ex;
-      num = fmaf(ex, xv, num);
+      const float mn0 = fmaxf(m0, cm0), mn1 = fmaxf(m1, cm1);
+      const float sc0 = ex2f(m0 - mn0), sc1 = ex2f(m1 - mn1);  // 0 while the sums are empty
+      den0 *= sc0;
+      num0 *= sc0;
+      den1 *= sc1;
+      num1 *= sc1;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float w0 = ex2f(lg0[k] - mn0), w1 = ex2f(lg1[k] - mn1);  // -inf (past the span) -> 0
+        den0 += w0;
+        den1 += w1;
+        num0 = fmaf(w0, xv0[k], num0);
+        num1 = fmaf(w1, xv1[k], num1);
+      }
+      m0 = mn0;
+      m1 = mn1;
     }
-    out[(out0 + j) * D + c] = from_f32<TOut>(num / den);
+    store_pair(out + (out0 + j) * D + c, num0 / den0, num1 / den1);
   }
 }
 
@@ -111,7 +164,8 @@ bool compress_supported(int D, int r, int S, int in_bytes) {
   int rows, E;
   size_t smem;
   compress_plan(D, r, S, in_bytes, &rows, &E, &smem);
-  return E >= 1 && smem <= 200 * 1024;
+  // a thread takes two adjacent channels; one row of channel pairs fits the CTA
+  return E >= 1 && smem <= 200 * 1024 && D % 2 == 0 && D / 2 <= 256;
 }
 
 template <typename TIn, typename TOut>
