@@ -532,13 +532,12 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       }
       WS_ADD(2, s_ex);
       // the previous PV must be done before P^T / O^T are touched
-      WS_T0(s_od);
-      if (k > 0) ok = ok && mbar_wait_bounded(smem_u32(&s_odone[g]), (k - 1) & 1u, status);
-      WS_ADD(3, s_od);
       WS_T0(s_vote);
       // one vote per tile: a score above the reference by more than the slack, or a
-      // failed wait (the abort is then decided uniformly inside)
+      // failed wait (the abort is then decided uniformly inside).  The previous tile's
+      // PV keeps running meanwhile: it is waited for only where P^T / O^T are touched.
       const bool bad = !ok || *abort_flag != 0;
+      bool pv_done = k == 0;
       if (bar_or(gbar, kSoftThreads, excess > kTau || bad)) {
         // new reference: the tile's per-head column maxima (t + m is the scaled score)
 #pragma unroll
@@ -547,7 +546,10 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
           const int v = __reduce_max_sync(0xffffffffu, ord_of(valid ? sc : -INFINITY));
           if (lane == 0) s_wmax[g][quad][hh * 32 + j] = v;
         }
-        if (bar_or(gbar, kSoftThreads, bad)) {
+        bool ok2 = true;
+        if (!pv_done) ok2 = mbar_wait_bounded(smem_u32(&s_odone[g]), (k - 1) & 1u, status);
+        pv_done = true;
+        if (bar_or(gbar, kSoftThreads, bad || !ok2)) {
           *abort_flag = 1;
           break;
         }
@@ -589,6 +591,11 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
         }
       }
       WS_ADD(4, s_vote);
+      WS_T0(s_od);
+      // P^T is overwritten below: the previous tile's PV must be done reading it
+      if (!pv_done && !mbar_wait_bounded(smem_u32(&s_odone[g]), (k - 1) & 1u, status)) *abort_flag = 1;
+      tc::fence_after_sync();
+      WS_ADD(3, s_od);
       WS_T0(s_p);
       // ---- this thread's half of the key's P^T row: 32 heads -> 4 swizzled 16-byte chunks ----
 #pragma unroll
