@@ -51,20 +51,38 @@ compress_kernel(const TIn* __restrict__ x, const TIn* __restrict__ z, const floa
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_b, s_j0, s_j1;
 
-  if (threadIdx.x == 0) {
-    // blockIdx.x counts chunks of E entries over the sequences in order.
+  if (threadIdx.x < 32) {
+    // blockIdx.x counts chunks of E entries over the sequences in order; warp 0
+    // finds the owning sequence 32 sequences at a time (one load round trip each)
+    const int lane = threadIdx.x;
     int c = blockIdx.x, b = -1, n = 0;
-    for (int bb = 0; bb < B; ++bb) {
-      int L = __ldg(cu + bb + 1) - __ldg(cu + bb);
+    for (int base = 0; base < B && b < 0; base += 32) {
+      const int bb = base + lane;
+      int L = bb < B ? __ldg(cu + bb + 1) - __ldg(cu + bb) : 0;
       if (L < 0) { raise_status(status, CSA_ERR_DEVICE_BOUNDS); L = 0; }
-      n = L / r;
-      const int nch = (n + E - 1) / E;
-      if (c < nch) { b = bb; break; }
-      c -= nch;
+      const int nb = L / r;
+      const int nch = (nb + E - 1) / E;
+      int incl = nch;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const uint32_t hit = __ballot_sync(0xffffffffu, bb < B && c < incl);
+      if (hit != 0u) {
+        const int w = __ffs(hit) - 1;  // first sequence whose chunks reach c
+        b = base + w;
+        c -= __shfl_sync(0xffffffffu, incl - nch, w);
+        n = __shfl_sync(0xffffffffu, nb, w);
+      } else {
+        c -= __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
-    s_b = b;
-    s_j0 = c * E;
-    s_j1 = b >= 0 ? min(c * E + E, n) : 0;
+    if (lane == 0) {
+      s_b = b;
+      s_j0 = c * E;
+      s_j1 = b >= 0 ? min(c * E + E, n) : 0;
+    }
   }
   __syncthreads();
   const int b = s_b;
@@ -153,7 +171,9 @@ compress_kernel(const TIn* __restrict__ x, const TIn* __restrict__ z, const floa
 
 // Rows of the staging buffer and entries per CTA for a given span.
 static void compress_plan(int D, int r, int S, int in_bytes, int* rows_max, int* E, size_t* smem) {
-  int rows = S > 128 ? S : 128;
+  // runs of about 64 rows: many CTAs per SM, so one CTA's staging copy overlaps
+  // another's reduction
+  int rows = S > 64 ? S : 64 + (S - r);
   if ((size_t)2 * rows * D * in_bytes > 200 * 1024) rows = S;
   *rows_max = rows;
   *E = (rows - (S - r)) / r;
