@@ -6,8 +6,7 @@ stream, spawned in a fixed order from ``SeedSequence(seed)``:
 
     x_kv, z_kv, P_kv, x_I, z_I, P_I, q, qI, w, v
 
-Each bf16 tensor is ``standard_normal`` float32, times the workload's
-``input_scale`` (1 unless a workload says otherwise), rounded to bf16
+Each bf16 tensor is ``standard_normal`` float32 rounded to bf16
 (round-to-nearest-even); the rounded values are what both the GPU and the
 oracle consume.  The compressor positional biases ``P_kv``/``P_I`` are float32
 parameters and are not rounded.
@@ -65,7 +64,6 @@ class Workload:
     io_fp32: bool = False    # float32 I/O arrays holding bf16 values
     kl_mode: str = "none"    # "sparse" (selected set), "dense" (all visible) or "none"
     cap_align: int = 1       # T_cap = total rounded up to this
-    input_scale: float = 1.0 # activation streams are standard normal times this
     notes: str = ""
     extra: dict = field(default_factory=dict)
 
@@ -107,10 +105,9 @@ WORKLOADS = {
     # one sequence L=512, r=4, 4 heads x 64, indexer 2 x 32, top-k 16, W=64, fp32 I/O
     "tiny": Workload("tiny", [512], 4, True, 4, 64, 64, H_I=2, d_I=32, topk=16, k_pad=16,
                      separate_v=True, io_fp32=True, kl_mode="sparse"),
-    # CSA sparse mode: L=8192, r=4, 64 x 128, indexer 8 x 64, top-k 512, W=128,
-    # activations N(0,1) scaled by 1/sqrt(head_dim)
+    # CSA sparse mode: L=8192, r=4, 64 x 128, indexer 8 x 64, top-k 512, W=128
     "csa8k": Workload("csa8k", [8192], 4, True, 64, 128, 128, H_I=8, d_I=64, topk=512,
-                      k_pad=512, kl_mode="sparse", input_scale=1.0 / float(np.sqrt(128.0))),
+                      k_pad=512, kl_mode="sparse"),
     # HCA: L=65536, r=128 (no overlap), 64 x 128, W=128, no indexer
     "hca64k": Workload("hca64k", [65536], 128, False, 64, 128, 128),
     # packed THD varlen CSA: 16 sequences, lengths uniform in [1024, 16384] from seed 0
@@ -146,9 +143,7 @@ def generate(wl: Workload, seed: int = 0) -> dict:
 
     def normal(name, shape, round_bf16=True):
         a = gens[name].standard_normal(shape, dtype=np.float32)
-        if round_bf16:  # activation stream: scaled, then rounded to bf16
-            return bf16_round(a * np.float32(wl.input_scale))
-        return a
+        return bf16_round(a) if round_bf16 else a
 
     out["x_kv"] = normal("x_kv", (T, wl.d))
     if wl.ratio > 0:
