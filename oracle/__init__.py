@@ -11,6 +11,7 @@ from .oracle import (  # noqa: F401
     set_num_threads,
     compressed_offsets,
     compress,
+    compress_ex,
     indexer_logits,
     indexer_topk,
     attention,

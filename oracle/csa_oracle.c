@@ -135,6 +135,81 @@ void oracle_compress(const float* x, const float* z, const float* P,
   }
 }
 
+/* Compressor variant with the extras the pages list around the compressor
+ * (§10 "compressor softmax and normalization intermediates"; §12 invariant 2
+ * "RoPE mode is per layer and per compressed coordinate system"; §9 FP32
+ * positional parameter).  Three steps, in this order, per compressed entry:
+ *
+ *  1. gate: the per-channel softmax-weighted sum of oracle_compress, except
+ *     that with x_prev/z_prev given (overlapping spans only) span positions
+ *     u < r -- the previous block -- read x_prev/z_prev and positions u >= r
+ *     read x/z (two projections of the same tokens, one per half of the span);
+ *  2. RMSNorm (when gamma is given): y <- y / sqrt(mean_c y_c^2 + eps) * gamma;
+ *  3. RoPE (when rope_dim > 0) on the last rope_dim channels, as rope_dim/2
+ *     interleaved pairs (2i, 2i+1) rotated by the angle p * theta^(-2i/rope_dim)
+ *     (the rotary embedding of Su et al., "RoFormer", 2021), p = the entry's
+ *     position in its sequence's compressed coordinates scaled as
+ *     p = j * pos_stride + pos_offset.
+ * Arguments as oracle_compress; x_prev, z_prev, gamma may be NULL. */
+void oracle_compress_ex(const float* x, const float* z, const float* x_prev, const float* z_prev,
+                        const float* P, const float* gamma, float eps, int rope_dim, double theta,
+                        int64_t pos_stride, int64_t pos_offset, const int32_t* cu,
+                        const int32_t* cu_cmp, int B, int D, int r, int overlap, double* out) {
+  const int S = overlap ? 2 * r : r;
+  const int two = overlap && x_prev != NULL && z_prev != NULL;
+  for (int b = 0; b < B; ++b) {
+    const int64_t L = (int64_t)cu[b + 1] - cu[b];
+    const int64_t n = r > 0 ? L / r : 0;
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < n; ++j) {
+      double* y = out + ((int64_t)cu_cmp[b] + j) * D;
+      const int64_t first = (int64_t)r * j + r - S;
+      /* 1. softmax gate over the span */
+      for (int c = 0; c < D; ++c) {
+        double m = -INFINITY;
+        for (int u = 0; u < S; ++u) {
+          const int64_t t = first + u;
+          if (t < 0) continue;
+          const float* zs = (two && u < r) ? z_prev : z;
+          const double logit = (double)zs[(cu[b] + t) * (int64_t)D + c] + (double)P[(int64_t)u * D + c];
+          if (logit > m) m = logit;
+        }
+        double den = 0.0, num = 0.0;
+        for (int u = 0; u < S; ++u) {
+          const int64_t t = first + u;
+          if (t < 0) continue;
+          const float* zs = (two && u < r) ? z_prev : z;
+          const float* xs = (two && u < r) ? x_prev : x;
+          const double logit = (double)zs[(cu[b] + t) * (int64_t)D + c] + (double)P[(int64_t)u * D + c];
+          const double e = exp(logit - m);
+          den += e;
+          num += e * (double)xs[(cu[b] + t) * (int64_t)D + c];
+        }
+        y[c] = num / den;
+      }
+      /* 2. RMSNorm over the D channels of the entry */
+      if (gamma != NULL) {
+        double ss = 0.0;
+        for (int c = 0; c < D; ++c) ss += y[c] * y[c];
+        const double rms = sqrt(ss / D + (double)eps);
+        for (int c = 0; c < D; ++c) y[c] = y[c] / rms * (double)gamma[c];
+      }
+      /* 3. rotary embedding of the trailing rope_dim channels */
+      if (rope_dim > 0) {
+        const double p = (double)(j * pos_stride + pos_offset);
+        for (int i = 0; i < rope_dim / 2; ++i) {
+          const int c = D - rope_dim + 2 * i;
+          const double ang = p * pow(theta, -(2.0 * i) / rope_dim);
+          const double cs = cos(ang), sn = sin(ang);
+          const double a = y[c], bb = y[c + 1];
+          y[c] = a * cs - bb * sn;
+          y[c + 1] = a * sn + bb * cs;
+        }
+      }
+    }
+  }
+}
+
 /* Lightning-indexer logits of one query against its visible entries
  * (§3 i_{t,j}; form sum_h w * ReLU(qI . kI)).  logits must hold nvis values. */
 static void indexer_logits_one(const float* qI, const float* w, const float* kI,

@@ -58,6 +58,8 @@ def _load():
         lib.oracle_compressed_offsets.argtypes = [P, i32, i32, P]
         lib.oracle_compressed_offsets.restype = i64
         lib.oracle_compress.argtypes = [P, P, P, P, P, i32, i32, i32, i32, P]
+        lib.oracle_compress_ex.argtypes = [P, P, P, P, P, P, ctypes.c_float, i32, f64, i64, i64, P, P,
+                                           i32, i32, i32, i32, P]
         lib.oracle_indexer_logits.argtypes = [P, P, P, P, P, i32, i32, i32, i32, P, i32, i64, P, P]
         lib.oracle_indexer_topk.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, i32, P]
         lib.oracle_attention.argtypes = [i32, P, P, P, P, P, P, i32, P, P, P, i32, i32, i32, i32,
@@ -113,6 +115,33 @@ def compress(x, z, P, cu_seqlens, ratio: int, overlap: bool) -> np.ndarray:
     out = np.zeros((int(cu_cmp[-1]), D), dtype=np.float64)
     _load().oracle_compress(_ptr(x), _ptr(z), _ptr(P), _ptr(cu), _ptr(cu_cmp), cu.shape[0] - 1,
                             D, int(ratio), int(bool(overlap)), _ptr(out))
+    return out
+
+
+def compress_ex(x, z, P, cu_seqlens, ratio: int, overlap: bool, x_prev=None, z_prev=None,
+                gamma=None, eps: float = 1e-6, rope_dim: int = 0, theta: float = 10000.0,
+                pos_stride: int = 1, pos_offset: int = 0) -> np.ndarray:
+    """Compressor variant: optional separate (x_prev, z_prev) stream for the
+    previous-block half of an overlapping span, then RMSNorm (gamma), then RoPE
+    on the trailing rope_dim channels; returns float64 [N_c, D]."""
+    x, z, P, cu = _f32(x), _f32(z), _f32(P), _i32(cu_seqlens)
+    D = x.shape[1]
+    S = 2 * ratio if overlap else ratio
+    assert z.shape == x.shape and P.shape == (S, D)
+    x_prev = None if x_prev is None else _f32(x_prev)
+    z_prev = None if z_prev is None else _f32(z_prev)
+    assert (x_prev is None) == (z_prev is None)
+    if x_prev is not None:
+        assert x_prev.shape == x.shape and z_prev.shape == x.shape
+    gamma = None if gamma is None else _f32(gamma)
+    assert gamma is None or gamma.shape == (D,)
+    assert 0 <= rope_dim <= D and rope_dim % 2 == 0
+    cu_cmp = compressed_offsets(cu, ratio)
+    out = np.zeros((int(cu_cmp[-1]), D), dtype=np.float64)
+    _load().oracle_compress_ex(_ptr(x), _ptr(z), _ptr(x_prev), _ptr(z_prev), _ptr(P), _ptr(gamma),
+                               float(eps), int(rope_dim), float(theta), int(pos_stride), int(pos_offset),
+                               _ptr(cu), _ptr(cu_cmp), cu.shape[0] - 1, D, int(ratio),
+                               int(bool(overlap)), _ptr(out))
     return out
 
 
