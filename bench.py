@@ -8,6 +8,7 @@ dense teacher over every visible entry), the shape of the DeepSeek-V4 CSA
 layers in "DeepSeek-V4 Attention Training Systems" (§2 phase table).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--compressor plain|v4]
 
 Prints one JSON line (rank 0).  Multi-GPU: one process per GPU under
 torch.distributed.run; each rank runs its own copy of the workload (the path
@@ -18,6 +19,7 @@ sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -113,10 +115,15 @@ def cpu_baseline(wl, arrs, seconds_target=15.0, max_rows=None):
     threads = oracle.num_threads()
     scale = wl.scale
     t0 = time.perf_counter()
-    kv = I.bf16_round(oracle.compress(arrs["x_kv"], arrs["z_kv"], arrs["P_kv"], cu, wl.ratio, wl.overlap)
-                      .astype(np.float32)) if wl.ratio > 0 else None
-    kI = I.bf16_round(oracle.compress(arrs["x_I"], arrs["z_I"], arrs["P_I"], cu, wl.ratio, wl.overlap)
-                      .astype(np.float32)) if wl.H_I > 0 else None
+    def comp(s, rope):
+        if wl.compressor == "v4":
+            return oracle.compress_ex(arrs["x_" + s], arrs["z_" + s], arrs["P_" + s], cu, wl.ratio, wl.overlap,
+                                      x_prev=arrs.get(f"x_{s}_prev"), z_prev=arrs.get(f"z_{s}_prev"),
+                                      gamma=arrs["g_" + s], eps=wl.norm_eps, rope_dim=rope, theta=wl.rope_theta)
+        return oracle.compress(arrs["x_" + s], arrs["z_" + s], arrs["P_" + s], cu, wl.ratio, wl.overlap)
+
+    kv = I.bf16_round(comp("kv", wl.rope_kv).astype(np.float32)) if wl.ratio > 0 else None
+    kI = I.bf16_round(comp("I", wl.rope_I).astype(np.float32)) if wl.H_I > 0 else None
     t_comp = time.perf_counter() - t0
     # probe cost on a few rows near the end (the most expensive queries), then size the sample
     n = 8
@@ -285,6 +292,12 @@ def run_ours(args, wl):
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
     tflops = counts["total_flops"] / (ms_step * 1e-3) / 1e12
+    # the HBM-bound compress stage against the copy bandwidth, whichever stage dominates
+    comp_hbm = None
+    if "compress" in stage_ms:
+        gbs = counts["compress_bytes"] / (stage_ms["compress"] * 1e-3) / 1e9
+        comp_hbm = {"achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                    "bytes": counts["compress_bytes"]}
     traffic = _traffic(dom, wl.name)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -292,7 +305,8 @@ def run_ours(args, wl):
         "data": "synthetic",
         "config": {"workload": wl.name, "global_batch": wl.B * ws, "seq_len": max(wl.lengths),
                    "tokens_per_gpu": wl.T, "ratio": wl.ratio, "heads": wl.H, "head_dim": wl.d, "topk": wl.topk,
-                   "window": wl.window, "kl": wl.kl_mode, "parallelism": f"replicas{ws}",
+                   "window": wl.window, "kl": wl.kl_mode, "compressor": wl.compressor,
+                   "parallelism": f"replicas{ws}",
                    "l2": "inputs larger than L2 (q alone is %.0f MB)" % (wl.T_cap * wl.H * wl.d * 2 / 1e6)},
         "tflops": tflops,
         "tflops_frac_of_peak": tflops / peaks["bf16_tflops_sustained"],
@@ -300,6 +314,7 @@ def run_ours(args, wl):
         "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"},
+        "compress_hbm": comp_hbm,
         "e2e": {"value": ws * wl.T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * f_launches(wl),
@@ -347,8 +362,12 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compressor", default="plain", choices=["plain", "v4"],
+                    help="v4: previous-half stream + RMSNorm + RoPE fused into both compressors")
     args = ap.parse_args()
     wl = I.WORKLOADS[args.workload]
+    if args.compressor != "plain":
+        wl = dataclasses.replace(wl, compressor=args.compressor)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

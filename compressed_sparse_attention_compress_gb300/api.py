@@ -48,6 +48,7 @@ def _load():
         "csa_get_device_status": [P, P, P],
         "csa_compressed_offsets": [P, P, I, I, P, P],
         "csa_compress": [P, P, P, P, P, P, I, I, I, I, I, I, I, P, P],
+        "csa_compress_ex": [P, P, P, P, P, P, P, F, I, F, I, I, P, P, I, I, I, I, I, I, I, P, P],
         "csa_indexer_topk": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P],
         "csa_sparse_attn_fwd": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P],
         "hca_attn_fwd": [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P],
@@ -138,6 +139,17 @@ def csa_compress(h: Handle, x, z, pos_bias, cu_seqlens, cu_cmp, max_seqlen: int,
     return _check("csa_compress", LIB.csa_compress(
         h.ptr, _p(x), _p(z), _p(pos_bias), _p(cu_seqlens), _p(cu_cmp), cu_seqlens.numel() - 1, T_cap,
         int(max_seqlen), D, int(ratio), int(bool(overlap)), _dtype(x), _p(out), _stream(stream)))
+
+
+def csa_compress_ex(h: Handle, x, z, pos_bias, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int, overlap: bool,
+                    out, x_prev=None, z_prev=None, norm_weight=None, norm_eps: float = 1e-6, rope_dim: int = 0,
+                    rope_theta: float = 10000.0, rope_pos_stride: int = 1, rope_pos_offset: int = 0, stream=None):
+    T_cap, D = x.shape
+    return _check("csa_compress_ex", LIB.csa_compress_ex(
+        h.ptr, _p(x), _p(z), _p(x_prev), _p(z_prev), _p(pos_bias), _p(norm_weight), float(norm_eps),
+        int(rope_dim), float(rope_theta), int(rope_pos_stride), int(rope_pos_offset), _p(cu_seqlens),
+        _p(cu_cmp), cu_seqlens.numel() - 1, T_cap, int(max_seqlen), D, int(ratio), int(bool(overlap)),
+        _dtype(x), _p(out), _stream(stream)))
 
 
 def csa_indexer_topk(h: Handle, qI, w, kI, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int, topk: int, idx,

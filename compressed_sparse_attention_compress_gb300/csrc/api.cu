@@ -125,6 +125,34 @@ csa_status_t csa_compress(csa_handle_t h, const void* x, const void* z, const fl
                                         stream));
 }
 
+csa_status_t csa_compress_ex(csa_handle_t h, const void* x, const void* z, const void* x_prev,
+                             const void* z_prev, const float* pos_bias, const float* norm_weight, float norm_eps,
+                             int rope_dim, float rope_theta, int rope_pos_stride, int rope_pos_offset,
+                             const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int D,
+                             int ratio, int overlap, csa_dtype_t dtype, void* out, cudaStream_t stream) {
+  if (!h || !x || !z || !pos_bias || !cu_cmp || !out || !packing_ok(cu, B, T_cap, max_seqlen))
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(z) || !aligned16(out) || !aligned16(pos_bias) || !opt_aligned16(x_prev) ||
+      !opt_aligned16(z_prev) || !opt_aligned16(norm_weight))
+    return CSA_ERR_INVALID_ARG;
+  if ((dtype != CSA_BF16 && dtype != CSA_FP32) || (overlap != 0 && overlap != 1) || ratio < 1)
+    return CSA_ERR_INVALID_ARG;
+  const bool two = x_prev != nullptr;
+  if (two != (z_prev != nullptr) || (two && !overlap)) return CSA_ERR_INVALID_ARG;
+  if (rope_dim < 0 || rope_dim > D || (rope_dim & 1) || !(norm_eps >= 0.f) ||
+      (rope_dim > 0 && !(rope_theta > 1.f)))
+    return CSA_ERR_INVALID_ARG;
+  const int S = overlap ? 2 * ratio : ratio;
+  if (!pow2_in(D, 32, 512) || ratio > 128 || S > 256) return CSA_ERR_UNSUPPORTED;
+  const bool fp32 = dtype == CSA_FP32;
+  if (!csa::compress_ex_supported(D, ratio, S, fp32 ? 4 : 2, two)) return CSA_ERR_UNSUPPORTED;
+  DeviceGuard g(h->device);
+  if (!g.ok) return CSA_ERR_CUDA;
+  return from_cuda(csa::launch_compress_ex(x, z, x_prev, z_prev, pos_bias, norm_weight, norm_eps, rope_dim,
+                                           rope_theta, rope_pos_stride, rope_pos_offset, cu, cu_cmp, B, T_cap, D,
+                                           ratio, S, fp32, out, h->status, stream));
+}
+
 csa_status_t csa_indexer_topk(csa_handle_t h, const void* qI, const void* w, const void* kI, const int32_t* cu,
                               const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H_I, int d_I, int ratio,
                               int topk, int k_pad, csa_dtype_t dtype, int32_t* idx, cudaStream_t stream) {

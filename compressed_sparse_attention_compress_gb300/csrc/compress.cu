@@ -16,6 +16,8 @@
 // chunk's logits z + P (log2 domain) in registers, one max, one rescale of the
 // running sums, then ex2 (MUFU) weights -- a float32 softmax over the span,
 // stored as a coalesced pair of the output row.
+#include <math.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -40,6 +42,43 @@ __device__ __forceinline__ void store_pair(float* p, float a, float b) {
   *reinterpret_cast<float2*>(p) = make_float2(a, b);
 }
 
+// Warp 0 finds the run of blockIdx.x: blockIdx.x counts chunks of E entries
+// over the sequences in order, 32 sequences at a time (one load round trip
+// each).  Writes the owning sequence (-1: past the last run) and the run's
+// entry range [j0, j1).
+__device__ __forceinline__ void locate_run(const int32_t* __restrict__ cu, int B, int r, int E, int* status,
+                                           int* s_b, int* s_j0, int* s_j1) {
+  const int lane = threadIdx.x;
+  int c = blockIdx.x, b = -1, n = 0;
+  for (int base = 0; base < B && b < 0; base += 32) {
+    const int bb = base + lane;
+    int L = bb < B ? __ldg(cu + bb + 1) - __ldg(cu + bb) : 0;
+    if (L < 0) { raise_status(status, CSA_ERR_DEVICE_BOUNDS); L = 0; }
+    const int nb = L / r;
+    const int nch = (nb + E - 1) / E;
+    int incl = nch;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t hit = __ballot_sync(0xffffffffu, bb < B && c < incl);
+    if (hit != 0u) {
+      const int w = __ffs(hit) - 1;  // first sequence whose chunks reach c
+      b = base + w;
+      c -= __shfl_sync(0xffffffffu, incl - nch, w);
+      n = __shfl_sync(0xffffffffu, nb, w);
+    } else {
+      c -= __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  if (lane == 0) {
+    *s_b = b;
+    *s_j0 = c * E;
+    *s_j1 = b >= 0 ? min(c * E + E, n) : 0;
+  }
+}
+
 }  // namespace
 
 template <typename TIn, typename TOut>
@@ -51,39 +90,7 @@ compress_kernel(const TIn* __restrict__ x, const TIn* __restrict__ z, const floa
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_b, s_j0, s_j1;
 
-  if (threadIdx.x < 32) {
-    // blockIdx.x counts chunks of E entries over the sequences in order; warp 0
-    // finds the owning sequence 32 sequences at a time (one load round trip each)
-    const int lane = threadIdx.x;
-    int c = blockIdx.x, b = -1, n = 0;
-    for (int base = 0; base < B && b < 0; base += 32) {
-      const int bb = base + lane;
-      int L = bb < B ? __ldg(cu + bb + 1) - __ldg(cu + bb) : 0;
-      if (L < 0) { raise_status(status, CSA_ERR_DEVICE_BOUNDS); L = 0; }
-      const int nb = L / r;
-      const int nch = (nb + E - 1) / E;
-      int incl = nch;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const uint32_t hit = __ballot_sync(0xffffffffu, bb < B && c < incl);
-      if (hit != 0u) {
-        const int w = __ffs(hit) - 1;  // first sequence whose chunks reach c
-        b = base + w;
-        c -= __shfl_sync(0xffffffffu, incl - nch, w);
-        n = __shfl_sync(0xffffffffu, nb, w);
-      } else {
-        c -= __shfl_sync(0xffffffffu, incl, 31);
-      }
-    }
-    if (lane == 0) {
-      s_b = b;
-      s_j0 = c * E;
-      s_j1 = b >= 0 ? min(c * E + E, n) : 0;
-    }
-  }
+  if (threadIdx.x < 32) locate_run(cu, B, r, E, status, &s_b, &s_j0, &s_j1);
   __syncthreads();
   const int b = s_b;
   if (b < 0) return;
@@ -169,6 +176,195 @@ compress_kernel(const TIn* __restrict__ x, const TIn* __restrict__ z, const floa
   }
 }
 
+// ---- compressor variant ---------------------------------------------------
+// The same gate, with the extras the page lists around the compressor (§10
+// "compressor softmax and normalization intermediates", §12 "RoPE mode is per
+// layer and per compressed coordinate system"), fused before the one rounding
+// of the output:
+//   * a second (x_prev, z_prev) stream that span positions u < r (the previous
+//     block of an overlapping span) read instead of (x, z);
+//   * RMSNorm over the entry's D channels;
+//   * a rotary embedding of the trailing rope_dim channels, interleaved pairs
+//     (2i, 2i+1), at position p = j*stride + offset.
+// One warp owns an entry (two entries per warp at D = 32): lane l takes the
+// channel pairs l, l+32, ... so every shared-memory read of the span is one
+// coalesced row segment, and the RMSNorm sum of squares is a warp reduction
+// with no block barrier.  The rotation angle is kept exact for long sequences
+// by working in turns: the frequency of pair i, theta^(-2i/rope_dim) / (2 pi)
+// turns per position, is a 64-bit fixed-point fraction of a turn that the
+// launcher evaluates once in double precision (a constant of theta and
+// rope_dim, passed by value: the GPU's FP64 units are far too slow to evaluate
+// it per thread), and p times it modulo 2^64 -- an integer product -- is the
+// angle's fraction of a turn, handed to sincospif.
+constexpr int kMaxRopePairs = 256;
+
+struct CompressExArgs {
+  const void* x;
+  const void* z;
+  const void* xp;          // nullptr: one stream
+  const void* zp;
+  const float* P;
+  const float* gamma;      // nullptr: no RMSNorm
+  float eps;
+  int rope_dim;            // 0: no rotary embedding
+  int pos_stride, pos_offset;
+  uint64_t rope_turn[kMaxRopePairs];  // pair i: theta^(-2i/rope_dim) / (2 pi) in units of 2^-64 turn
+  const int32_t* cu;
+  const int32_t* cu_cmp;
+  int B, r, S, E, rows_max;
+  void* out;
+  int* status;
+};
+
+template <typename TIn, typename TOut, int D>
+__global__ void __launch_bounds__(256) compress_ex_kernel(const __grid_constant__ CompressExArgs a) {
+  constexpr int kPairs = D / 2;
+  constexpr int kLanes = kPairs < 32 ? kPairs : 32;  // lanes per entry
+  constexpr int kPerWarp = 32 / kLanes;              // entries per warp
+  constexpr int kQ = kPairs / kLanes;                // channel pairs per lane
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_b, s_j0, s_j1;
+
+  const int r = a.r, S = a.S;
+  if (threadIdx.x < 32) locate_run(a.cu, a.B, r, a.E, a.status, &s_b, &s_j0, &s_j1);
+  __syncthreads();
+  const int b = s_b;
+  if (b < 0) return;
+  const int j0 = s_j0, j1 = s_j1;
+  const bool two = a.xp != nullptr;
+  const int tok0 = max(0, r * j0 + r - S);   // first local token the run reads
+  const int tok1 = r * j1;                   // one past the last
+  const int cur0 = two ? r * j0 : tok0;      // first token of the current-half rows
+  const int Rc = tok1 - cur0;                // rows of x / z
+  const int Rp = two ? tok1 - r - tok0 : 0;  // rows of x_prev / z_prev
+  const int64_t seq0 = (int64_t)__ldg(a.cu + b);
+  const size_t region = (size_t)a.rows_max * D;
+  TIn* sx = reinterpret_cast<TIn*>(smem);
+  TIn* sz = sx + region;
+  TIn* sxp = sz + region;
+  TIn* szp = sxp + region;
+  const uint32_t bar_a = smem_u32(&bar);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_a, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t bc = (uint32_t)Rc * D * sizeof(TIn), bp = (uint32_t)Rp * D * sizeof(TIn);
+    mbar_arrive_expect_tx(bar_a, 2u * (bc + bp));
+    constexpr uint32_t kPiece = 32768;
+    const TIn* src[4] = {static_cast<const TIn*>(a.x) + (seq0 + cur0) * D,
+                         static_cast<const TIn*>(a.z) + (seq0 + cur0) * D,
+                         two ? static_cast<const TIn*>(a.xp) + (seq0 + tok0) * D : nullptr,
+                         two ? static_cast<const TIn*>(a.zp) + (seq0 + tok0) * D : nullptr};
+    TIn* dst[4] = {sx, sz, sxp, szp};
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t bytes = k < 2 ? bc : bp;
+      const char* g = reinterpret_cast<const char*>(src[k]);
+      for (uint32_t off = 0; off < bytes; off += kPiece)
+        bulk_g2s(smem_u32(dst[k]) + off, g + off, min(kPiece, bytes - off), bar_a);
+    }
+  }
+  const bool ok = mbar_wait_bounded(bar_a, 0, a.status);
+  if (__syncthreads_or(!ok)) return;
+
+  constexpr float kLog2e = 1.4426950408889634f;
+  const int lane = (int)threadIdx.x & 31, warp = (int)threadIdx.x >> 5;
+  const int le = lane % kLanes, sub = lane / kLanes;
+  const bool norm = a.gamma != nullptr;
+  const int rope_lo = D - a.rope_dim;              // first rotated channel (D: none)
+  TOut* out = static_cast<TOut*>(a.out) + (int64_t)__ldg(a.cu_cmp + b) * D;
+  const int n = j1 - j0;
+  constexpr int kWarps = 256 / 32;
+  for (int e0 = warp * kPerWarp; e0 < n; e0 += kWarps * kPerWarp) {  // uniform within a warp
+    const int e = e0 + sub;
+    const bool active = e < n;
+    const int j = j0 + e;
+    float y[2 * kQ];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const int c = 2 * (le + q * kLanes);
+      float m0 = -INFINITY, m1 = -INFINITY, den0 = 0.f, den1 = 0.f, num0 = 0.f, num1 = 0.f;
+      const int first = r * j + r - S;             // span position u reads local token first + u
+      for (int u0 = active ? max(0, -first) : S; u0 < S; u0 += 8) {
+        float lg0[8], lg1[8], xv0[8], xv1[8];
+        float cm0 = -INFINITY, cm1 = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int u = u0 + k;
+          lg0[k] = -INFINITY;
+          lg1[k] = -INFINITY;
+          xv0[k] = 0.f;
+          xv1[k] = 0.f;
+          if (u < S) {
+            const bool prev = two && u < r;
+            const size_t sofs = (size_t)(first + u - (prev ? tok0 : cur0)) * D + c;
+            const float2 zz = load_pair((prev ? szp : sz) + sofs), xx = load_pair((prev ? sxp : sx) + sofs);
+            const float2 pp = __ldg(reinterpret_cast<const float2*>(a.P + (size_t)u * D + c));
+            lg0[k] = (zz.x + pp.x) * kLog2e;
+            lg1[k] = (zz.y + pp.y) * kLog2e;
+            xv0[k] = xx.x;
+            xv1[k] = xx.y;
+            cm0 = fmaxf(cm0, lg0[k]);
+            cm1 = fmaxf(cm1, lg1[k]);
+          }
+        }
+        const float mn0 = fmaxf(m0, cm0), mn1 = fmaxf(m1, cm1);
+        const float sc0 = ex2f(m0 - mn0), sc1 = ex2f(m1 - mn1);  // 0 while the sums are empty
+        den0 *= sc0;
+        num0 *= sc0;
+        den1 *= sc1;
+        num1 *= sc1;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float w0 = ex2f(lg0[k] - mn0), w1 = ex2f(lg1[k] - mn1);
+          den0 += w0;
+          den1 += w1;
+          num0 = fmaf(w0, xv0[k], num0);
+          num1 = fmaf(w1, xv1[k], num1);
+        }
+        m0 = mn0;
+        m1 = mn1;
+      }
+      y[2 * q] = active ? num0 / den0 : 0.f;
+      y[2 * q + 1] = active ? num1 / den1 : 0.f;
+    }
+    if (norm) {
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < 2 * kQ; ++k) ss = fmaf(y[k], y[k], ss);
+#pragma unroll
+      for (int o = kLanes / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float inv = rsqrtf(ss * (1.0f / D) + a.eps);
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const float2 g = __ldg(reinterpret_cast<const float2*>(a.gamma + 2 * (le + q * kLanes)));
+        y[2 * q] *= inv * g.x;
+        y[2 * q + 1] *= inv * g.y;
+      }
+    }
+    if (!active) continue;
+    const int64_t p = (int64_t)j * a.pos_stride + a.pos_offset;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const int c = 2 * (le + q * kLanes);
+      float y0 = y[2 * q], y1 = y[2 * q + 1];
+      if (c >= rope_lo) {
+        const uint64_t ph = (uint64_t)p * a.rope_turn[(c - rope_lo) >> 1];  // fraction of a turn
+        const float half_turns = (float)(int64_t)ph * 1.0842021724855044e-19f;  // 2^-63: angle / pi
+        float sn, cs;
+        sincospif(half_turns, &sn, &cs);
+        const float t0 = y0 * cs - y1 * sn;
+        y1 = y0 * sn + y1 * cs;
+        y0 = t0;
+      }
+      store_pair(out + (int64_t)j * D + c, y0, y1);
+    }
+  }
+}
+
 // Rows of the staging buffer and entries per CTA for a given span.
 static void compress_plan(int D, int r, int S, int in_bytes, int* rows_max, int* E, size_t* smem) {
   // runs of about 64 rows: many CTAs per SM, so one CTA's staging copy overlaps
@@ -213,6 +409,68 @@ cudaError_t launch_compress(const void* x, const void* z, const float* P, const 
     return launch_compress_t<float, float>(x, z, P, cu, cu_cmp, B, T_cap, D, r, S, out, status, stream);
   return launch_compress_t<__nv_bfloat16, __nv_bfloat16>(x, z, P, cu, cu_cmp, B, T_cap, D, r, S, out,
                                                          status, stream);
+}
+
+// Staging rows and entries per CTA of the variant: about 64 span rows per run,
+// fewer when `streams` staging buffers of that size would hold more than 64 KB
+// (several CTAs per SM keep copies in flight while others reduce).
+static void compress_ex_plan(int D, int r, int S, int in_bytes, int streams, int* rows_max, int* E,
+                             size_t* smem) {
+  const size_t row_bytes = (size_t)streams * D * in_bytes;
+  int e = S > 64 ? 1 : 64 / r;
+  const long long fit = ((long long)(64 * 1024 / row_bytes) - (S - r)) / r;
+  if (e > fit) e = (int)(fit < 1 ? 1 : fit);
+  *E = e;
+  *rows_max = (S - r) + r * e;
+  *smem = row_bytes * (size_t)*rows_max;
+}
+
+bool compress_ex_supported(int D, int r, int S, int in_bytes, bool two) {
+  int rows, E;
+  size_t smem;
+  compress_ex_plan(D, r, S, in_bytes, two ? 4 : 2, &rows, &E, &smem);
+  return smem <= 200 * 1024 && (D == 32 || D == 64 || D == 128 || D == 256 || D == 512);
+}
+
+template <typename TIn, typename TOut, int D>
+static cudaError_t launch_compress_ex_d(CompressExArgs& a, int T_cap, cudaStream_t stream) {
+  size_t smem;
+  compress_ex_plan(D, a.r, a.S, (int)sizeof(TIn), a.xp ? 4 : 2, &a.rows_max, &a.E, &smem);
+  auto kern = compress_ex_kernel<TIn, TOut, D>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const long long chunks = (long long)T_cap / ((long long)a.r * a.E) + a.B + 1;
+  kern<<<(unsigned)chunks, 256, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut>
+static cudaError_t launch_compress_ex_t(CompressExArgs& a, int D, int T_cap, cudaStream_t stream) {
+  switch (D) {
+    case 32: return launch_compress_ex_d<TIn, TOut, 32>(a, T_cap, stream);
+    case 64: return launch_compress_ex_d<TIn, TOut, 64>(a, T_cap, stream);
+    case 128: return launch_compress_ex_d<TIn, TOut, 128>(a, T_cap, stream);
+    case 256: return launch_compress_ex_d<TIn, TOut, 256>(a, T_cap, stream);
+    case 512: return launch_compress_ex_d<TIn, TOut, 512>(a, T_cap, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_compress_ex(const void* x, const void* z, const void* x_prev, const void* z_prev,
+                               const float* P, const float* gamma, float eps, int rope_dim, float theta,
+                               int pos_stride, int pos_offset, const int32_t* cu, const int32_t* cu_cmp,
+                               int B, int T_cap, int D, int r, int S, bool fp32, void* out, int* status,
+                               cudaStream_t stream) {
+  if (rope_dim / 2 > kMaxRopePairs) return cudaErrorInvalidValue;
+  CompressExArgs a{x, z, x_prev, z_prev, P, gamma, eps, rope_dim, pos_stride, pos_offset, {},
+                   cu, cu_cmp, B, r, S, 0, 0, out, status};
+  for (int i = 0; i < rope_dim / 2; ++i) {
+    // 2^64 / (2 pi) fixed-point turns per radian; the product stays below 2^63
+    const double turns = pow((double)theta, -2.0 * i / rope_dim) * 2935890503282001226.0;
+    a.rope_turn[i] = (uint64_t)llrint(turns);
+  }
+  if (fp32) return launch_compress_ex_t<float, float>(a, D, T_cap, stream);
+  return launch_compress_ex_t<__nv_bfloat16, __nv_bfloat16>(a, D, T_cap, stream);
 }
 
 // cu_cmp[b] = sum_{b'<b} floor(L_b' / r); also checks cu_seqlens.

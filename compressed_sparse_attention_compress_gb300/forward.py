@@ -24,6 +24,8 @@ class Forward:
         self.dev = torch.device("cuda", device)
         self.h = handle or api.Handle(device)
         self.x = inputs
+        if wl.compressor == "v4" and wl.separate_v:
+            raise ValueError("the v4 compressor takes K = V (one compressed KV stream)")
         dt = torch.float32 if wl.io_fp32 else torch.bfloat16
         T, H, d = wl.T_cap, wl.H, wl.d
         self.cu = inputs["cu_seqlens"]
@@ -51,6 +53,18 @@ class Forward:
     def compress(self, stream=None):
         wl, x = self.wl, self.x
         api.csa_compressed_offsets(self.h, self.cu, wl.ratio, self.cu_cmp, stream)
+        if wl.compressor == "v4":
+            # previous-half stream (overlapping spans), RMSNorm and RoPE fused in
+            api.csa_compress_ex(self.h, x["x_kv"], x["z_kv"], x["P_kv"], self.cu, self.cu_cmp, self.max_seqlen,
+                                wl.ratio, wl.overlap, self.kv_cmp, x_prev=x.get("x_kv_prev"),
+                                z_prev=x.get("z_kv_prev"), norm_weight=x["g_kv"], norm_eps=wl.norm_eps,
+                                rope_dim=wl.rope_kv, rope_theta=wl.rope_theta, stream=stream)
+            if wl.H_I > 0:
+                api.csa_compress_ex(self.h, x["x_I"], x["z_I"], x["P_I"], self.cu, self.cu_cmp, self.max_seqlen,
+                                    wl.ratio, wl.overlap, self.kI, x_prev=x.get("x_I_prev"),
+                                    z_prev=x.get("z_I_prev"), norm_weight=x["g_I"], norm_eps=wl.norm_eps,
+                                    rope_dim=wl.rope_I, rope_theta=wl.rope_theta, stream=stream)
+            return
         api.csa_compress(self.h, x["x_kv"], x["z_kv"], x["P_kv"], self.cu, self.cu_cmp, self.max_seqlen,
                          wl.ratio, wl.overlap, self.kv_cmp, stream)
         if self.v_cmp is not None:
@@ -100,7 +114,8 @@ class Forward:
 
 
     # inputs each stage needs first, in the order the stages run
-    _STAGE_INPUTS = (("cu_seqlens", "x_kv", "z_kv", "P_kv", "x_I", "z_I", "P_I", "v"), ("qI", "w"), ("q",))
+    _STAGE_INPUTS = (("cu_seqlens", "x_kv", "z_kv", "P_kv", "x_I", "z_I", "P_I", "v", "x_kv_prev", "z_kv_prev",
+                      "x_I_prev", "z_I_prev", "g_kv", "g_I"), ("qI", "w"), ("q",))
 
     def run_from_host(self, host: dict, stream=None, copy_stream=None):
         """The forward with its inputs still in (pinned) host memory.
@@ -151,7 +166,7 @@ def to_device(arrs: dict, io_fp32: bool, device: int = 0) -> dict:
         t = torch.from_numpy(v)
         if k == "cu_seqlens":
             out[k] = t.to(dev, torch.int32)
-        elif k.startswith("P_"):
+        elif k.startswith(("P_", "g_")):
             out[k] = t.to(dev, torch.float32)
         else:
             out[k] = t.to(dev, torch.float32 if io_fp32 else torch.bfloat16)

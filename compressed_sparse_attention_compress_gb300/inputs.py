@@ -4,12 +4,16 @@ This module draws random numbers and rounds them to bf16; it holds none of the
 method's arithmetic.  Every tensor comes from its own ``numpy`` generator
 stream, spawned in a fixed order from ``SeedSequence(seed)``:
 
-    x_kv, z_kv, P_kv, x_I, z_I, P_I, q, qI, w, v
+    x_kv, z_kv, P_kv, x_I, z_I, P_I, q, qI, w, v,
+    x_kv_prev, z_kv_prev, x_I_prev, z_I_prev, g_kv, g_I
 
 Each bf16 tensor is ``standard_normal`` float32 rounded to bf16
 (round-to-nearest-even); the rounded values are what both the GPU and the
 oracle consume.  The compressor positional biases ``P_kv``/``P_I`` are float32
-parameters and are not rounded.
+parameters and are not rounded.  Workloads with the DeepSeek-V4 style
+compressor (``compressor="v4"``) also draw the previous-half projections
+``*_prev`` (overlapping spans) and the float32 RMSNorm gains ``g_kv``/``g_I``
+as 1 + 0.1 N(0, 1).
 
 Workloads follow the shapes of the DeepSeek-V4 CSA/HCA layers described in
 "DeepSeek-V4 Attention Training Systems" (§2 phase table, §4 THD packing,
@@ -22,7 +26,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-STREAMS = ("x_kv", "z_kv", "P_kv", "x_I", "z_I", "P_I", "q", "qI", "w", "v")
+STREAMS = ("x_kv", "z_kv", "P_kv", "x_I", "z_I", "P_I", "q", "qI", "w", "v",
+           "x_kv_prev", "z_kv_prev", "x_I_prev", "z_I_prev", "g_kv", "g_I")
 
 
 def bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -64,6 +69,7 @@ class Workload:
     io_fp32: bool = False    # float32 I/O arrays holding bf16 values
     kl_mode: str = "none"    # "sparse" (selected set), "dense" (all visible) or "none"
     cap_align: int = 1       # T_cap = total rounded up to this
+    compressor: str = "plain"  # "plain" gate only; "v4": previous-half stream + RMSNorm + RoPE
     notes: str = ""
     extra: dict = field(default_factory=dict)
 
@@ -91,6 +97,18 @@ class Workload:
     @property
     def scale(self) -> float:
         return 1.0 / float(np.sqrt(self.d))
+
+    # compressor extras of the "v4" compressor: RMSNorm eps, RoPE band and base
+    norm_eps = 1e-6
+    rope_theta = 10000.0
+
+    @property
+    def rope_kv(self) -> int:
+        return min(64, self.d // 2)
+
+    @property
+    def rope_I(self) -> int:
+        return min(64, self.d_I // 2)
 
     @property
     def n_cmp(self) -> int:
@@ -159,4 +177,37 @@ def generate(wl: Workload, seed: int = 0) -> dict:
         out["w"] = normal("w", (T, wl.H_I))
     if wl.separate_v:
         out["v"] = normal("v", (T, wl.d))
+    if wl.compressor == "v4" and wl.ratio > 0:
+        if wl.overlap:
+            out["x_kv_prev"] = normal("x_kv_prev", (T, wl.d))
+            out["z_kv_prev"] = normal("z_kv_prev", (T, wl.d))
+        out["g_kv"] = 1.0 + 0.1 * normal("g_kv", (wl.d,), round_bf16=False)
+        if wl.H_I > 0:
+            if wl.overlap:
+                out["x_I_prev"] = normal("x_I_prev", (T, wl.d_I))
+                out["z_I_prev"] = normal("z_I_prev", (T, wl.d_I))
+            out["g_I"] = 1.0 + 0.1 * normal("g_I", (wl.d_I,), round_bf16=False)
+    return out
+
+
+COMPRESS_EX_STREAMS = ("x", "z", "x_prev", "z_prev", "P", "gamma")
+
+
+def generate_compress_ex(lengths, D: int, ratio: int, overlap: bool, two: bool, seed: int = 0,
+                         cap_align: int = 1) -> dict:
+    """Inputs of the compressor variant: bf16-valued x, z (and x_prev, z_prev
+    when ``two``) [T_cap, D] standard normal, a float32 positional bias [S, D]
+    standard normal and a float32 RMSNorm gain [D] drawn as 1 + 0.1 N(0, 1).
+    Each stream has its own generator spawned from ``SeedSequence(seed)``."""
+    ss = np.random.SeedSequence(seed).spawn(len(COMPRESS_EX_STREAMS))
+    gens = {name: np.random.default_rng(s) for name, s in zip(COMPRESS_EX_STREAMS, ss)}
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T = int(cu[-1])
+    T_cap = ((T + cap_align - 1) // cap_align) * cap_align
+    S = 2 * ratio if overlap else ratio
+    out = {"cu_seqlens": cu}
+    for name in ("x", "z") + (("x_prev", "z_prev") if two else ()):
+        out[name] = bf16_round(gens[name].standard_normal((T_cap, D), dtype=np.float32))
+    out["P"] = gens["P"].standard_normal((S, D), dtype=np.float32)
+    out["gamma"] = (1.0 + 0.1 * gens["gamma"].standard_normal(D)).astype(np.float32)
     return out

@@ -5,7 +5,8 @@ cost model, §5.5 replicated-state size):
   attention  4*H*d FLOPs per (query, candidate key)   QK^T + PV
   indexer    2*H_I*d_I FLOPs per (query, visible entry)
   teacher    2*H*d FLOPs per (query, C_t entry), counted once
-  compress   read x and z (2 B each per channel) + write one row per r tokens
+  compress   read x and z (2 B each per channel) + write one row per r tokens;
+             the "v4" compressor also reads the previous-half x and z
 """
 from __future__ import annotations
 
@@ -65,6 +66,8 @@ def counts(wl) -> dict:
         comp += wl.T * 4 * d + wl.n_cmp * 2 * d + wl.span * d * 4
         if wl.H_I > 0:
             comp += wl.T * 4 * wl.d_I + wl.n_cmp * 2 * wl.d_I + wl.span * wl.d_I * 4
+        if wl.compressor == "v4" and wl.overlap:   # previous-half x and z streams
+            comp += wl.T * 4 * (wl.d + (wl.d_I if wl.H_I > 0 else 0))
     out["compress_bytes"] = int(comp)
     out["gather_bytes"] = attn_pairs * d * 2
     out["total_flops"] = out["attn_flops"] + out["indexer_flops"] + out["teacher_flops"]

@@ -112,6 +112,40 @@ csa_status_t csa_compress(csa_handle_t handle, const void* x, const void* z,
                           int ratio, int overlap, csa_dtype_t dtype, void* out,
                           cudaStream_t stream);
 
+/* Compressor variant: csa_compress with the extras that sit around the
+ * compressor in a DeepSeek-V4 layer, fused before the single rounding of the
+ * output (§10 "compressor softmax and normalization intermediates"; §12
+ * invariants 2 "RoPE mode is per layer and per compressed coordinate system"
+ * and 3 "packed sample boundaries must reset both compressors"; §9 FP32
+ * positional parameter).  Per compressed entry, in this order:
+ *   1. gate     out[j,c] as csa_compress, except that with x_prev/z_prev given
+ *               (overlap = 1 only) span positions u < ratio -- the previous
+ *               block -- read x_prev/z_prev and u >= ratio read x/z;
+ *   2. RMSNorm  (norm_weight non-null) y <- y / sqrt(mean_c y_c^2 + norm_eps)
+ *               * norm_weight[c];
+ *   3. RoPE     (rope_dim > 0) the trailing rope_dim channels as interleaved
+ *               pairs (2i, 2i+1) rotated by p * rope_theta^(-2i/rope_dim),
+ *               p = j * rope_pos_stride + rope_pos_offset with j the entry's
+ *               index within its own sequence (1, 0: compressed coordinates;
+ *               ratio, 0: the first token of the entry's block).
+ *   x, z, x_prev, z_prev  [T_cap, D]  (dtype); x_prev, z_prev both null or both set
+ *   pos_bias              [S, D]      float32
+ *   norm_weight           [D]         float32 or null
+ *   out                   [cu_cmp[B], D] (dtype)
+ * The math is float32 (the rotation angle is reduced exactly in turns).
+ * Errors: CSA_ERR_INVALID_ARG for one-sided x_prev/z_prev, x_prev without
+ * overlap, an odd or oversize rope_dim, rope_theta <= 1 with rope_dim > 0 or a
+ * negative norm_eps; CSA_ERR_UNSUPPORTED unless D is a power of two in
+ * 32..512 and the staging rows fit shared memory (ratio-128 spans at D = 512
+ * do not).  No counterpart call is named by the page: it describes these
+ * steps only as parts of the layer around the compressor. */
+csa_status_t csa_compress_ex(csa_handle_t handle, const void* x, const void* z, const void* x_prev,
+                             const void* z_prev, const float* pos_bias, const float* norm_weight,
+                             float norm_eps, int rope_dim, float rope_theta, int rope_pos_stride,
+                             int rope_pos_offset, const int32_t* cu_seqlens, const int32_t* cu_cmp,
+                             int B, int T_cap, int max_seqlen, int D, int ratio, int overlap,
+                             csa_dtype_t dtype, void* out, cudaStream_t stream);
+
 /* Lightning-indexer scoring and per-query top-k (§3 indexer logit i_{t,j},
  * §8 "indexer scoring and radix top-k", §8.1 top-k padding, §8.2 flat global
  * index list).  For every packed query row t of sequence b:

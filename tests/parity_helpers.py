@@ -49,6 +49,16 @@ def check_compress(gpu_out: torch.Tensor, x, z, P, cu, ratio, overlap, n_c):
     return err
 
 
+def check_compress_ex(gpu_out: torch.Tensor, x, z, P, cu, ratio, overlap, n_c, **extras):
+    """The compressor variant (previous-half stream, RMSNorm, RoPE) against the oracle."""
+    ref = oracle.compress_ex(x, z, P, cu, ratio, overlap, **extras)
+    got = np32(gpu_out[:n_c]).astype(np.float64)
+    quant = bf16_half_ulp(ref) if gpu_out.dtype == torch.bfloat16 else 0.0
+    err = (np.abs(got - ref) - quant).max() if ref.size else 0.0
+    assert err <= ATOL, f"compress_ex max-abs {err}"
+    return err
+
+
 def check_topk(idx_gpu: np.ndarray, qI, w, kI, cu, ratio, topk, rows):
     """Compare GPU index rows (global compressed rows) with the oracle's on ``rows``."""
     idx_ref = oracle.indexer_topk(qI, w, kI, cu, ratio, topk, idx_gpu.shape[1], rows)

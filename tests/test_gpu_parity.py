@@ -6,6 +6,8 @@ top-k decision in the next one.  Small cases are checked on every query and
 span several tiles with ragged tails; the full-size workloads are checked on a
 sample of queries (all, for the KL sum where the oracle is cheap enough).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -42,7 +44,12 @@ def _check_all(f, arrs, wl, rows=None, sink=None, kl_full=True):
         cu_cmp = ph.np32(f.cu_cmp).astype(np.int64)
         assert np.array_equal(cu_cmp, oracle.compressed_offsets(cu, wl.ratio))
         n_c = int(cu_cmp[-1])
-        ph.check_compress(f.kv_cmp, arrs["x_kv"], arrs["z_kv"], arrs["P_kv"], cu, wl.ratio, wl.overlap, n_c)
+        if wl.compressor == "v4":
+            ph.check_compress_ex(f.kv_cmp, arrs["x_kv"], arrs["z_kv"], arrs["P_kv"], cu, wl.ratio, wl.overlap, n_c,
+                                 x_prev=arrs.get("x_kv_prev"), z_prev=arrs.get("z_kv_prev"), gamma=arrs["g_kv"],
+                                 eps=wl.norm_eps, rope_dim=wl.rope_kv, theta=wl.rope_theta)
+        else:
+            ph.check_compress(f.kv_cmp, arrs["x_kv"], arrs["z_kv"], arrs["P_kv"], cu, wl.ratio, wl.overlap, n_c)
         kv_cmp = ph.operand(f.kv_cmp[:n_c])
         v_cmp = None
         if wl.separate_v:
@@ -54,7 +61,12 @@ def _check_all(f, arrs, wl, rows=None, sink=None, kl_full=True):
                            cu, 0, wl.window, f.scale, None, rows, sink=sink)
         return
     if wl.H_I > 0:
-        ph.check_compress(f.kI, arrs["x_I"], arrs["z_I"], arrs["P_I"], cu, wl.ratio, wl.overlap, n_c)
+        if wl.compressor == "v4":
+            ph.check_compress_ex(f.kI, arrs["x_I"], arrs["z_I"], arrs["P_I"], cu, wl.ratio, wl.overlap, n_c,
+                                 x_prev=arrs.get("x_I_prev"), z_prev=arrs.get("z_I_prev"), gamma=arrs["g_I"],
+                                 eps=wl.norm_eps, rope_dim=wl.rope_I, theta=wl.rope_theta)
+        else:
+            ph.check_compress(f.kI, arrs["x_I"], arrs["z_I"], arrs["P_I"], cu, wl.ratio, wl.overlap, n_c)
         kI = ph.operand(f.kI[:n_c])
         idx = f.idx.cpu().numpy()
         ph.check_topk(idx, arrs["qI"], arrs["w"], kI, cu, wl.ratio, wl.topk, rows)
@@ -135,6 +147,27 @@ def test_full_size_workloads_sampled(name):
     f, arrs = _run(wl, seed=0)
     rows = _sample_rows(wl)
     _check_all(f, arrs, wl, rows=rows, kl_full=False)
+
+
+V4 = [
+    # the DeepSeek-V4 style compressor (previous-half stream, RMSNorm, RoPE) feeding the whole step
+    I.custom("v4_ragged_csa", lengths=[700, 0, 301, 1029, 5], ratio=4, overlap=True, H=64, d=128, window=128,
+             H_I=8, d_I=64, topk=96, k_pad=128, kl_mode="sparse", cap_align=64, compressor="v4"),
+    I.custom("v4_hca", lengths=[2000, 700], ratio=128, overlap=False, H=64, d=128, window=128, cap_align=32,
+             compressor="v4"),
+]
+
+
+@pytest.mark.parametrize("wl", V4, ids=[w.name for w in V4])
+def test_v4_compressor_workloads(wl):
+    f, arrs = _run(wl, seed=6)
+    _check_all(f, arrs, wl)
+
+
+def test_v4_compressor_full_size_packed_sampled():
+    wl = dataclasses.replace(I.WORKLOADS["thd128k"], compressor="v4")
+    f, arrs = _run(wl, seed=0)
+    _check_all(f, arrs, wl, rows=_sample_rows(wl), kl_full=False)
 
 
 def test_host_side_argument_errors():
