@@ -116,13 +116,13 @@ csa_status_t csa_compress(csa_handle_t h, const void* x, const void* z, const fl
   if ((dtype != CSA_BF16 && dtype != CSA_FP32) || (overlap != 0 && overlap != 1) || ratio < 1)
     return CSA_ERR_INVALID_ARG;
   const int S = overlap ? 2 * ratio : ratio;
-  if (!pow2_in(D, 32, 256) || ratio > 128 || S > 256) return CSA_ERR_UNSUPPORTED;
+  if (!pow2_in(D, 32, 512) || ratio > 128 || S > 256) return CSA_ERR_UNSUPPORTED;
   const bool fp32 = dtype == CSA_FP32;
-  if (!csa::compress_supported(D, ratio, S, fp32 ? 4 : 2)) return CSA_ERR_UNSUPPORTED;
+  if (!csa::compress_supported(D, ratio, S, fp32 ? 4 : 2, false)) return CSA_ERR_UNSUPPORTED;
   DeviceGuard g(h->device);
   if (!g.ok) return CSA_ERR_CUDA;
-  return from_cuda(csa::launch_compress(x, z, pos_bias, cu, cu_cmp, B, T_cap, D, ratio, S, fp32, out, h->status,
-                                        stream));
+  return from_cuda(csa::launch_compress(x, z, nullptr, nullptr, pos_bias, nullptr, 0.f, 0, 0.f, 0, 0, cu, cu_cmp, B,
+                                        T_cap, D, ratio, S, fp32, out, h->status, stream));
 }
 
 csa_status_t csa_compress_ex(csa_handle_t h, const void* x, const void* z, const void* x_prev,
@@ -145,10 +145,10 @@ csa_status_t csa_compress_ex(csa_handle_t h, const void* x, const void* z, const
   const int S = overlap ? 2 * ratio : ratio;
   if (!pow2_in(D, 32, 512) || ratio > 128 || S > 256) return CSA_ERR_UNSUPPORTED;
   const bool fp32 = dtype == CSA_FP32;
-  if (!csa::compress_ex_supported(D, ratio, S, fp32 ? 4 : 2, two)) return CSA_ERR_UNSUPPORTED;
+  if (!csa::compress_supported(D, ratio, S, fp32 ? 4 : 2, two)) return CSA_ERR_UNSUPPORTED;
   DeviceGuard g(h->device);
   if (!g.ok) return CSA_ERR_CUDA;
-  return from_cuda(csa::launch_compress_ex(x, z, x_prev, z_prev, pos_bias, norm_weight, norm_eps, rope_dim,
+  return from_cuda(csa::launch_compress(x, z, x_prev, z_prev, pos_bias, norm_weight, norm_eps, rope_dim,
                                            rope_theta, rope_pos_stride, rope_pos_offset, cu, cu_cmp, B, T_cap, D,
                                            ratio, S, fp32, out, h->status, stream));
 }

@@ -4,18 +4,37 @@
 // compressed; compression resets at packed-sample boundaries), §5.1 (spans
 // D_compress = 8 for overlapping ratio-4 CSA, 128 for ratio-128 HCA), §8.2
 // ("C4/C128 compression": learned-score reduction), §9 (FP32 positional
-// parameter, FP32 math).
+// parameter, FP32 math), §10 ("compressor softmax and normalization
+// intermediates"), §12 ("RoPE mode is per layer and per compressed coordinate
+// system").
 //
-// One CTA owns a run of consecutive entries of one sequence.  The raw rows the
-// run needs are one contiguous span of the packed x and z arrays, so a single
-// thread stages both spans into shared memory with bulk asynchronous copies
-// (cp.async.bulk, completion on an mbarrier); every input byte is read from
-// HBM once per CTA and the overlap between neighbouring entries is served from
-// shared memory.  A thread owns a pair of adjacent channels and walks the
-// run's entries; per entry it takes the span in chunks of 8 positions: the
-// chunk's logits z + P (log2 domain) in registers, one max, one rescale of the
-// running sums, then ex2 (MUFU) weights -- a float32 softmax over the span,
-// stored as a coalesced pair of the output row.
+// One kernel serves csa_compress and csa_compress_ex.  A CTA owns a run of
+// consecutive entries of one sequence.  The raw rows the run needs are one
+// contiguous span of each packed input stream, so a single thread stages them
+// into shared memory with bulk asynchronous copies (cp.async.bulk, completion
+// on an mbarrier): every input byte is read from HBM once per CTA and the
+// overlap between neighbouring entries is served from shared memory.
+//
+// One warp owns an entry (two entries per warp at D = 32): lane l takes the
+// channel pairs l, l+32, ... so every shared-memory read is one coalesced row
+// segment.  Per pair and span position: the logit z + P, one running maximum
+// per chunk of 8 positions, ex2 (MUFU) weights of (logit - max) * log2(e) --
+// a float32 softmax over the span.  The extras of csa_compress_ex follow
+// before the single rounding of the output:
+//   * a second (x_prev, z_prev) stream that span positions u < r (the previous
+//     block of an overlapping span) read instead of (x, z);
+//   * RMSNorm over the entry's D channels (a warp reduction, no barrier);
+//   * a rotary embedding of the trailing rope_dim channels, interleaved pairs
+//     (2i, 2i+1), at position p = j*stride + offset.  The angle is reduced
+//     exactly in turns: the frequency of pair i, theta^(-2i/rope_dim) / (2 pi)
+//     turns per position, is a 64-bit fixed-point fraction of a turn that the
+//     launcher evaluates once in double precision (a constant of theta and
+//     rope_dim, passed by value: the GPU's FP64 units are far too slow to
+//     evaluate it per thread); p times it modulo 2^64 -- an integer product --
+//     is the angle's fraction of a turn, so the sine and cosine only ever see
+//     an angle in [-pi, pi) (MUFU sin/cos, absolute error about 2^-21 there).
+// The ratio-4 overlapping span (8 positions) is compiled with its span fixed;
+// other spans take the general loop.
 #include <math.h>
 
 #include "common.cuh"
@@ -81,121 +100,6 @@ __device__ __forceinline__ void locate_run(const int32_t* __restrict__ cu, int B
 
 }  // namespace
 
-template <typename TIn, typename TOut>
-__global__ void __launch_bounds__(256)
-compress_kernel(const TIn* __restrict__ x, const TIn* __restrict__ z, const float* __restrict__ P,
-                const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_cmp, int B, int D,
-                int r, int S, int E, int rows_max, TOut* __restrict__ out, int* status) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ int s_b, s_j0, s_j1;
-
-  if (threadIdx.x < 32) locate_run(cu, B, r, E, status, &s_b, &s_j0, &s_j1);
-  __syncthreads();
-  const int b = s_b;
-  if (b < 0) return;
-  const int j0 = s_j0, j1 = s_j1;
-  const int tok0 = max(0, r * j0 + r - S);  // first local token the run reads
-  const int tok1 = r * j1;                  // one past the last
-  const int R = tok1 - tok0;                // <= rows_max by construction of E
-  const int64_t row0 = (int64_t)__ldg(cu + b) + tok0;
-  TIn* sx = reinterpret_cast<TIn*>(smem);
-  TIn* sz = sx + (size_t)rows_max * D;
-  const uint32_t bar_a = smem_u32(&bar);
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar_a, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t bytes = (uint32_t)R * D * sizeof(TIn);
-    mbar_arrive_expect_tx(bar_a, 2u * bytes);
-    constexpr uint32_t kPiece = 32768;
-    const char* gx = reinterpret_cast<const char*>(x + row0 * D);
-    const char* gz = reinterpret_cast<const char*>(z + row0 * D);
-    for (uint32_t off = 0; off < bytes; off += kPiece) {
-      const uint32_t len = min(kPiece, bytes - off);
-      bulk_g2s(smem_u32(sx) + off, gx + off, len, bar_a);
-      bulk_g2s(smem_u32(sz) + off, gz + off, len, bar_a);
-    }
-  }
-  if (!mbar_wait_bounded(bar_a, 0, status)) return;
-
-  const int64_t out0 = (int64_t)__ldg(cu_cmp + b);
-  constexpr float kLog2e = 1.4426950408889634f;
-  const int pairs = D >> 1;                        // D is even (checked on the host)
-  const int groups = (int)blockDim.x / pairs;      // entries worked on side by side
-  const int cpair = (int)threadIdx.x % pairs, eg = (int)threadIdx.x / pairs;
-  if (eg >= groups) return;
-  const int c = 2 * cpair;
-  for (int e = eg; e < j1 - j0; e += groups) {
-    const int j = j0 + e;
-    const int first = r * j + r - S;               // span position u reads local token first + u
-    float m0 = -INFINITY, m1 = -INFINITY, den0 = 0.f, den1 = 0.f, num0 = 0.f, num1 = 0.f;
-    for (int u0 = max(0, -first); u0 < S; u0 += 8) {
-      float lg0[8], lg1[8], xv0[8], xv1[8];
-      float cm0 = -INFINITY, cm1 = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int u = u0 + k;
-        lg0[k] = -INFINITY;
-        lg1[k] = -INFINITY;
-        xv0[k] = 0.f;
-        xv1[k] = 0.f;
-        if (u < S) {
-          const size_t sofs = (size_t)(first + u - tok0) * D + c;
-          const float2 zz = load_pair(sz + sofs), xx = load_pair(sx + sofs);
-          const float2 pp = __ldg(reinterpret_cast<const float2*>(P + (size_t)u * D + c));
-          lg0[k] = (zz.x + pp.x) * kLog2e;
-          lg1[k] = (zz.y + pp.y) * kLog2e;
-          xv0[k] = xx.x;
-          xv1[k] = xx.y;
-          cm0 = fmaxf(cm0, lg0[k]);
-          cm1 = fmaxf(cm1, lg1[k]);
-        }
-      }
-      const float mn0 = fmaxf(m0, cm0), mn1 = fmaxf(m1, cm1);
-      const float sc0 = ex2f(m0 - mn0), sc1 = ex2f(m1 - mn1);  // 0 while the sums are empty
-      den0 *= sc0;
-      num0 *= sc0;
-      den1 *= sc1;
-      num1 *= sc1;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float w0 = ex2f(lg0[k] - mn0), w1 = ex2f(lg1[k] - mn1);  // -inf (past the span) -> 0
-        den0 += w0;
-        den1 += w1;
-        num0 = fmaf(w0, xv0[k], num0);
-        num1 = fmaf(w1, xv1[k], num1);
-      }
-      m0 = mn0;
-      m1 = mn1;
-    }
-    store_pair(out + (out0 + j) * D + c, num0 / den0, num1 / den1);
-  }
-}
-
-// ---- compressor variant ---------------------------------------------------
-// The same gate, with the extras the page lists around the compressor (§10
-// "compressor softmax and normalization intermediates", §12 "RoPE mode is per
-// layer and per compressed coordinate system"), fused before the one rounding
-// of the output:
-//   * a second (x_prev, z_prev) stream that span positions u < r (the previous
-//     block of an overlapping span) read instead of (x, z);
-//   * RMSNorm over the entry's D channels;
-//   * a rotary embedding of the trailing rope_dim channels, interleaved pairs
-//     (2i, 2i+1), at position p = j*stride + offset.
-// One warp owns an entry (two entries per warp at D = 32): lane l takes the
-// channel pairs l, l+32, ... so every shared-memory read of the span is one
-// coalesced row segment, and the RMSNorm sum of squares is a warp reduction
-// with no block barrier.  The rotation angle is kept exact for long sequences
-// by working in turns: the frequency of pair i, theta^(-2i/rope_dim) / (2 pi)
-// turns per position, is a 64-bit fixed-point fraction of a turn that the
-// launcher evaluates once in double precision (a constant of theta and
-// rope_dim, passed by value: the GPU's FP64 units are far too slow to evaluate
-// it per thread), and p times it modulo 2^64 -- an integer product -- is the
-// angle's fraction of a turn, handed to sincospif.
 constexpr int kMaxRopePairs = 256;
 
 struct CompressExArgs {
@@ -216,17 +120,19 @@ struct CompressExArgs {
   int* status;
 };
 
-template <typename TIn, typename TOut, int D>
+// kR, kS: the ratio and span when fixed at compile time (0: taken from a).
+template <typename TIn, typename TOut, int D, int kR, int kS>
 __global__ void __launch_bounds__(256) compress_ex_kernel(const __grid_constant__ CompressExArgs a) {
   constexpr int kPairs = D / 2;
   constexpr int kLanes = kPairs < 32 ? kPairs : 32;  // lanes per entry
   constexpr int kPerWarp = 32 / kLanes;              // entries per warp
   constexpr int kQ = kPairs / kLanes;                // channel pairs per lane
+  constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_b, s_j0, s_j1;
 
-  const int r = a.r, S = a.S;
+  const int r = kR ? kR : a.r, S = kS ? kS : a.S;
   if (threadIdx.x < 32) locate_run(a.cu, a.B, r, a.E, a.status, &s_b, &s_j0, &s_j1);
   __syncthreads();
   const int b = s_b;
@@ -239,7 +145,7 @@ __global__ void __launch_bounds__(256) compress_ex_kernel(const __grid_constant_
   const int Rc = tok1 - cur0;                // rows of x / z
   const int Rp = two ? tok1 - r - tok0 : 0;  // rows of x_prev / z_prev
   const int64_t seq0 = (int64_t)__ldg(a.cu + b);
-  const size_t region = (size_t)a.rows_max * D;
+  const int region = a.rows_max * D;
   TIn* sx = reinterpret_cast<TIn*>(smem);
   TIn* sz = sx + region;
   TIn* sxp = sz + region;
@@ -270,11 +176,11 @@ __global__ void __launch_bounds__(256) compress_ex_kernel(const __grid_constant_
   const bool ok = mbar_wait_bounded(bar_a, 0, a.status);
   if (__syncthreads_or(!ok)) return;
 
-  constexpr float kLog2e = 1.4426950408889634f;
   const int lane = (int)threadIdx.x & 31, warp = (int)threadIdx.x >> 5;
   const int le = lane % kLanes, sub = lane / kLanes;
   const bool norm = a.gamma != nullptr;
   const int rope_lo = D - a.rope_dim;              // first rotated channel (D: none)
+  const int usplit = two ? r : 0;                  // positions u < usplit read the previous half
   TOut* out = static_cast<TOut*>(a.out) + (int64_t)__ldg(a.cu_cmp + b) * D;
   const int n = j1 - j0;
   constexpr int kWarps = 256 / 32;
@@ -282,15 +188,24 @@ __global__ void __launch_bounds__(256) compress_ex_kernel(const __grid_constant_
     const int e = e0 + sub;
     const bool active = e < n;
     const int j = j0 + e;
+    const int first = r * j + r - S;                 // span position u reads local token first + u
+    const int ustart = active ? max(0, -first) : S;  // positions before the sequence start are left out
+    // the row of span position u is base + u*D
+    const TIn* xcur = sx + (first - cur0) * D;
+    const TIn* zcur = sz + (first - cur0) * D;
+    const TIn* xprv = two ? sxp + (first - tok0) * D : xcur;
+    const TIn* zprv = two ? szp + (first - tok0) * D : zcur;
     float y[2 * kQ];
 #pragma unroll
     for (int q = 0; q < kQ; ++q) {
       const int c = 2 * (le + q * kLanes);
+      const float2* pcol = reinterpret_cast<const float2*>(a.P + c);
       float m0 = -INFINITY, m1 = -INFINITY, den0 = 0.f, den1 = 0.f, num0 = 0.f, num1 = 0.f;
-      const int first = r * j + r - S;             // span position u reads local token first + u
-      for (int u0 = active ? max(0, -first) : S; u0 < S; u0 += 8) {
+      // a fixed span runs one masked pass from u = 0; otherwise chunks from ustart
+      const int ubeg = kS ? 0 : ustart;
+      for (int u0 = ubeg; u0 < S; u0 += 8) {
         float lg0[8], lg1[8], xv0[8], xv1[8];
-        float cm0 = -INFINITY, cm1 = -INFINITY;
+        float cm0 = m0, cm1 = m1;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int u = u0 + k;
@@ -298,38 +213,42 @@ __global__ void __launch_bounds__(256) compress_ex_kernel(const __grid_constant_
           lg1[k] = -INFINITY;
           xv0[k] = 0.f;
           xv1[k] = 0.f;
-          if (u < S) {
-            const bool prev = two && u < r;
-            const size_t sofs = (size_t)(first + u - (prev ? tok0 : cur0)) * D + c;
-            const float2 zz = load_pair((prev ? szp : sz) + sofs), xx = load_pair((prev ? sxp : sx) + sofs);
-            const float2 pp = __ldg(reinterpret_cast<const float2*>(a.P + (size_t)u * D + c));
-            lg0[k] = (zz.x + pp.x) * kLog2e;
-            lg1[k] = (zz.y + pp.y) * kLog2e;
+          if ((kS ? k < kS : u < S) && u >= ustart) {
+            const bool pv = u < usplit;
+            const float2 zz = load_pair((pv ? zprv : zcur) + u * D + c);
+            const float2 xx = load_pair((pv ? xprv : xcur) + u * D + c);
+            const float2 pp = __ldg(pcol + u * (D / 2));
+            lg0[k] = zz.x + pp.x;
+            lg1[k] = zz.y + pp.y;
             xv0[k] = xx.x;
             xv1[k] = xx.y;
             cm0 = fmaxf(cm0, lg0[k]);
             cm1 = fmaxf(cm1, lg1[k]);
           }
         }
-        const float mn0 = fmaxf(m0, cm0), mn1 = fmaxf(m1, cm1);
-        const float sc0 = ex2f(m0 - mn0), sc1 = ex2f(m1 - mn1);  // 0 while the sums are empty
-        den0 *= sc0;
-        num0 *= sc0;
-        den1 *= sc1;
-        num1 *= sc1;
+        const float ms0 = -cm0 * kLog2e, ms1 = -cm1 * kLog2e;
+        if (u0 != ubeg) {                            // rescale the running sums to the new maximum
+          const float sc0 = ex2f(fmaf(m0, kLog2e, ms0)), sc1 = ex2f(fmaf(m1, kLog2e, ms1));
+          den0 *= sc0;
+          num0 *= sc0;
+          den1 *= sc1;
+          num1 *= sc1;
+        }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float w0 = ex2f(lg0[k] - mn0), w1 = ex2f(lg1[k] - mn1);
-          den0 += w0;
+          if (kS && k >= kS) break;
+          const float w0 = ex2f(fmaf(lg0[k], kLog2e, ms0)), w1 = ex2f(fmaf(lg1[k], kLog2e, ms1));
+          den0 += w0;                                // a left-out position has weight 0
           den1 += w1;
           num0 = fmaf(w0, xv0[k], num0);
           num1 = fmaf(w1, xv1[k], num1);
         }
-        m0 = mn0;
-        m1 = mn1;
+        m0 = cm0;
+        m1 = cm1;
       }
-      y[2 * q] = active ? num0 / den0 : 0.f;
-      y[2 * q + 1] = active ? num1 / den1 : 0.f;
+      // den >= 1 (the maximum's own weight): the fast reciprocal divide is exact to 2 ulp
+      y[2 * q] = active ? __fdividef(num0, den0) : 0.f;
+      y[2 * q + 1] = active ? __fdividef(num1, den1) : 0.f;
     }
     if (norm) {
       float ss = 0.f;
@@ -352,10 +271,11 @@ __global__ void __launch_bounds__(256) compress_ex_kernel(const __grid_constant_
       const int c = 2 * (le + q * kLanes);
       float y0 = y[2 * q], y1 = y[2 * q + 1];
       if (c >= rope_lo) {
-        const uint64_t ph = (uint64_t)p * a.rope_turn[(c - rope_lo) >> 1];  // fraction of a turn
-        const float half_turns = (float)(int64_t)ph * 1.0842021724855044e-19f;  // 2^-63: angle / pi
+        // fraction of a turn (top 32 bits, signed: [-1/2, 1/2) turn) -> radians in [-pi, pi)
+        const uint64_t ph = (uint64_t)p * a.rope_turn[(c - rope_lo) >> 1];
+        const float ang = (float)(int32_t)(uint32_t)(ph >> 32) * 1.4629180792671596e-09f;  // 2 pi / 2^32
         float sn, cs;
-        sincospif(half_turns, &sn, &cs);
+        __sincosf(ang, &sn, &cs);
         const float t0 = y0 * cs - y1 * sn;
         y1 = y0 * sn + y1 * cs;
         y0 = t0;
@@ -365,78 +285,34 @@ __global__ void __launch_bounds__(256) compress_ex_kernel(const __grid_constant_
   }
 }
 
-// Rows of the staging buffer and entries per CTA for a given span.
-static void compress_plan(int D, int r, int S, int in_bytes, int* rows_max, int* E, size_t* smem) {
-  // runs of about 64 rows: many CTAs per SM, so one CTA's staging copy overlaps
-  // another's reduction
-  int rows = S > 64 ? S : 64 + (S - r);
-  if ((size_t)2 * rows * D * in_bytes > 200 * 1024) rows = S;
-  *rows_max = rows;
-  *E = (rows - (S - r)) / r;
-  *smem = (size_t)2 * rows * D * in_bytes;
-}
-
-bool compress_supported(int D, int r, int S, int in_bytes) {
-  int rows, E;
-  size_t smem;
-  compress_plan(D, r, S, in_bytes, &rows, &E, &smem);
-  // a thread takes two adjacent channels; one row of channel pairs fits the CTA
-  return E >= 1 && smem <= 200 * 1024 && D % 2 == 0 && D / 2 <= 256;
-}
-
-template <typename TIn, typename TOut>
-static cudaError_t launch_compress_t(const void* x, const void* z, const float* P, const int32_t* cu,
-                                     const int32_t* cu_cmp, int B, int T_cap, int D, int r, int S,
-                                     void* out, int* status, cudaStream_t stream) {
-  int rows_max, E;
-  size_t smem;
-  compress_plan(D, r, S, (int)sizeof(TIn), &rows_max, &E, &smem);
-  auto kern = compress_kernel<TIn, TOut>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
-  const long long chunks = (long long)T_cap / ((long long)r * E) + B + 1;
-  if (chunks <= 0) return cudaSuccess;
-  kern<<<(unsigned)chunks, 256, smem, stream>>>(static_cast<const TIn*>(x), static_cast<const TIn*>(z), P,
-                                                cu, cu_cmp, B, D, r, S, E, rows_max,
-                                                static_cast<TOut*>(out), status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_compress(const void* x, const void* z, const float* P, const int32_t* cu,
-                            const int32_t* cu_cmp, int B, int T_cap, int D, int r, int S, bool fp32,
-                            void* out, int* status, cudaStream_t stream) {
-  if (fp32)
-    return launch_compress_t<float, float>(x, z, P, cu, cu_cmp, B, T_cap, D, r, S, out, status, stream);
-  return launch_compress_t<__nv_bfloat16, __nv_bfloat16>(x, z, P, cu, cu_cmp, B, T_cap, D, r, S, out,
-                                                         status, stream);
-}
-
-// Staging rows and entries per CTA of the variant: about 64 span rows per run,
-// fewer when `streams` staging buffers of that size would hold more than 64 KB
-// (several CTAs per SM keep copies in flight while others reduce).
-static void compress_ex_plan(int D, int r, int S, int in_bytes, int streams, int* rows_max, int* E,
-                             size_t* smem) {
+// Staging rows and entries per CTA: about 64 span rows per run, fewer when
+// `streams` staging buffers of that size would hold more than 40 KB (five
+// CTAs per SM keep copies in flight while others reduce), but at least one
+// entry per warp where the span allows.
+static void compress_plan(int D, int r, int S, int in_bytes, int streams, int* rows_max, int* E, size_t* smem) {
   const size_t row_bytes = (size_t)streams * D * in_bytes;
   int e = S > 64 ? 1 : 64 / r;
-  const long long fit = ((long long)(64 * 1024 / row_bytes) - (S - r)) / r;
+  const long long fit = ((long long)(40 * 1024 / row_bytes) - (S - r)) / r;
   if (e > fit) e = (int)(fit < 1 ? 1 : fit);
+  const int floor_e = S > 64 ? 1 : (64 / r < 8 ? 64 / r : 8);
+  if (e < floor_e && row_bytes * (size_t)((S - r) + r * floor_e) <= 200 * 1024) e = floor_e;
   *E = e;
   *rows_max = (S - r) + r * e;
   *smem = row_bytes * (size_t)*rows_max;
 }
 
-bool compress_ex_supported(int D, int r, int S, int in_bytes, bool two) {
+bool compress_supported(int D, int r, int S, int in_bytes, bool two) {
   int rows, E;
   size_t smem;
-  compress_ex_plan(D, r, S, in_bytes, two ? 4 : 2, &rows, &E, &smem);
+  compress_plan(D, r, S, in_bytes, two ? 4 : 2, &rows, &E, &smem);
   return smem <= 200 * 1024 && (D == 32 || D == 64 || D == 128 || D == 256 || D == 512);
 }
 
-template <typename TIn, typename TOut, int D>
-static cudaError_t launch_compress_ex_d(CompressExArgs& a, int T_cap, cudaStream_t stream) {
+template <typename TIn, typename TOut, int D, int kR, int kS>
+static cudaError_t launch_d(CompressExArgs& a, int T_cap, cudaStream_t stream) {
   size_t smem;
-  compress_ex_plan(D, a.r, a.S, (int)sizeof(TIn), a.xp ? 4 : 2, &a.rows_max, &a.E, &smem);
-  auto kern = compress_ex_kernel<TIn, TOut, D>;
+  compress_plan(D, a.r, a.S, (int)sizeof(TIn), a.xp ? 4 : 2, &a.rows_max, &a.E, &smem);
+  auto kern = compress_ex_kernel<TIn, TOut, D, kR, kS>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const long long chunks = (long long)T_cap / ((long long)a.r * a.E) + a.B + 1;
@@ -444,23 +320,28 @@ static cudaError_t launch_compress_ex_d(CompressExArgs& a, int T_cap, cudaStream
   return cudaGetLastError();
 }
 
+template <typename TIn, typename TOut, int D>
+static cudaError_t launch_span(CompressExArgs& a, int T_cap, cudaStream_t stream) {
+  if (a.r == 4 && a.S == 8) return launch_d<TIn, TOut, D, 4, 8>(a, T_cap, stream);
+  return launch_d<TIn, TOut, D, 0, 0>(a, T_cap, stream);
+}
+
 template <typename TIn, typename TOut>
-static cudaError_t launch_compress_ex_t(CompressExArgs& a, int D, int T_cap, cudaStream_t stream) {
+static cudaError_t launch_t(CompressExArgs& a, int D, int T_cap, cudaStream_t stream) {
   switch (D) {
-    case 32: return launch_compress_ex_d<TIn, TOut, 32>(a, T_cap, stream);
-    case 64: return launch_compress_ex_d<TIn, TOut, 64>(a, T_cap, stream);
-    case 128: return launch_compress_ex_d<TIn, TOut, 128>(a, T_cap, stream);
-    case 256: return launch_compress_ex_d<TIn, TOut, 256>(a, T_cap, stream);
-    case 512: return launch_compress_ex_d<TIn, TOut, 512>(a, T_cap, stream);
+    case 32: return launch_span<TIn, TOut, 32>(a, T_cap, stream);
+    case 64: return launch_span<TIn, TOut, 64>(a, T_cap, stream);
+    case 128: return launch_span<TIn, TOut, 128>(a, T_cap, stream);
+    case 256: return launch_span<TIn, TOut, 256>(a, T_cap, stream);
+    case 512: return launch_span<TIn, TOut, 512>(a, T_cap, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_compress_ex(const void* x, const void* z, const void* x_prev, const void* z_prev,
-                               const float* P, const float* gamma, float eps, int rope_dim, float theta,
-                               int pos_stride, int pos_offset, const int32_t* cu, const int32_t* cu_cmp,
-                               int B, int T_cap, int D, int r, int S, bool fp32, void* out, int* status,
-                               cudaStream_t stream) {
+cudaError_t launch_compress(const void* x, const void* z, const void* x_prev, const void* z_prev, const float* P,
+                            const float* gamma, float eps, int rope_dim, float theta, int pos_stride,
+                            int pos_offset, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int D,
+                            int r, int S, bool fp32, void* out, int* status, cudaStream_t stream) {
   if (rope_dim / 2 > kMaxRopePairs) return cudaErrorInvalidValue;
   CompressExArgs a{x, z, x_prev, z_prev, P, gamma, eps, rope_dim, pos_stride, pos_offset, {},
                    cu, cu_cmp, B, r, S, 0, 0, out, status};
@@ -469,8 +350,8 @@ cudaError_t launch_compress_ex(const void* x, const void* z, const void* x_prev,
     const double turns = pow((double)theta, -2.0 * i / rope_dim) * 2935890503282001226.0;
     a.rope_turn[i] = (uint64_t)llrint(turns);
   }
-  if (fp32) return launch_compress_ex_t<float, float>(a, D, T_cap, stream);
-  return launch_compress_ex_t<__nv_bfloat16, __nv_bfloat16>(a, D, T_cap, stream);
+  if (fp32) return launch_t<float, float>(a, D, T_cap, stream);
+  return launch_t<__nv_bfloat16, __nv_bfloat16>(a, D, T_cap, stream);
 }
 
 // cu_cmp[b] = sum_{b'<b} floor(L_b' / r); also checks cu_seqlens.

@@ -7,16 +7,13 @@
 
 namespace csa {
 
-bool compress_supported(int D, int r, int S, int in_bytes);
-cudaError_t launch_compress(const void* x, const void* z, const float* P, const int32_t* cu,
-                            const int32_t* cu_cmp, int B, int T_cap, int D, int r, int S, bool fp32,
-                            void* out, int* status, cudaStream_t stream);
-bool compress_ex_supported(int D, int r, int S, int in_bytes, bool two);
-cudaError_t launch_compress_ex(const void* x, const void* z, const void* x_prev, const void* z_prev,
-                               const float* P, const float* gamma, float eps, int rope_dim, float theta,
-                               int pos_stride, int pos_offset, const int32_t* cu, const int32_t* cu_cmp,
-                               int B, int T_cap, int D, int r, int S, bool fp32, void* out, int* status,
-                               cudaStream_t stream);
+// Block compression (csa_compress, and csa_compress_ex with its extras:
+// x_prev/z_prev, gamma and rope_dim > 0 each optional).
+bool compress_supported(int D, int r, int S, int in_bytes, bool two);
+cudaError_t launch_compress(const void* x, const void* z, const void* x_prev, const void* z_prev, const float* P,
+                            const float* gamma, float eps, int rope_dim, float theta, int pos_stride,
+                            int pos_offset, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int D,
+                            int r, int S, bool fp32, void* out, int* status, cudaStream_t stream);
 cudaError_t launch_compressed_offsets(const int32_t* cu, int B, int r, int32_t* cu_cmp, int* status,
                                       cudaStream_t stream);
 

@@ -105,7 +105,9 @@ csa_status_t csa_compressed_offsets(csa_handle_t handle, const int32_t* cu_seqle
  *   out[j,c] = sum_u softmax_u(z[t_u,c] + pos_bias[u,c]) * x[t_u,c]
  * over the span positions u with t_u >= 0 (positions before the sequence start
  * are left out).  The math is float32.  Rows of `out` past cu_cmp[B] are not
- * written.  D in {32, 64, 128, 256}, ratio in 1..128, S <= 256. */
+ * written.  D in {32, 64, 128, 256, 512}, ratio in 1..128, S <= 256; a span
+ * whose staging rows do not fit shared memory (ratio-128 spans at D = 512)
+ * returns CSA_ERR_UNSUPPORTED. */
 csa_status_t csa_compress(csa_handle_t handle, const void* x, const void* z,
                           const float* pos_bias, const int32_t* cu_seqlens,
                           const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int D,
