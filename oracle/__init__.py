@@ -15,6 +15,7 @@ from .oracle import (  # noqa: F401
     indexer_logits,
     indexer_topk,
     attention,
+    attention_bwd,
     indexer_kl,
     KIND_CSA,
     KIND_HCA,

@@ -389,6 +389,122 @@ void oracle_attention(int kind, const float* q, const float* kc, const float* vc
   }
 }
 
+/* Backward of oracle_attention for a list of query rows (§8.2 "main attention
+ * backward": consumes saved output/LSE and produces Q, KV and attention-sink
+ * gradients).  Given the upstream gradient dout = dL/do, for each query row t
+ * and head h, with the candidate list, s_i, lse and o of oracle_attention:
+ *   p_i      = exp(s_i - lse)                  (the attention weights)
+ *   D        = sum_c dout[c] o[c]
+ *   dp_i     = dout . V_i
+ *   ds_i     = p_i (dp_i - D)                  (gradient of L w.r.t. s_i / scale)
+ *   dq       = scale sum_i ds_i K_i
+ *   dK_i    += scale ds_i q                    (accumulated over queries)
+ *   dV_i    += p_i dout
+ *   dsink_h += -exp(sink_h - lse) D            (the sink is a logit with no value)
+ * These are the chain rule through o = sum_i p_i V_i and p = softmax(s, sink).
+ * dq is [nq, H, d]; dkc/dvc are [rows of kc, d], dkr/dvr [rows of kr, d] and
+ * dsink [H], all accumulated into (the caller zeroes them); any of dkc, dvc,
+ * dkr, dvr, dsink may be NULL (not wanted).  Capacity rows contribute nothing
+ * (dq = 0).  err[q] as in oracle_attention. */
+void oracle_attention_bwd(int kind, const float* q, const float* kc, const float* vc,
+                          const float* kr, const float* vr, const int32_t* idx, int k_pad,
+                          const float* sink, const int32_t* cu, const int32_t* cu_cmp, int B, int H,
+                          int d, int r, int W, double scale, const float* dout,
+                          const int64_t* rows, int nq, double* dq, double* dkc, double* dvc,
+                          double* dkr, double* dvr, double* dsink, int32_t* err) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int qi = 0; qi < nq; ++qi) {
+    const int64_t row = rows[qi];
+    double* dqq = dq + (int64_t)qi * H * d;
+    for (int64_t e = 0; e < (int64_t)H * d; ++e) dqq[e] = 0.0;
+    err[qi] = 0;
+    const int b = owner_sequence(cu, B, row);
+    if (b < 0) continue;
+    const int64_t t = row - cu[b];
+    const int64_t nvis = kind == ORACLE_WINDOW ? 0 : visible_count(t, r);
+    int64_t ncmp = 0;
+    const int64_t cap = kind == ORACLE_CSA ? k_pad : nvis;
+    int64_t* crow = (int64_t*)malloc(sizeof(int64_t) * (cap > 0 ? cap : 1));
+    if (kind == ORACLE_CSA) {
+      for (int i = 0; i < k_pad; ++i) {
+        const int64_t g = idx[row * (int64_t)k_pad + i];
+        if (g < 0) continue;
+        if (g < cu_cmp[b] || g >= cu_cmp[b] + nvis) { err[qi] = 1; continue; }
+        crow[ncmp++] = g;
+      }
+    } else if (kind == ORACLE_HCA) {
+      for (int64_t j = 0; j < nvis; ++j) crow[ncmp++] = cu_cmp[b] + j;
+    }
+    const int64_t w0 = t - W + 1 > 0 ? t - W + 1 : 0;
+    const int64_t nwin = t - w0 + 1;
+    const int64_t n = ncmp + nwin;
+    double* s = (double*)malloc(sizeof(double) * n);
+    double* p = (double*)malloc(sizeof(double) * n);
+    double* ds = (double*)malloc(sizeof(double) * n);
+    double* o = (double*)malloc(sizeof(double) * d);
+    /* this row's contributions to the key / value gradients, merged at the end */
+    double* gk = (double*)calloc((size_t)n * d, sizeof(double));
+    double* gv = (double*)calloc((size_t)n * d, sizeof(double));
+    double* gsink = (double*)calloc((size_t)H, sizeof(double));
+    for (int h = 0; h < H; ++h) {
+      const float* qh = q + (row * H + h) * (int64_t)d;
+      const float* gh = dout + (row * H + h) * (int64_t)d;
+      for (int64_t i = 0; i < n; ++i) {
+        const float* kk = i < ncmp ? kc + crow[i] * d : kr + (cu[b] + w0 + (i - ncmp)) * (int64_t)d;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += (double)qh[c] * (double)kk[c];
+        s[i] = scale * dot;
+      }
+      double m = -INFINITY;
+      for (int64_t i = 0; i < n; ++i) if (s[i] > m) m = s[i];
+      if (sink && (double)sink[h] > m) m = (double)sink[h];
+      double Z = 0.0;
+      for (int64_t i = 0; i < n; ++i) Z += exp(s[i] - m);
+      if (sink) Z += exp((double)sink[h] - m);
+      const double lse = m + log(Z);
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      for (int64_t i = 0; i < n; ++i) {
+        p[i] = exp(s[i] - lse);
+        const float* vv = i < ncmp ? vc + crow[i] * d : vr + (cu[b] + w0 + (i - ncmp)) * (int64_t)d;
+        for (int c = 0; c < d; ++c) o[c] += p[i] * (double)vv[c];
+      }
+      double D = 0.0;
+      for (int c = 0; c < d; ++c) D += (double)gh[c] * o[c];
+      for (int64_t i = 0; i < n; ++i) {
+        const float* vv = i < ncmp ? vc + crow[i] * d : vr + (cu[b] + w0 + (i - ncmp)) * (int64_t)d;
+        double dp = 0.0;
+        for (int c = 0; c < d; ++c) dp += (double)gh[c] * (double)vv[c];
+        ds[i] = p[i] * (dp - D);
+      }
+      double* dqh = dqq + (int64_t)h * d;
+      for (int64_t i = 0; i < n; ++i) {
+        const float* kk = i < ncmp ? kc + crow[i] * d : kr + (cu[b] + w0 + (i - ncmp)) * (int64_t)d;
+        for (int c = 0; c < d; ++c) {
+          dqh[c] += scale * ds[i] * (double)kk[c];
+          gk[i * d + c] += scale * ds[i] * (double)qh[c];
+          gv[i * d + c] += p[i] * (double)gh[c];
+        }
+      }
+      if (sink) gsink[h] = -exp((double)sink[h] - lse) * D;
+    }
+#pragma omp critical(oracle_attention_bwd_merge)
+    {
+      for (int64_t i = 0; i < n; ++i) {
+        const int64_t krow = i < ncmp ? crow[i] : cu[b] + w0 + (i - ncmp);
+        double* dk = i < ncmp ? dkc : dkr;
+        double* dv = i < ncmp ? dvc : dvr;
+        for (int c = 0; c < d; ++c) {
+          if (dk) dk[krow * d + c] += gk[i * d + c];
+          if (dv) dv[krow * d + c] += gv[i * d + c];
+        }
+      }
+      if (dsink && sink)
+        for (int h = 0; h < H; ++h) dsink[h] += gsink[h];
+    }
+    free(gsink); free(gv); free(gk); free(o); free(ds); free(p); free(s); free(crow);
+  }
+}
+
 /* Indexer KL auxiliary loss for a list of query rows (§3 equation; §2 phase
  * table: dense warm-up teacher over every visible entry, sparse mode over the
  * selected set; §9 FP32 loss math).

@@ -64,6 +64,8 @@ def _load():
         lib.oracle_indexer_topk.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, i32, P]
         lib.oracle_attention.argtypes = [i32, P, P, P, P, P, P, i32, P, P, P, i32, i32, i32, i32,
                                          i32, f64, P, i32, P, P, P, P]
+        lib.oracle_attention_bwd.argtypes = [i32, P, P, P, P, P, P, i32, P, P, P, i32, i32, i32, i32, i32,
+                                             f64, P, P, i32, P, P, P, P, P, P, P]
         lib.oracle_indexer_kl.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
                                           i32, f64, P, i32, P, P, P]
         _lib = lib
@@ -205,6 +207,51 @@ def attention(kind: int, q, k_cmp, v_cmp, k_raw, v_raw, cu_seqlens, ratio: int, 
                              float(scale), _ptr(rows), nq, _ptr(o), _ptr(lse), _ptr(lse_cmp),
                              _ptr(err))
     return o, lse, lse_cmp, err
+
+
+def attention_bwd(kind: int, q, k_cmp, v_cmp, k_raw, v_raw, cu_seqlens, ratio: int, window: int,
+                  scale: float, dout, idx=None, sink=None, rows=None, want_kv: bool = True):
+    """Gradients of the attention forward for upstream ``dout`` [T, H, d].
+
+    Returns a dict: ``dq`` [nq, H, d] for the given rows, and (``want_kv``) the
+    key / value gradients accumulated over those rows -- ``dk_cmp``, ``dv_cmp``
+    [rows of k_cmp, d], ``dk_raw``, ``dv_raw`` [T, d] -- and ``dsink`` [H]
+    (None without a sink), plus ``err`` [nq].  With K = V (v_cmp / v_raw None)
+    the gradient of the shared array is dk + dv.
+    """
+    q, k_raw, cu, dout = _f32(q), _f32(k_raw), _i32(cu_seqlens), _f32(dout)
+    v_raw = k_raw if v_raw is None else _f32(v_raw)
+    T, H, d = q.shape
+    if k_cmp is None:
+        k_cmp = np.zeros((1, d), np.float32)
+    k_cmp = _f32(k_cmp)
+    v_cmp = k_cmp if v_cmp is None else _f32(v_cmp)
+    rows = _rows(rows, T)
+    cu_cmp = compressed_offsets(cu, ratio if kind != KIND_WINDOW else 0)
+    if kind == KIND_CSA:
+        idx = _i32(idx)
+        k_pad = idx.shape[1]
+    else:
+        idx, k_pad = None, 0
+    sink = None if sink is None else _f32(sink)
+    nq = rows.shape[0]
+    dq = np.zeros((nq, H, d), np.float64)
+    out = {"dq": dq}
+    if want_kv:
+        out["dk_cmp"] = np.zeros(k_cmp.shape, np.float64)
+        out["dv_cmp"] = np.zeros(v_cmp.shape, np.float64)
+        out["dk_raw"] = np.zeros(k_raw.shape, np.float64)
+        out["dv_raw"] = np.zeros(v_raw.shape, np.float64)
+        out["dsink"] = np.zeros(H, np.float64) if sink is not None else None
+    err = np.zeros(nq, np.int32)
+    g = out.get
+    _load().oracle_attention_bwd(int(kind), _ptr(q), _ptr(k_cmp), _ptr(v_cmp), _ptr(k_raw), _ptr(v_raw),
+                                 _ptr(idx), int(k_pad), _ptr(sink), _ptr(cu), _ptr(cu_cmp), cu.shape[0] - 1, H, d,
+                                 int(ratio), int(window), float(scale), _ptr(dout), _ptr(rows), nq, _ptr(dq),
+                                 _ptr(g("dk_cmp")), _ptr(g("dv_cmp")), _ptr(g("dk_raw")), _ptr(g("dv_raw")),
+                                 _ptr(g("dsink")), _ptr(err))
+    out["err"] = err
+    return out
 
 
 def indexer_kl(q, k_cmp, qI, w, kI, cu_seqlens, ratio: int, scale: float, idx=None, rows=None):
