@@ -53,6 +53,10 @@ def _load():
         "csa_sparse_attn_fwd": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P],
         "hca_attn_fwd": [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P],
         "window_attn_fwd": [P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P],
+        "csa_sparse_attn_bwd": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P, P, P, P, P,
+                                P, P, P],
+        "hca_attn_bwd": [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P, P, P, P, P, P, P, P],
+        "window_attn_bwd": [P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P, P, P, P, P, P, P],
         "csa_indexer_kl": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, P, Z, P],
         "csa_indexer_kl_static_scratch": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, P],
     }
@@ -186,6 +190,37 @@ def window_attn_fwd(h: Handle, q, kv_raw, cu_seqlens, max_seqlen: int, window: i
     return _check("window_attn_fwd", LIB.window_attn_fwd(
         h.ptr, _p(q), _p(kv_raw), _p(v_raw), _p(sink), _p(cu_seqlens), cu_seqlens.numel() - 1, T_cap,
         int(max_seqlen), H, d, int(window), float(softmax_scale), _dtype(q), _p(out), _p(lse), _stream(stream)))
+
+
+def csa_sparse_attn_bwd(h: Handle, q, kv_cmp, kv_raw, idx, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int,
+                        window: int, softmax_scale: float, out, lse, dout, dq, dkv_cmp, dkv_raw, delta,
+                        v_cmp=None, v_raw=None, dv_cmp=None, dv_raw=None, sink=None, dsink=None, stream=None):
+    T_cap, H, d = q.shape
+    return _check("csa_sparse_attn_bwd", LIB.csa_sparse_attn_bwd(
+        h.ptr, _p(q), _p(kv_cmp), _p(v_cmp), _p(kv_raw), _p(v_raw), _p(idx), idx.shape[1], _p(sink),
+        _p(cu_seqlens), _p(cu_cmp), cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H, d, int(ratio),
+        int(window), float(softmax_scale), _dtype(q), _p(out), _p(lse), _p(dout), _p(dq), _p(dkv_cmp),
+        _p(dv_cmp), _p(dkv_raw), _p(dv_raw), _p(dsink), _p(delta), _stream(stream)))
+
+
+def hca_attn_bwd(h: Handle, q, kv_cmp, kv_raw, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int, window: int,
+                 softmax_scale: float, out, lse, dout, dq, dkv_cmp, dkv_raw, delta, v_cmp=None, v_raw=None,
+                 dv_cmp=None, dv_raw=None, sink=None, dsink=None, stream=None):
+    T_cap, H, d = q.shape
+    return _check("hca_attn_bwd", LIB.hca_attn_bwd(
+        h.ptr, _p(q), _p(kv_cmp), _p(v_cmp), _p(kv_raw), _p(v_raw), _p(sink), _p(cu_seqlens), _p(cu_cmp),
+        cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H, d, int(ratio), int(window), float(softmax_scale),
+        _dtype(q), _p(out), _p(lse), _p(dout), _p(dq), _p(dkv_cmp), _p(dv_cmp), _p(dkv_raw), _p(dv_raw),
+        _p(dsink), _p(delta), _stream(stream)))
+
+
+def window_attn_bwd(h: Handle, q, kv_raw, cu_seqlens, max_seqlen: int, window: int, softmax_scale: float, out,
+                    lse, dout, dq, dkv_raw, delta, v_raw=None, dv_raw=None, sink=None, dsink=None, stream=None):
+    T_cap, H, d = q.shape
+    return _check("window_attn_bwd", LIB.window_attn_bwd(
+        h.ptr, _p(q), _p(kv_raw), _p(v_raw), _p(sink), _p(cu_seqlens), cu_seqlens.numel() - 1, T_cap,
+        int(max_seqlen), H, d, int(window), float(softmax_scale), _dtype(q), _p(out), _p(lse), _p(dout), _p(dq),
+        _p(dkv_raw), _p(dv_raw), _p(dsink), _p(delta), _stream(stream)))
 
 
 def csa_indexer_kl_workspace(T_cap: int) -> int:

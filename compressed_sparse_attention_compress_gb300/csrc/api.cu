@@ -220,6 +220,72 @@ csa_status_t window_attn_fwd(csa_handle_t h, const void* q, const void* kv_raw, 
                      T_cap, max_seqlen, H, d, 0, window, scale, dtype, out, lse, nullptr, stream);
 }
 
+static csa_status_t attn_bwd_common(csa::AttnKind kind, csa_handle_t h, const void* q, const void* kv_cmp,
+                                    const void* v_cmp, const void* kv_raw, const void* v_raw, const int32_t* idx,
+                                    int k_pad, const float* sink, const int32_t* cu, const int32_t* cu_cmp, int B,
+                                    int T_cap, int max_seqlen, int H, int d, int ratio, int window, float scale,
+                                    csa_dtype_t dtype, const void* out, const float* lse, const void* dout,
+                                    void* dq, float* dkv_cmp, float* dv_cmp, float* dkv_raw, float* dv_raw,
+                                    float* dsink, float* delta, cudaStream_t stream) {
+  if (!h || !q || !kv_raw || !out || !lse || !dout || !dq || !dkv_raw || !delta ||
+      !packing_ok(cu, B, T_cap, max_seqlen))
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_raw) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dkv_raw) || !aligned16(lse) || !aligned16(delta) || !opt_aligned16(v_raw) ||
+      !opt_aligned16(v_cmp) || !opt_aligned16(dv_cmp) || !opt_aligned16(dv_raw) || !opt_aligned16(dkv_cmp))
+    return CSA_ERR_INVALID_ARG;
+  if ((v_raw == nullptr) != (dv_raw == nullptr)) return CSA_ERR_INVALID_ARG;  // dV wanted iff V is separate
+  if (kind != csa::kAttnWindow) {
+    if (!kv_cmp || !cu_cmp || !dkv_cmp || !aligned16(kv_cmp) || ratio < 1) return CSA_ERR_INVALID_ARG;
+    if ((v_cmp == nullptr) != (v_raw == nullptr) || (v_cmp == nullptr) != (dv_cmp == nullptr))
+      return CSA_ERR_INVALID_ARG;
+  }
+  if (kind == csa::kAttnCSA && (!idx || k_pad < 1)) return CSA_ERR_INVALID_ARG;
+  if ((dtype != CSA_BF16 && dtype != CSA_FP32) || window < 1 || !(scale > 0.f)) return CSA_ERR_INVALID_ARG;
+  if ((d != 64 && d != 128) || !pow2_in(H, 4, 128)) return CSA_ERR_UNSUPPORTED;
+  DeviceGuard g(h->device);
+  if (!g.ok) return CSA_ERR_CUDA;
+  const int n_cmp_cap = kind == csa::kAttnWindow ? 0 : T_cap / ratio;
+  csa::AttnBwdArgs a{q, kv_cmp, v_cmp, kv_raw, v_raw, idx, k_pad, sink, cu, cu_cmp, B, T_cap, H, d,
+                     kind == csa::kAttnWindow ? 0 : ratio, window, n_cmp_cap, scale, out, lse, dout, dq,
+                     kind == csa::kAttnWindow ? nullptr : dkv_cmp, kind == csa::kAttnWindow ? nullptr : dv_cmp,
+                     dkv_raw, dv_raw, dsink, delta, h->status};
+  return from_cuda(csa::launch_attention_bwd(kind, a, dtype == CSA_FP32, stream));
+}
+
+csa_status_t csa_sparse_attn_bwd(csa_handle_t h, const void* q, const void* kv_cmp, const void* v_cmp,
+                                 const void* kv_raw, const void* v_raw, const int32_t* idx, int k_pad,
+                                 const float* sink, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap,
+                                 int max_seqlen, int H, int d, int ratio, int window, float scale,
+                                 csa_dtype_t dtype, const void* out, const float* lse, const void* dout, void* dq,
+                                 float* dkv_cmp, float* dv_cmp, float* dkv_raw, float* dv_raw, float* dsink,
+                                 float* delta, cudaStream_t stream) {
+  return attn_bwd_common(csa::kAttnCSA, h, q, kv_cmp, v_cmp, kv_raw, v_raw, idx, k_pad, sink, cu, cu_cmp, B,
+                         T_cap, max_seqlen, H, d, ratio, window, scale, dtype, out, lse, dout, dq, dkv_cmp,
+                         dv_cmp, dkv_raw, dv_raw, dsink, delta, stream);
+}
+
+csa_status_t hca_attn_bwd(csa_handle_t h, const void* q, const void* kv_cmp, const void* v_cmp,
+                          const void* kv_raw, const void* v_raw, const float* sink, const int32_t* cu,
+                          const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H, int d, int ratio,
+                          int window, float scale, csa_dtype_t dtype, const void* out, const float* lse,
+                          const void* dout, void* dq, float* dkv_cmp, float* dv_cmp, float* dkv_raw,
+                          float* dv_raw, float* dsink, float* delta, cudaStream_t stream) {
+  return attn_bwd_common(csa::kAttnHCA, h, q, kv_cmp, v_cmp, kv_raw, v_raw, nullptr, 0, sink, cu, cu_cmp, B,
+                         T_cap, max_seqlen, H, d, ratio, window, scale, dtype, out, lse, dout, dq, dkv_cmp,
+                         dv_cmp, dkv_raw, dv_raw, dsink, delta, stream);
+}
+
+csa_status_t window_attn_bwd(csa_handle_t h, const void* q, const void* kv_raw, const void* v_raw,
+                             const float* sink, const int32_t* cu, int B, int T_cap, int max_seqlen, int H, int d,
+                             int window, float scale, csa_dtype_t dtype, const void* out, const float* lse,
+                             const void* dout, void* dq, float* dkv_raw, float* dv_raw, float* dsink, float* delta,
+                             cudaStream_t stream) {
+  return attn_bwd_common(csa::kAttnWindow, h, q, nullptr, nullptr, kv_raw, v_raw, nullptr, 0, sink, cu, nullptr,
+                         B, T_cap, max_seqlen, H, d, 0, window, scale, dtype, out, lse, dout, dq, nullptr, nullptr,
+                         dkv_raw, dv_raw, dsink, delta, stream);
+}
+
 size_t csa_indexer_kl_workspace(int T_cap) {
   if (T_cap < 0) return 0;
   return ((size_t)T_cap * 8 + 255) & ~(size_t)255;  // float kl[T_cap] + int32 csize[T_cap]

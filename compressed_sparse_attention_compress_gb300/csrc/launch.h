@@ -56,6 +56,37 @@ cudaError_t launch_attention_ws(AttnKind kind, const AttnArgs& a, cudaStream_t s
 bool attention_tc_supported(const AttnArgs& a, bool fp32);
 cudaError_t launch_attention_tc(AttnKind kind, const AttnArgs& a, cudaStream_t stream);
 
+// Attention backward: gradients of the forward above from its saved output
+// and LSE.  Key / value gradients are float32 and accumulated (zeroed by the
+// launcher); with K = V (v_cmp and v_raw null) dk_* receives dK + dV.
+struct AttnBwdArgs {
+  const void* q;
+  const void* k_cmp;
+  const void* v_cmp;
+  const void* k_raw;
+  const void* v_raw;
+  const int32_t* idx;
+  int k_pad;
+  const float* sink;
+  const int32_t* cu;
+  const int32_t* cu_cmp;
+  int B, T_cap, H, d, r, window;
+  int n_cmp_cap;          // rows of dk_cmp / dv_cmp to zero
+  float scale;
+  const void* out;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  float* dk_cmp;
+  float* dv_cmp;
+  float* dk_raw;
+  float* dv_raw;
+  float* dsink;
+  float* delta;           // [T_cap, H] scratch: dout . out
+  int* status;
+};
+cudaError_t launch_attention_bwd(AttnKind kind, const AttnBwdArgs& a, bool fp32, cudaStream_t stream);
+
 struct KLArgs {
   const void* q;
   const void* k_cmp;

@@ -102,6 +102,37 @@ class Forward:
                            idx=self.idx if sparse else None, lse_cmp=self.lse_cmp if sparse else None,
                            kl_per_query=self.kl_rows, n_valid=self.n_valid, stream=stream)
 
+    def backward(self, dout, stream=None, sink=None, dsink=None):
+        """Gradients of the attention stage for upstream ``dout`` [T_cap, H, d],
+        from the saved output and LSE of the last forward: ``dq`` (I/O dtype),
+        float32 ``dkv_cmp`` / ``dkv_raw`` (dK + dV of the shared KV rows, or dK
+        with ``dv_cmp`` / ``dv_raw`` for a separate V) and ``dsink`` when given."""
+        wl, x = self.wl, self.x
+        if getattr(self, "dq", None) is None:
+            T, d = wl.T_cap, wl.d
+            self.dq = torch.empty_like(self.out)
+            self.dkv_raw = torch.empty(T, d, dtype=torch.float32, device=self.dev)
+            self.dv_raw = torch.empty(T, d, dtype=torch.float32, device=self.dev) if wl.separate_v else None
+            if wl.ratio > 0:
+                n_cap = max(1, T // wl.ratio)
+                self.dkv_cmp = torch.empty(n_cap, d, dtype=torch.float32, device=self.dev)
+                self.dv_cmp = torch.empty(n_cap, d, dtype=torch.float32, device=self.dev) if wl.separate_v else None
+            self.delta = torch.empty(T, wl.H, dtype=torch.float32, device=self.dev)
+        v_raw = x.get("v") if wl.separate_v else None
+        common = dict(v_raw=v_raw, dv_raw=self.dv_raw, sink=sink, dsink=dsink, stream=stream)
+        if wl.ratio == 0:
+            api.window_attn_bwd(self.h, x["q"], x["x_kv"], self.cu, self.max_seqlen, wl.window, self.scale,
+                                self.out, self.lse, dout, self.dq, self.dkv_raw, self.delta, **common)
+        elif wl.H_I > 0:
+            api.csa_sparse_attn_bwd(self.h, x["q"], self.kv_cmp, x["x_kv"], self.idx, self.cu, self.cu_cmp,
+                                    self.max_seqlen, wl.ratio, wl.window, self.scale, self.out, self.lse, dout,
+                                    self.dq, self.dkv_cmp, self.dkv_raw, self.delta, v_cmp=self.v_cmp,
+                                    dv_cmp=self.dv_cmp, **common)
+        else:
+            api.hca_attn_bwd(self.h, x["q"], self.kv_cmp, x["x_kv"], self.cu, self.cu_cmp, self.max_seqlen,
+                             wl.ratio, wl.window, self.scale, self.out, self.lse, dout, self.dq, self.dkv_cmp,
+                             self.dkv_raw, self.delta, v_cmp=self.v_cmp, dv_cmp=self.dv_cmp, **common)
+
     def run(self, stream=None, sink=None):
         """The whole hot path of one forward, enqueued on ``stream``."""
         if self.wl.ratio > 0:

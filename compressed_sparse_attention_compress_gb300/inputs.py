@@ -211,3 +211,64 @@ def generate_compress_ex(lengths, D: int, ratio: int, overlap: bool, two: bool, 
     out["P"] = gens["P"].standard_normal((S, D), dtype=np.float32)
     out["gamma"] = (1.0 + 0.1 * gens["gamma"].standard_normal(D)).astype(np.float32)
     return out
+
+
+ATTN_BWD_STREAMS = ("q", "k_cmp", "k_raw", "v_cmp", "v_raw", "sel", "sink", "dout")
+
+
+def random_index_sets(lengths, ratio: int, topk: int, k_pad: int, rng, T_cap: int | None = None) -> np.ndarray:
+    """[T_cap, k_pad] int32: for every query a uniformly random set of
+    min(topk, |V_t|) of its visible compressed entries (global rows, ascending,
+    -1 padded); capacity rows are all -1.  Drawn as the smallest of per-entry
+    uniform keys, a block of queries at a time."""
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    cu_cmp = np.concatenate([[0], np.cumsum([L // ratio for L in lengths])]).astype(np.int64)
+    T = int(cu[-1])
+    idx = np.full((T if T_cap is None else T_cap, k_pad), -1, np.int32)
+    for b, L in enumerate(lengths):
+        n_b = L // ratio
+        if n_b == 0:
+            continue
+        for t0 in range(0, L, 256):
+            t = np.arange(t0, min(L, t0 + 256))
+            nvis = (t + 1) // ratio
+            keys = rng.random((t.size, n_b))
+            keys[np.arange(n_b)[None, :] >= nvis[:, None]] = 2.0   # not visible
+            m = min(topk, n_b)
+            part = np.argpartition(keys, m - 1, axis=1)[:, :m] if m < n_b else np.tile(np.arange(n_b), (t.size, 1))
+            for i, tt in enumerate(t):
+                c = part[i][keys[i, part[i]] < 2.0]
+                c.sort()
+                idx[cu[b] + tt, :c.size] = cu_cmp[b] + c
+    return idx
+
+
+def generate_attention_bwd(lengths, H: int, d: int, ratio: int, topk: int = 0, k_pad: int = 0,
+                           separate_v: bool = False, sink: bool = False, seed: int = 0, cap_align: int = 1) -> dict:
+    """Inputs of an attention backward test: bf16-valued q, dout [T_cap, H, d],
+    compressed and raw key (and value) rows, a random valid index set per
+    query (``topk`` > 0) and a float32 sink [H].  One generator per stream
+    spawned from ``SeedSequence(seed)``."""
+    ss = np.random.SeedSequence(seed).spawn(len(ATTN_BWD_STREAMS))
+    gens = {name: np.random.default_rng(s) for name, s in zip(ATTN_BWD_STREAMS, ss)}
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T = int(cu[-1])
+    T_cap = ((T + cap_align - 1) // cap_align) * cap_align
+    n_cap = max(1, T_cap // ratio) if ratio > 0 else 1
+    out = {"cu_seqlens": cu}
+
+    def normal(name, shape):
+        return bf16_round(gens[name].standard_normal(shape, dtype=np.float32))
+
+    out["q"] = normal("q", (T_cap, H, d))
+    out["dout"] = normal("dout", (T_cap, H, d))
+    out["k_raw"] = normal("k_raw", (T_cap, d))
+    out["k_cmp"] = normal("k_cmp", (n_cap, d))
+    if separate_v:
+        out["v_raw"] = normal("v_raw", (T_cap, d))
+        out["v_cmp"] = normal("v_cmp", (n_cap, d))
+    if sink:
+        out["sink"] = gens["sink"].standard_normal(H, dtype=np.float32)
+    if topk > 0:
+        out["idx"] = random_index_sets(lengths, ratio, topk, k_pad, gens["sel"], T_cap)
+    return out

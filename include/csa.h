@@ -210,6 +210,56 @@ csa_status_t window_attn_fwd(csa_handle_t handle, const void* q, const void* kv_
                              float softmax_scale, csa_dtype_t dtype, void* out, float* lse,
                              cudaStream_t stream);
 
+/* Attention backward, CSA (§8.2 "main attention backward": consumes the saved
+ * output and LSE and produces Q, KV and attention-sink gradients without
+ * materializing a dense attention matrix; §9 FP32 sink and softmax math).
+ * Arguments up to `dtype` are those of the forward call whose gradient is
+ * taken; out and lse are that call's outputs (out in dtype, lse float32).
+ * Given dout = dL/dout [T_cap, H, d] (dtype), with p_i = exp(s_i - lse[t,h]):
+ *   D[t,h]      = dout[t,h,:] . out[t,h,:]            (written to delta)
+ *   ds_i        = p_i (dout[t,h,:] . V_i - D[t,h])
+ *   dq[t,h,:]   = softmax_scale sum_i ds_i K_i          (dtype; capacity rows 0)
+ *   dK_i       += softmax_scale ds_i q[t,h,:],   dV_i += p_i dout[t,h,:]
+ *   dsink[h]    = -sum_t exp(sink[h] - lse[t,h]) D[t,h]
+ * Key / value gradients are float32 and summed over every query and head:
+ *   dkv_cmp [floor(T_cap/ratio), d], dkv_raw [T_cap, d]  receive dK (+ dV when
+ *   K = V, i.e. v_cmp / v_raw NULL: the gradient of the shared KV rows);
+ *   dv_cmp, dv_raw receive dV when V is separate, NULL otherwise.
+ * The call zeroes them first; the sums are float32 atomic additions, so
+ * their low bits depend on the order the GPU runs them in.  dsink [H] is
+ * written when both sink and dsink are given.  delta [T_cap, H] float32 is
+ * scratch (D above).  Errors as the forward; in addition every gradient
+ * array must be 16-byte aligned and dv_* set exactly when V is separate. */
+csa_status_t csa_sparse_attn_bwd(csa_handle_t handle, const void* q, const void* kv_cmp,
+                                 const void* v_cmp, const void* kv_raw, const void* v_raw,
+                                 const int32_t* idx, int k_pad, const float* sink,
+                                 const int32_t* cu_seqlens, const int32_t* cu_cmp, int B,
+                                 int T_cap, int max_seqlen, int H, int d, int ratio, int window,
+                                 float softmax_scale, csa_dtype_t dtype, const void* out,
+                                 const float* lse, const void* dout, void* dq, float* dkv_cmp,
+                                 float* dv_cmp, float* dkv_raw, float* dv_raw, float* dsink,
+                                 float* delta, cudaStream_t stream);
+
+/* HCA attention backward: as csa_sparse_attn_bwd with the compressed
+ * candidates of hca_attn_fwd (every visible entry). */
+csa_status_t hca_attn_bwd(csa_handle_t handle, const void* q, const void* kv_cmp,
+                          const void* v_cmp, const void* kv_raw, const void* v_raw,
+                          const float* sink, const int32_t* cu_seqlens, const int32_t* cu_cmp,
+                          int B, int T_cap, int max_seqlen, int H, int d, int ratio, int window,
+                          float softmax_scale, csa_dtype_t dtype, const void* out,
+                          const float* lse, const void* dout, void* dq, float* dkv_cmp,
+                          float* dv_cmp, float* dkv_raw, float* dv_raw, float* dsink,
+                          float* delta, cudaStream_t stream);
+
+/* Window-only attention backward: as csa_sparse_attn_bwd with the window rows
+ * as the only candidates (no compressed gradients). */
+csa_status_t window_attn_bwd(csa_handle_t handle, const void* q, const void* kv_raw,
+                             const void* v_raw, const float* sink, const int32_t* cu_seqlens,
+                             int B, int T_cap, int max_seqlen, int H, int d, int window,
+                             float softmax_scale, csa_dtype_t dtype, const void* out,
+                             const float* lse, const void* dout, void* dq, float* dkv_raw,
+                             float* dv_raw, float* dsink, float* delta, cudaStream_t stream);
+
 /* Indexer KL auxiliary loss (§3 equation
  *   L_I = sum_t KL(Softmax(a_{t,C_t}) || Softmax(i_{t,C_t})),
  * §2 phase table: dense teacher over every visible entry in the sparse
