@@ -8,7 +8,7 @@ dense teacher over every visible entry), the shape of the DeepSeek-V4 CSA
 layers in "DeepSeek-V4 Attention Training Systems" (§2 phase table).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-                    [--compressor plain|v4]
+                    [--compressor plain|v4] [--backward]
 
 Prints one JSON line (rank 0).  Multi-GPU: one process per GPU under
 torch.distributed.run; each rank runs its own copy of the workload (the path
@@ -212,6 +212,13 @@ def run_ours(args, wl):
     stages.append(("attention", f.attend))
     if wl.kl_mode != "none":
         stages.append(("indexer_kl", f.kl))
+    dout = None
+    if args.backward:
+        # upstream gradient of the attention output: bf16 N(0,1), its own seeded stream
+        g = np.random.default_rng(np.random.SeedSequence(args.seed).spawn(len(I.STREAMS) + 1)[-1])
+        dout = torch.from_numpy(I.bf16_round(g.standard_normal(tuple(f.out.shape), dtype=np.float32)))
+        dout = dout.to(f.out.device, f.out.dtype)
+        stages.append(("attention_bwd", lambda: f.backward(dout)))
 
     for _ in range(max(args.warmup, 3)):
         f.run()
@@ -244,6 +251,9 @@ def run_ours(args, wl):
     # copied in and the loss (or lse) read back inside the timed region
     host = {k: v.cpu().pin_memory() for k, v in dev_in.items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
+    dout_host = dout.cpu().pin_memory() if dout is not None else None
+    if dout_host is not None:
+        h2d += dout_host.numel() * dout_host.element_size()
     res = f.kl_sum if wl.kl_mode != "none" else f.lse
     res_host = torch.empty(res.shape, dtype=res.dtype).pin_memory()
     d2h = res_host.numel() * res_host.element_size()
@@ -251,6 +261,9 @@ def run_ours(args, wl):
     def e2e_step():
         # inputs copied in stage order on a side stream; each stage waits for its own
         f.run_from_host(host, stream)
+        if dout_host is not None:
+            dout.copy_(dout_host, non_blocking=True)
+            f.backward(dout, stream)
         res_host.copy_(res, non_blocking=True)
 
     for _ in range(2):
@@ -280,7 +293,8 @@ def run_ours(args, wl):
     per_launch = {"attention": ("tensor", counts["attn_flops"]),
                   "indexer_kl": ("tensor", counts["teacher_flops"]),
                   "indexer_topk": ("tensor", counts["indexer_flops"]),
-                  "compress": ("hbm", counts["compress_bytes"])}
+                  "compress": ("hbm", counts["compress_bytes"]),
+                  "attention_bwd": ("tensor", counts["attn_bwd_flops"])}
     bound, work = per_launch[dom]
     sec = stage_ms[dom] * 1e-3
     if bound == "tensor":
@@ -291,7 +305,8 @@ def run_ours(args, wl):
         achieved = work / sec / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
-    tflops = counts["total_flops"] / (ms_step * 1e-3) / 1e12
+    total_flops = counts["total_flops"] + (counts["attn_bwd_flops"] if args.backward else 0)
+    tflops = total_flops / (ms_step * 1e-3) / 1e12
     # the HBM-bound compress stage against the copy bandwidth, whichever stage dominates
     comp_hbm = None
     if "compress" in stage_ms:
@@ -306,6 +321,7 @@ def run_ours(args, wl):
         "config": {"workload": wl.name, "global_batch": wl.B * ws, "seq_len": max(wl.lengths),
                    "tokens_per_gpu": wl.T, "ratio": wl.ratio, "heads": wl.H, "head_dim": wl.d, "topk": wl.topk,
                    "window": wl.window, "kl": wl.kl_mode, "compressor": wl.compressor,
+                   "backward": bool(args.backward),
                    "parallelism": f"replicas{ws}",
                    "l2": "inputs larger than L2 (q alone is %.0f MB)" % (wl.T_cap * wl.H * wl.d * 2 / 1e6)},
         "tflops": tflops,
@@ -315,9 +331,13 @@ def run_ours(args, wl):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"},
         "compress_hbm": comp_hbm,
+        "attention_bwd": ({"ms": stage_ms["attention_bwd"], "flops": counts["attn_bwd_flops"],
+                           "tflops": counts["attn_bwd_flops"] / (stage_ms["attention_bwd"] * 1e-3) / 1e12,
+                           "frac": counts["attn_bwd_flops"] / (stage_ms["attention_bwd"] * 1e-3) / 1e12
+                           / peaks["bf16_tflops_sustained"]} if args.backward else None),
         "e2e": {"value": ws * wl.T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * f_launches(wl),
+        "gpu_launches": args.steps * (f_launches(wl) + (2 if args.backward else 0)),
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and ws >= 1:
@@ -362,6 +382,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="add the attention backward (dq, dKV from the saved output and LSE) to every step")
     ap.add_argument("--compressor", default="plain", choices=["plain", "v4"],
                     help="v4: previous-half stream + RMSNorm + RoPE fused into both compressors")
     args = ap.parse_args()

@@ -3,6 +3,7 @@
 Per-unit figures ("DeepSeek-V4 Attention Training Systems", §2 phase table
 cost model, §5.5 replicated-state size):
   attention  4*H*d FLOPs per (query, candidate key)   QK^T + PV
+  attn bwd   10*H*d FLOPs per (query, candidate key)  S recompute, dP, dQ, dK, dV
   indexer    2*H_I*d_I FLOPs per (query, visible entry)
   teacher    2*H*d FLOPs per (query, C_t entry), counted once
   compress   read x and z (2 B each per channel) + write one row per r tokens;
@@ -47,6 +48,7 @@ def counts(wl) -> dict:
         "visible_pairs": int(vis.sum()),
         "attn_pairs": attn_pairs,
         "attn_flops": 4 * H * d * attn_pairs,
+        "attn_bwd_flops": 10 * H * d * attn_pairs,
     }
     if wl.H_I > 0:
         out["indexer_flops"] = 2 * wl.H_I * wl.d_I * int(vis.sum())
