@@ -17,6 +17,7 @@ from .oracle import (  # noqa: F401
     attention,
     attention_bwd,
     indexer_kl,
+    indexer_kl_bwd,
     KIND_CSA,
     KIND_HCA,
     KIND_WINDOW,

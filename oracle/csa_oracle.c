@@ -580,3 +580,100 @@ void oracle_indexer_kl(const float* q, const float* kc, const float* qI,
     free(s); free(p); free(ilog); free(all_i); free(cj);
   }
 }
+
+/* Backward of the indexer KL loss for a list of query rows (§8.2 "indexer
+ * backward": the discrete top-k has no LM-loss gradient, so the indexer is
+ * trained only through this auxiliary loss; "teacher operands are detached").
+ * With p(j) the teacher and q(j) = softmax over C_t of i_{t,j} as in
+ * oracle_indexer_kl, the gradient of KL(p || q) with respect to the indexer
+ * logit is g_j = q(j) - p(j) (p sums to 1); times the upstream loss gradient
+ * grad_scale, and through i_{t,j} = sum_h w[t,h] ReLU(qI[t,h,:] . kI[j,:]):
+ *   dw[t,h]     = sum_j g_j ReLU(a_{h,j}),            a_{h,j} = qI[t,h,:] . kI[j,:]
+ *   dqI[t,h,:]  = w[t,h] sum_j g_j [a_{h,j} > 0] kI[j,:]
+ *   dkI[j,:]   += sum_h g_j w[t,h] [a_{h,j} > 0] qI[t,h,:]   (accumulated over rows)
+ * dqI is [nq, H_I, dI], dw [nq, H_I], dkI [rows of kI, dI] (the caller zeroes
+ * it; may be NULL).  Rows with an empty C_t and capacity rows give zeros.
+ * err[q] as in oracle_indexer_kl. */
+void oracle_indexer_kl_bwd(const float* q, const float* kc, const float* qI,
+                           const float* w, const float* kI, const int32_t* idx,
+                           int k_pad, const int32_t* cu, const int32_t* cu_cmp,
+                           int B, int H, int d, int H_I, int dI, int r,
+                           double scale, double grad_scale, const int64_t* rows, int nq,
+                           double* dqI, double* dw, double* dkI, int32_t* err) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int qi = 0; qi < nq; ++qi) {
+    const int64_t row = rows[qi];
+    double* dqq = dqI + (int64_t)qi * H_I * dI;
+    double* dwq = dw + (int64_t)qi * H_I;
+    for (int64_t e = 0; e < (int64_t)H_I * dI; ++e) dqq[e] = 0.0;
+    for (int h = 0; h < H_I; ++h) dwq[h] = 0.0;
+    err[qi] = 0;
+    const int b = owner_sequence(cu, B, row);
+    if (b < 0) continue;
+    const int64_t t = row - cu[b];
+    const int64_t nvis = visible_count(t, r);
+    int64_t cap = idx ? k_pad : nvis;
+    int64_t* cj = (int64_t*)malloc(sizeof(int64_t) * (cap > 0 ? cap : 1));
+    int64_t n = 0;
+    if (idx) {
+      for (int i = 0; i < k_pad; ++i) {
+        const int64_t g = idx[row * (int64_t)k_pad + i];
+        if (g < 0) continue;
+        if (g < cu_cmp[b] || g >= cu_cmp[b] + nvis) { err[qi] = 1; continue; }
+        cj[n++] = g - cu_cmp[b];
+      }
+    } else {
+      for (int64_t j = 0; j < nvis; ++j) cj[n++] = j;
+    }
+    if (n == 0) { free(cj); continue; }
+    /* student distribution over C_t */
+    double* all_i = (double*)malloc(sizeof(double) * (nvis > 0 ? nvis : 1));
+    indexer_logits_one(qI, w, kI, row, cu_cmp[b], nvis, H_I, dI, all_i);
+    double mi = -INFINITY;
+    for (int64_t k = 0; k < n; ++k) if (all_i[cj[k]] > mi) mi = all_i[cj[k]];
+    double Zi = 0.0;
+    for (int64_t k = 0; k < n; ++k) Zi += exp(all_i[cj[k]] - mi);
+    /* teacher: head average of per-head softmaxes over C_t */
+    double* p = (double*)calloc((size_t)n, sizeof(double));
+    double* s = (double*)malloc(sizeof(double) * n);
+    for (int h = 0; h < H; ++h) {
+      const float* qh = q + (row * H + h) * (int64_t)d;
+      for (int64_t k = 0; k < n; ++k) {
+        const float* kk = kc + (cu_cmp[b] + cj[k]) * (int64_t)d;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += (double)qh[c] * (double)kk[c];
+        s[k] = scale * dot;
+      }
+      double m = -INFINITY;
+      for (int64_t k = 0; k < n; ++k) if (s[k] > m) m = s[k];
+      double Z = 0.0;
+      for (int64_t k = 0; k < n; ++k) Z += exp(s[k] - m);
+      for (int64_t k = 0; k < n; ++k) p[k] += exp(s[k] - m) / Z;
+    }
+    /* g_j and the chain rule through the indexer logit */
+    double* gk = dkI ? (double*)calloc((size_t)n * dI, sizeof(double)) : NULL;
+    for (int64_t k = 0; k < n; ++k) {
+      const double g = grad_scale * (exp(all_i[cj[k]] - mi) / Zi - p[k] / H);
+      const float* kr = kI + (cu_cmp[b] + cj[k]) * (int64_t)dI;
+      for (int h = 0; h < H_I; ++h) {
+        const float* qh = qI + (row * H_I + h) * (int64_t)dI;
+        double a = 0.0;
+        for (int c = 0; c < dI; ++c) a += (double)qh[c] * (double)kr[c];
+        if (a <= 0.0) continue;
+        const double wh = (double)w[row * H_I + h];
+        dwq[h] += g * a;
+        for (int c = 0; c < dI; ++c) {
+          dqq[(int64_t)h * dI + c] += g * wh * (double)kr[c];
+          if (gk) gk[k * dI + c] += g * wh * (double)qh[c];
+        }
+      }
+    }
+    if (gk) {
+#pragma omp critical(oracle_indexer_kl_bwd_merge)
+      for (int64_t k = 0; k < n; ++k)
+        for (int c = 0; c < dI; ++c) dkI[(cu_cmp[b] + cj[k]) * (int64_t)dI + c] += gk[k * dI + c];
+      free(gk);
+    }
+    free(s); free(p); free(all_i); free(cj);
+  }
+}

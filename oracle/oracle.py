@@ -68,6 +68,8 @@ def _load():
                                              f64, P, P, i32, P, P, P, P, P, P, P]
         lib.oracle_indexer_kl.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
                                           i32, f64, P, i32, P, P, P]
+        lib.oracle_indexer_kl_bwd.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                              f64, f64, P, i32, P, P, P, P]
         _lib = lib
         return lib
 
@@ -275,3 +277,30 @@ def indexer_kl(q, k_cmp, qI, w, kI, cu_seqlens, ratio: int, scale: float, idx=No
                               int(ratio), float(scale), _ptr(rows), nq, _ptr(kl), _ptr(csize),
                               _ptr(err))
     return kl, csize, err
+
+
+def indexer_kl_bwd(q, k_cmp, qI, w, kI, cu_seqlens, ratio: int, scale: float, idx=None, rows=None,
+                   grad_scale: float = 1.0, want_kI: bool = True):
+    """Gradients of the indexer KL loss (teacher detached) for upstream
+    ``grad_scale``: dict with ``dqI`` [nq, H_I, dI], ``dw`` [nq, H_I], ``dkI``
+    [rows of kI, dI] (accumulated over the given rows; None unless want_kI)
+    and ``err`` [nq].  idx None = dense teacher over every visible entry."""
+    q, k_cmp, qI, w, kI, cu = _f32(q), _f32(k_cmp), _f32(qI), _f32(w), _f32(kI), _i32(cu_seqlens)
+    T, H, d = q.shape
+    _, H_I, dI = qI.shape
+    rows = _rows(rows, T)
+    cu_cmp = compressed_offsets(cu, ratio)
+    if idx is not None:
+        idx = _i32(idx)
+        k_pad = idx.shape[1]
+    else:
+        k_pad = 0
+    nq = rows.shape[0]
+    dqI = np.zeros((nq, H_I, dI), np.float64)
+    dw = np.zeros((nq, H_I), np.float64)
+    dkI = np.zeros(kI.shape, np.float64) if want_kI else None
+    err = np.zeros(nq, np.int32)
+    _load().oracle_indexer_kl_bwd(_ptr(q), _ptr(k_cmp), _ptr(qI), _ptr(w), _ptr(kI), _ptr(idx), int(k_pad),
+                                  _ptr(cu), _ptr(cu_cmp), cu.shape[0] - 1, H, d, H_I, dI, int(ratio), float(scale),
+                                  float(grad_scale), _ptr(rows), nq, _ptr(dqI), _ptr(dw), _ptr(dkI), _ptr(err))
+    return {"dqI": dqI, "dw": dw, "dkI": dkI, "err": err}
