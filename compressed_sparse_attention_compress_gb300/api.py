@@ -57,6 +57,7 @@ def _load():
                                 P, P, P],
         "hca_attn_bwd": [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P, P, P, P, P, P, P, P],
         "window_attn_bwd": [P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P, P, P, P, P, P, P],
+        "csa_indexer_kl_bwd": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, F, I, P, P, P, P],
         "csa_indexer_kl": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, P, Z, P],
         "csa_indexer_kl_static_scratch": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, P],
     }
@@ -252,3 +253,15 @@ def csa_indexer_kl_static_scratch(h: Handle, q, kv_cmp, qI, w, kI, cu_seqlens, c
         h.ptr, _p(q), _p(kv_cmp), _p(qI), _p(w), _p(kI), _p(idx), k_pad, _p(lse_cmp), _p(cu_seqlens),
         _p(cu_cmp), cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H, d, H_I, d_I, int(ratio),
         float(softmax_scale), _dtype(q), _p(kl_sum), _p(kl_per_query), _p(n_valid), _stream(stream)))
+
+
+def csa_indexer_kl_bwd(h: Handle, q, kv_cmp, qI, w, kI, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int,
+                       softmax_scale: float, dqI, dw, dkI, idx=None, lse_cmp=None, grad_scale: float = 1.0,
+                       stream=None):
+    T_cap, H, d = q.shape
+    _, H_I, d_I = qI.shape
+    k_pad = idx.shape[1] if idx is not None else 0
+    return _check("csa_indexer_kl_bwd", LIB.csa_indexer_kl_bwd(
+        h.ptr, _p(q), _p(kv_cmp), _p(qI), _p(w), _p(kI), _p(idx), k_pad, _p(lse_cmp), _p(cu_seqlens), _p(cu_cmp),
+        cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H, d, H_I, d_I, int(ratio), float(softmax_scale),
+        float(grad_scale), _dtype(q), _p(dqI), _p(dw), _p(dkI), _stream(stream)))

@@ -313,6 +313,29 @@ csa_status_t csa_indexer_kl(csa_handle_t h, const void* q, const void* kv_cmp, c
   return from_cuda(csa::launch_indexer_kl(a, dtype == CSA_FP32, stream));
 }
 
+csa_status_t csa_indexer_kl_bwd(csa_handle_t h, const void* q, const void* kv_cmp, const void* qI, const void* w,
+                                const void* kI, const int32_t* idx, int k_pad, const float* lse_cmp,
+                                const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H,
+                                int d, int H_I, int d_I, int ratio, float scale, float grad_scale,
+                                csa_dtype_t dtype, void* dqI, void* dw, float* dkI, cudaStream_t stream) {
+  if (!h || !q || !kv_cmp || !qI || !w || !kI || !cu_cmp || !dqI || !dw || !dkI ||
+      !packing_ok(cu, B, T_cap, max_seqlen))
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_cmp) || !aligned16(qI) || !aligned16(kI) || !aligned16(dqI) ||
+      !aligned16(dw) || !aligned16(dkI))
+    return CSA_ERR_INVALID_ARG;
+  if ((dtype != CSA_BF16 && dtype != CSA_FP32) || ratio < 1 || !(scale > 0.f) || !(grad_scale == grad_scale))
+    return CSA_ERR_INVALID_ARG;
+  if (idx != nullptr && k_pad < 1) return CSA_ERR_INVALID_ARG;
+  if ((d != 64 && d != 128) || !pow2_in(H, 4, 128) || !pow2_in(H_I, 1, 8) || (d_I != 32 && d_I != 64))
+    return CSA_ERR_UNSUPPORTED;
+  DeviceGuard g(h->device);
+  if (!g.ok) return CSA_ERR_CUDA;
+  csa::KLBwdArgs a{q, kv_cmp, qI, w, kI, idx, k_pad, lse_cmp, cu, cu_cmp, B, T_cap, H, d, H_I, d_I, ratio,
+                   T_cap / ratio, scale, grad_scale, dqI, dw, dkI, h->status};
+  return from_cuda(csa::launch_indexer_kl_bwd(a, dtype == CSA_FP32, stream));
+}
+
 }  // extern "C"
 
 namespace csa {

@@ -110,4 +110,27 @@ cudaError_t launch_indexer_kl(const KLArgs& a, bool fp32, cudaStream_t stream);
 bool indexer_kl_dense_tc_supported(const KLArgs& a, bool fp32);
 cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream);
 
+// Indexer KL backward: dqI, dw (I/O dtype) and float32 dkI (zeroed by the
+// launcher) for upstream gradient grad_scale; the teacher is detached.
+struct KLBwdArgs {
+  const void* q;
+  const void* k_cmp;
+  const void* qI;
+  const void* w;
+  const void* kI;
+  const int32_t* idx;   // nullptr: dense teacher
+  int k_pad;
+  const float* lse_cmp; // optional per-head normaliser over C_t (sparse mode)
+  const int32_t* cu;
+  const int32_t* cu_cmp;
+  int B, T_cap, H, d, H_I, d_I, r;
+  int n_cmp_cap;        // rows of dkI to zero
+  float scale, grad_scale;
+  void* dqI;
+  void* dw;
+  float* dkI;
+  int* status;
+};
+cudaError_t launch_indexer_kl_bwd(const KLBwdArgs& a, bool fp32, cudaStream_t stream);
+
 }  // namespace csa

@@ -133,6 +133,22 @@ class Forward:
                              wl.ratio, wl.window, self.scale, self.out, self.lse, dout, self.dq, self.dkv_cmp,
                              self.dkv_raw, self.delta, v_cmp=self.v_cmp, dv_cmp=self.dv_cmp, **common)
 
+    def indexer_backward(self, grad_scale: float = 1.0, stream=None):
+        """Gradients of the indexer KL loss (teacher detached) with respect to
+        qI, w (I/O dtype) and the compressed indexer keys (float32), for the
+        upstream gradient ``grad_scale``: the step the page runs eagerly inside
+        the forward (§8.2)."""
+        wl, x = self.wl, self.x
+        if getattr(self, "dqI", None) is None:
+            self.dqI = torch.empty_like(x["qI"])
+            self.dw = torch.empty_like(x["w"])
+            self.dkI = torch.empty(max(1, wl.T_cap // wl.ratio), wl.d_I, dtype=torch.float32, device=self.dev)
+        sparse = wl.kl_mode == "sparse"
+        api.csa_indexer_kl_bwd(self.h, x["q"], self.kv_cmp, x["qI"], x["w"], self.kI, self.cu, self.cu_cmp,
+                               self.max_seqlen, wl.ratio, self.scale, self.dqI, self.dw, self.dkI,
+                               idx=self.idx if sparse else None, lse_cmp=self.lse_cmp if sparse else None,
+                               grad_scale=grad_scale, stream=stream)
+
     def run(self, stream=None, sink=None):
         """The whole hot path of one forward, enqueued on ``stream``."""
         if self.wl.ratio > 0:

@@ -272,3 +272,30 @@ def generate_attention_bwd(lengths, H: int, d: int, ratio: int, topk: int = 0, k
     if topk > 0:
         out["idx"] = random_index_sets(lengths, ratio, topk, k_pad, gens["sel"], T_cap)
     return out
+
+
+INDEXER_BWD_STREAMS = ("q", "k_cmp", "qI", "w", "k_I", "sel", "k_raw")
+
+
+def generate_indexer_bwd(lengths, H: int, d: int, H_I: int, d_I: int, ratio: int, topk: int = 0, k_pad: int = 0,
+                         seed: int = 0, cap_align: int = 1) -> dict:
+    """Inputs of an indexer backward test: bf16-valued q [T_cap, H, d], compressed
+    main KV [n_cap, d], qI [T_cap, H_I, d_I], w [T_cap, H_I], indexer keys
+    [n_cap, d_I], raw KV rows [T_cap, d] (for the forward that gives lse_cmp)
+    and, with ``topk`` > 0, a random valid index set per query."""
+    ss = np.random.SeedSequence(seed).spawn(len(INDEXER_BWD_STREAMS))
+    gens = {name: np.random.default_rng(s) for name, s in zip(INDEXER_BWD_STREAMS, ss)}
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T = int(cu[-1])
+    T_cap = ((T + cap_align - 1) // cap_align) * cap_align
+    n_cap = max(1, T_cap // ratio)
+
+    def normal(name, shape):
+        return bf16_round(gens[name].standard_normal(shape, dtype=np.float32))
+
+    out = {"cu_seqlens": cu, "q": normal("q", (T_cap, H, d)), "k_cmp": normal("k_cmp", (n_cap, d)),
+           "qI": normal("qI", (T_cap, H_I, d_I)), "w": normal("w", (T_cap, H_I)),
+           "k_I": normal("k_I", (n_cap, d_I)), "k_raw": normal("k_raw", (T_cap, d))}
+    if topk > 0:
+        out["idx"] = random_index_sets(lengths, ratio, topk, k_pad, gens["sel"], T_cap)
+    return out

@@ -312,6 +312,29 @@ csa_status_t csa_indexer_kl_static_scratch(csa_handle_t handle, const void* q, c
                                            float* kl_sum, float* kl_per_query, int32_t* n_valid,
                                            cudaStream_t stream);
 
+/* Indexer backward: gradients of the indexer KL loss of csa_indexer_kl with
+ * respect to the indexer inputs (§8.2 "indexer backward": the discrete top-k
+ * has no LM-loss gradient, so the indexer learns through this auxiliary loss
+ * only; the teacher operands q and kv_cmp are detached).  With p(j), q(j) and
+ * C_t as in csa_indexer_kl and a_{h,j} = qI[t,h,:] . kI[j,:]:
+ *   g_j          = grad_scale * (q(j) - p(j))            (dL_I / d i_{t,j})
+ *   dw[t,h]      = sum_{j in C_t} g_j ReLU(a_{h,j})
+ *   dqI[t,h,:]   = w[t,h] sum_{j in C_t} g_j [a_{h,j} > 0] kI[j,:]
+ *   dkI[j,:]    += sum_t sum_h g_j w[t,h] [a_{h,j} > 0] qI[t,h,:]
+ * grad_scale is the upstream gradient of L_I (1 for the unit gradient the page
+ * uses when it runs this step eagerly inside the forward; the loss scale can
+ * be passed here or applied later).  dqI [T_cap, H_I, d_I] and dw [T_cap, H_I]
+ * (dtype) are written (0 for capacity rows and rows with an empty C_t); dkI
+ * [floor(T_cap/ratio), d_I] float32 is zeroed and accumulated with float32
+ * atomic additions.  idx / lse_cmp as in csa_indexer_kl.  Same limits. */
+csa_status_t csa_indexer_kl_bwd(csa_handle_t handle, const void* q, const void* kv_cmp,
+                                const void* qI, const void* w, const void* kI, const int32_t* idx,
+                                int k_pad, const float* lse_cmp, const int32_t* cu_seqlens,
+                                const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H,
+                                int d, int H_I, int d_I, int ratio, float softmax_scale,
+                                float grad_scale, csa_dtype_t dtype, void* dqI, void* dw,
+                                float* dkI, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

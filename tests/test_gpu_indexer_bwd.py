@@ -1,0 +1,112 @@
+"""GPU parity of the indexer backward (csa_indexer_kl_bwd) against the fp64 oracle.
+
+"DeepSeek-V4 Attention Training Systems" §8.2: the indexer is trained through
+its KL auxiliary loss only, with the teacher detached.  Inputs are synthetic
+(random rows and random valid index sets); in sparse mode the per-head
+normaliser lse_cmp comes from the GPU attention forward on the same inputs,
+as the product path passes it.
+
+Tolerance.  The teacher scores run on bf16 tensor-core operands and the
+exponentials in float32, so g = q - p carries absolute errors of about 1e-3 of
+the largest probability; each gradient tensor is compared elementwise as
+|gpu - ref| <= 1e-2 max|ref| + 2e-2 |ref| (+ the half-ulp of bf16 outputs).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from compressed_sparse_attention_compress_gb300 import inputs as I
+from tests import parity_helpers as ph
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # the CPU suite never collects GPU work
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from compressed_sparse_attention_compress_gb300 import api  # noqa: E402
+
+
+def _close(name, got, ref, quant=0.0):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return
+    bound = 1e-2 * np.abs(ref).max() + 2e-2 * np.abs(ref) + quant
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), f"{name}: {bad.sum()} of {ref.size} outside, worst {np.abs(got - ref).max()}"
+
+
+def _run(lengths, mode, H=64, d=128, H_I=8, d_I=64, ratio=4, topk=96, k_pad=128, fp32=False, seed=0,
+         grad_scale=1.0, cap_align=64, rows=None, check_kI=True):
+    sparse = mode != "dense"
+    a = I.generate_indexer_bwd(lengths, H, d, H_I, d_I, ratio, topk if sparse else 0, k_pad, seed, cap_align)
+    cu_np = a["cu_seqlens"]
+    T_cap = a["q"].shape[0]
+    dev = lambda k: (torch.from_numpy(a[k]).cuda() if fp32 else torch.from_numpy(a[k]).cuda().to(torch.bfloat16))  # noqa: E731
+    h = api.Handle(0)
+    cu = torch.from_numpy(cu_np).cuda()
+    cmp_np = oracle.compressed_offsets(cu_np, ratio)
+    cu_cmp = torch.from_numpy(cmp_np).cuda()
+    q, kc, qI, w, kI = dev("q"), dev("k_cmp"), dev("qI"), dev("w"), dev("k_I")
+    idx = torch.from_numpy(a["idx"]).cuda() if sparse else None
+    scale = 1.0 / np.sqrt(d)
+    ms = max(lengths + [1])
+    lse_cmp = None
+    if mode == "sparse_lse":   # the per-head normaliser over C_t from the attention forward
+        kr = dev("k_raw")
+        out = torch.empty_like(q)
+        lse = torch.empty(T_cap, H, dtype=torch.float32, device="cuda")
+        lse_cmp = torch.empty_like(lse)
+        api.csa_sparse_attn_fwd(h, q, kc, kr, idx, cu, cu_cmp, ms, ratio, 128, scale, out, lse, lse_cmp)
+    dqI = torch.full_like(qI, 5.0)
+    dw = torch.full_like(w, 5.0)
+    dkI = torch.full((max(1, T_cap // ratio), d_I), 3.0, dtype=torch.float32, device="cuda")
+    api.csa_indexer_kl_bwd(h, q, kc, qI, w, kI, cu, cu_cmp, ms, ratio, scale, dqI, dw, dkI, idx=idx,
+                           lse_cmp=lse_cmp, grad_scale=grad_scale)
+    torch.cuda.synchronize()
+    assert h.device_status() == 0
+    T = int(cu_np[-1])
+    rows = np.arange(T_cap) if rows is None else np.asarray(rows)
+    ref = oracle.indexer_kl_bwd(a["q"], a["k_cmp"], a["qI"], a["w"], a["k_I"], cu_np, ratio, scale,
+                                idx=a.get("idx"), rows=rows, grad_scale=grad_scale, want_kI=check_kI)
+    bf = not fp32
+    _close("dqI", ph.np32(dqI)[rows], ref["dqI"], ph.bf16_half_ulp(ref["dqI"]) if bf else 0.0)
+    _close("dw", ph.np32(dw)[rows], ref["dw"], ph.bf16_half_ulp(ref["dw"]) if bf else 0.0)
+    assert not ph.np32(dqI)[rows][rows >= T].any()
+    if check_kI:
+        n_c = int(cmp_np[-1])
+        _close("dkI", ph.np32(dkI)[:n_c], ref["dkI"][:n_c])
+        assert not ph.np32(dkI)[n_c:].any()
+    return dict(dqI=dqI, dw=dw, dkI=dkI, qI=qI, w=w, kI=kI, n_c=int(cmp_np[-1]))
+
+
+RAGGED = [700, 0, 301, 1029, 5]
+
+
+@pytest.mark.parametrize("mode", ["sparse", "sparse_lse", "dense"])
+def test_64_heads_bf16_ragged(mode):
+    _run(RAGGED, mode)
+
+
+@pytest.mark.parametrize("mode", ["sparse", "dense"])
+def test_small_shapes_fp32(mode):
+    _run([389, 120, 3], mode, H=16, d=64, H_I=4, d_I=32, topk=40, k_pad=64, fp32=True, seed=3)
+
+
+@pytest.mark.parametrize("H,H_I", [(4, 1), (128, 8)])
+def test_head_counts(H, H_I):
+    _run([517, 64], "sparse", H=H, H_I=H_I, topk=50, k_pad=64, seed=5, grad_scale=-3.0)
+
+
+def test_full_size_dense_warmup_layer_sampled():
+    # the dense teacher at L = 32768: dqI and dw on sampled rows against the
+    # oracle; dkI through the homogeneity identity sum kI.dkI = sum w.dw, which
+    # holds for the whole tensors at any size
+    L = 32768
+    rng = np.random.default_rng(1)
+    rows = np.sort(np.concatenate([rng.choice(L, 24, replace=False), [3, 4, 8191, L - 1]]))
+    res = _run([L], "dense", rows=rows, check_kI=False, cap_align=128)
+    f64 = lambda t: t.double()  # noqa: E731
+    lhs = (f64(res["dkI"][:res["n_c"]]) * f64(res["kI"][:res["n_c"]])).sum()
+    rhs = (f64(res["dw"]) * f64(res["w"])).sum()
+    assert abs(float(lhs - rhs)) <= 2e-2 * max(1e-3, float((f64(res["dw"]).abs() * f64(res["w"]).abs()).sum()))
