@@ -219,6 +219,8 @@ def run_ours(args, wl):
         dout = torch.from_numpy(I.bf16_round(g.standard_normal(tuple(f.out.shape), dtype=np.float32)))
         dout = dout.to(f.out.device, f.out.dtype)
         stages.append(("attention_bwd", lambda: f.backward(dout)))
+        if wl.kl_mode != "none":
+            stages.append(("indexer_bwd", f.indexer_backward))
 
     for _ in range(max(args.warmup, 3)):
         f.run()
@@ -264,6 +266,8 @@ def run_ours(args, wl):
         if dout_host is not None:
             dout.copy_(dout_host, non_blocking=True)
             f.backward(dout, stream)
+            if wl.kl_mode != "none":
+                f.indexer_backward(stream=stream)
         res_host.copy_(res, non_blocking=True)
 
     for _ in range(2):
@@ -294,7 +298,8 @@ def run_ours(args, wl):
                   "indexer_kl": ("tensor", counts["teacher_flops"]),
                   "indexer_topk": ("tensor", counts["indexer_flops"]),
                   "compress": ("hbm", counts["compress_bytes"]),
-                  "attention_bwd": ("tensor", counts["attn_bwd_flops"])}
+                  "attention_bwd": ("tensor", counts["attn_bwd_flops"]),
+                  "indexer_bwd": ("tensor", counts["indexer_bwd_flops"])}
     bound, work = per_launch[dom]
     sec = stage_ms[dom] * 1e-3
     if bound == "tensor":
@@ -305,7 +310,9 @@ def run_ours(args, wl):
         achieved = work / sec / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
-    total_flops = counts["total_flops"] + (counts["attn_bwd_flops"] if args.backward else 0)
+    total_flops = counts["total_flops"]
+    if args.backward:
+        total_flops += counts["attn_bwd_flops"] + (counts["indexer_bwd_flops"] if wl.kl_mode != "none" else 0)
     tflops = total_flops / (ms_step * 1e-3) / 1e12
     # the HBM-bound compress stage against the copy bandwidth, whichever stage dominates
     comp_hbm = None
@@ -335,9 +342,14 @@ def run_ours(args, wl):
                            "tflops": counts["attn_bwd_flops"] / (stage_ms["attention_bwd"] * 1e-3) / 1e12,
                            "frac": counts["attn_bwd_flops"] / (stage_ms["attention_bwd"] * 1e-3) / 1e12
                            / peaks["bf16_tflops_sustained"]} if args.backward else None),
+        "indexer_bwd": ({"ms": stage_ms["indexer_bwd"], "flops": counts["indexer_bwd_flops"],
+                         "tflops": counts["indexer_bwd_flops"] / (stage_ms["indexer_bwd"] * 1e-3) / 1e12,
+                         "frac": counts["indexer_bwd_flops"] / (stage_ms["indexer_bwd"] * 1e-3) / 1e12
+                         / peaks["bf16_tflops_sustained"]} if args.backward and wl.kl_mode != "none" else None),
         "e2e": {"value": ws * wl.T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * (f_launches(wl) + (2 if args.backward else 0)),
+        "gpu_launches": args.steps * (f_launches(wl) + ((2 + (1 if wl.kl_mode != "none" else 0))
+                                                        if args.backward else 0)),
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and ws >= 1:
@@ -383,7 +395,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward", action="store_true",
-                    help="add the attention backward (dq, dKV from the saved output and LSE) to every step")
+                    help="add the attention backward (dq, dKV from the saved output and LSE) and, with an "
+                         "indexer loss, the indexer backward to every step")
     ap.add_argument("--compressor", default="plain", choices=["plain", "v4"],
                     help="v4: previous-half stream + RMSNorm + RoPE fused into both compressors")
     args = ap.parse_args()

@@ -15,7 +15,9 @@
 // Pass 1 (the teacher's per-head log-sum-exp is skipped when the forward's
 // lse_cmp is given) also takes the student's log-sum-exp over C_t; pass 2
 // recomputes S = Q K^T on mma.sync for p(j) and the indexer dots for i_j, then
-// forms g and the three gradient terms with the tile in shared memory.
+// forms g.  The indexer dots a = qI kI^T, dqI += C kI and the key-block
+// gradient dkI = C^T qI (C[h, j] = g_j w_h [a_hj > 0] as a bf16 tile, the 8
+// indexer heads padded to 16 rows) are mma.sync products too.
 #include <math.h>
 
 #include "common.cuh"
@@ -26,9 +28,8 @@
 namespace csa {
 
 namespace {
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+__device__ __forceinline__ void red_add_v2(float* p, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};\n" ::"l"(p), "f"(a), "f"(b) : "memory");
 }
 }  // namespace
 
@@ -45,14 +46,18 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
   constexpr int kThreads = NW * 32;
   constexpr int kHK = 8 * kKeys;                         // (indexer head, key) pairs of a tile
   constexpr int kIterHK = kHK / kThreads;
-  constexpr int kIterDQ = (8 * DI + kThreads - 1) / kThreads;
-  constexpr int kChunks = kKeys * (DI / 8);              // (key, 8-channel chunk) pairs of a tile
+  constexpr int kKIS = DI + 8;                           // bf16 row stride of the indexer rows (16 B pad)
+  constexpr int kCS = kKeys + 8;                         // bf16 row stride of the coefficient tile
+  constexpr int kDQB = DI / 16;                          // 16-channel blocks of dqI
+  constexpr int kDQPerWarp = (kDQB + NW - 1) / NW;
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ __align__(128) uint8_t smem[];
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem);
   __nv_bfloat16* sK = sQ + kRows * kStride;                       // [2][kKeys][kStride]
-  __nv_bfloat16* sKI = sK + 2 * kKeys * kStride;                  // [2][kKeys][DI]
-  float* sQI = reinterpret_cast<float*>(sKI + 2 * kKeys * DI);    // [8][DI]
+  __nv_bfloat16* sKI = sK + 2 * kKeys * kStride;                  // [2][kKeys][kKIS]
+  __nv_bfloat16* sQIb = sKI + 2 * kKeys * kKIS;                   // [16][kKIS] (rows >= H_I zero)
+  __nv_bfloat16* sC = sQIb + 16 * kKIS;                           // [16][kCS]  (rows >= 8 zero)
+  float* sQI = reinterpret_cast<float*>(sC + 16 * kCS);           // [8][DI]
   float* sW = sQI + 8 * DI;                                       // [8]
   float* sPsum = sW + 8;                                          // [NW][kKeys]
   float* sA = sPsum + NW * kKeys;                                 // [8][kKeys] ReLU(a_hj)
@@ -82,10 +87,13 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
     if (h < H) v = Load8<TIn>::run(q + ((int64_t)row * H + h) * D + c * 8);
     *reinterpret_cast<uint4*>(sQ + h * kStride + c * 8) = v;
   }
-  for (int i = tid; i < 8 * DI; i += kThreads) {
+  for (int i = tid; i < 16 * DI; i += kThreads) {
     const int h = i / DI, c = i - h * DI;
-    sQI[i] = h < H_I ? to_f32(qI[((int64_t)row * H_I + h) * DI + c]) : 0.f;
+    const float v = h < H_I ? to_f32(qI[((int64_t)row * H_I + h) * DI + c]) : 0.f;
+    if (h < 8) sQI[i] = v;
+    sQIb[h * kKIS + c] = __float2bfloat16_rn(v);
   }
+  for (int i = tid; i < 16 * kCS; i += kThreads) sC[i] = __float2bfloat16_rn(0.f);
   if (tid < 8) sW[tid] = tid < H_I ? to_f32(w[(int64_t)row * H_I + tid]) : 0.f;
 
   const int cmp_limit = __ldg(cu_cmp + B);
@@ -111,7 +119,7 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
     for (int i = tid; i < kKeys * (DI / 8); i += kThreads) {
       const int k = i / (DI / 8), c = i - k * (DI / 8);
       const int rr = s_rows[buf][k] < cmp_limit ? s_rows[buf][k] : -1;
-      __nv_bfloat16* dst = sKI + (buf * kKeys + k) * DI + c * 8;
+      __nv_bfloat16* dst = sKI + (buf * kKeys + k) * kKIS + c * 8;
       if constexpr (sizeof(TIn) == 2) {
         cp_async_16_zfill(smem_u32(dst), kI + (int64_t)(rr < 0 ? 0 : rr) * DI + c * 8, rr >= 0);
       } else {
@@ -121,17 +129,29 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
       }
     }
   };
-  // ReLU(a_hj) of the tile's (head, key) pairs into sA
+  // ReLU(a_hj) of the tile's (head, key) pairs into sA: a = qI kI^T on mma.sync
+  // (indexer heads on M, padded to 16; 16 keys per warp and step)
   auto indexer_dots = [&](int buf) {
-    const __nv_bfloat16* tKI = sKI + buf * kKeys * DI;
-    for (int wi = tid; wi < kHK; wi += kThreads) {
-      const int k = wi & (kKeys - 1), h = wi / kKeys;
-      float dot = 0.f;
-      if (h < H_I) {
-#pragma unroll 8
-        for (int c = 0; c < DI; ++c) dot = fmaf(sQI[h * DI + c], __bfloat162float(tKI[k * DI + c]), dot);
+    const __nv_bfloat16* tKI = sKI + buf * kKeys * kKIS;
+    for (int np = warp; np < kKeys / 16; np += NW) {
+      float c2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < DI / 16; ++kk) {
+        uint32_t a[4], bq[4];
+        ldmatrix_x4(smem_u32(sQIb + (lane & 15) * kKIS + kk * 16 + (lane >> 4) * 8), a[0], a[1], a[2], a[3]);
+        const int key = np * 16 + (lane & 7) + (lane >> 4) * 8;
+        const int col = kk * 16 + ((lane >> 3) & 1) * 8;
+        ldmatrix_x4(smem_u32(tKI + key * kKIS + col), bq[0], bq[1], bq[2], bq[3]);
+        mma_bf16_16816(c2[0], a, bq);
+        mma_bf16_16816(c2[1], a, bq + 2);
       }
-      sA[wi] = fmaxf(dot, 0.f);
+      const int h = lane >> 2;   // rows 0..7 hold the 8 indexer heads
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int key = np * 16 + j * 8 + (lane & 3) * 2;
+        sA[h * kKeys + key] = fmaxf(c2[j][0], 0.f);
+        sA[h * kKeys + key + 1] = fmaxf(c2[j][1], 0.f);
+      }
     }
   };
 
@@ -220,11 +240,13 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
   // ---- pass 2: g_j = grad_scale (q(j) - p(j)) and the gradient terms ----
   const float inv_h = 1.f / (float)H;
   float dwp[kIterHK];
-  float dqp[kIterDQ];
+  float dqf[kDQPerWarp][2][4];   // dqI fragments of this warp's 16-channel blocks (rows = heads)
 #pragma unroll
   for (int m = 0; m < kIterHK; ++m) dwp[m] = 0.f;
 #pragma unroll
-  for (int m = 0; m < kIterDQ; ++m) dqp[m] = 0.f;
+  for (int i = 0; i < kDQPerWarp; ++i)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) dqf[i][j][0] = dqf[i][j][1] = dqf[i][j][2] = dqf[i][j][3] = 0.f;
   if (ntiles > 0) { resolve(0, 0); __syncthreads(); issue(0); }
   cp_async_commit();
   for (int it = 0; it < ntiles; ++it) {
@@ -270,36 +292,58 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
       const int wi = tid + m * kThreads;
       dwp[m] = fmaf(sG[wi & (kKeys - 1)], sA[wi], dwp[m]);
     }
-    // dqI_h[c] += sum_j g_j w_h [a_hj > 0] kI_j[c]
-    const __nv_bfloat16* tKI = sKI + buf * kKeys * DI;
+    // coefficient tile C[h][j] = g_j w_h [a_hj > 0] (bf16, rows 0..7)
+    for (int wi = tid; wi < kHK; wi += kThreads) {
+      const int k = wi & (kKeys - 1), h = wi / kKeys;
+      sC[h * kCS + k] = __float2bfloat16_rn(sA[wi] > 0.f ? sG[k] * sW[h] : 0.f);
+    }
+    __syncthreads();
+    const __nv_bfloat16* tKI = sKI + buf * kKeys * kKIS;
+    // dqI += C kI: M = heads (16), N = 16 channels per block, K = the tile's keys
 #pragma unroll
-    for (int m = 0; m < kIterDQ; ++m) {
-      const int o = tid + m * kThreads;
-      if (o < 8 * DI) {
-        const int h = o / DI, c = o - h * DI;
-        float acc = 0.f;
-        for (int k = 0; k < kKeys; ++k)
-          if (sA[h * kKeys + k] > 0.f) acc = fmaf(sG[k], __bfloat162float(tKI[k * DI + c]), acc);
-        dqp[m] = fmaf(sW[h], acc, dqp[m]);
+    for (int i = 0; i < kDQPerWarp; ++i) {
+      const int blk = warp + i * NW;
+      if (blk < kDQB) {
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          uint32_t a[4], bk[4];
+          ldmatrix_x4(smem_u32(sC + (lane & 15) * kCS + kk * 16 + (lane >> 4) * 8), a[0], a[1], a[2], a[3]);
+          const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int col = blk * 16 + (lane >> 4) * 8;
+          ldmatrix_x4_trans(smem_u32(tKI + key * kKIS + col), bk[0], bk[1], bk[2], bk[3]);
+          mma_bf16_16816(dqf[i][0], a, bk);
+          mma_bf16_16816(dqf[i][1], a, bk + 2);
+        }
       }
     }
-    // dkI_j[c0..c0+8) += sum_h g_j w_h [a_hj > 0] qI_h[c0..c0+8)
-    for (int o = tid; o < kChunks; o += kThreads) {
-      const int k = o / (DI / 8), c0 = (o - k * (DI / 8)) * 8;
-      const int rr = s_rows[buf][k];
-      const float g = sG[k];
-      if (rr < 0 || g == 0.f) continue;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // dkI = C^T qI for 16-key blocks: M = keys, N = channels, K = heads (16)
+    for (int kg = warp; kg < kKeys / 16; kg += NW) {
+      const int m0 = kg * 16;
+      uint32_t a[4];
+      const int mi = lane >> 3;
+      ldmatrix_x4_trans(smem_u32(sC + ((mi >> 1) * 8 + (lane & 7)) * kCS + m0 + (mi & 1) * 8), a[0], a[1], a[2],
+                        a[3]);
+      float acc[DI / 8][4];
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        if (!(sA[h * kKeys + k] > 0.f)) continue;
-        const float cf = g * sW[h];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(cf, sQI[h * DI + c0 + e], acc[e]);
+      for (int nd = 0; nd < DI / 16; ++nd) {
+        uint32_t bq[4];
+        const int hr = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int col = nd * 16 + (lane >> 4) * 8;
+        ldmatrix_x4_trans(smem_u32(sQIb + hr * kKIS + col), bq[0], bq[1], bq[2], bq[3]);
+        acc[2 * nd][0] = acc[2 * nd][1] = acc[2 * nd][2] = acc[2 * nd][3] = 0.f;
+        acc[2 * nd + 1][0] = acc[2 * nd + 1][1] = acc[2 * nd + 1][2] = acc[2 * nd + 1][3] = 0.f;
+        mma_bf16_16816(acc[2 * nd], a, bq);
+        mma_bf16_16816(acc[2 * nd + 1], a, bq + 2);
       }
-      float* dst = dkI + (int64_t)rr * DI + c0;
-      red_add_v4(dst, acc[0], acc[1], acc[2], acc[3]);
-      red_add_v4(dst + 4, acc[4], acc[5], acc[6], acc[7]);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int k = m0 + (lane >> 2) + i * 8;
+        const int rr = s_rows[buf][k];
+        if (rr < 0 || sG[k] == 0.f) continue;
+#pragma unroll
+        for (int nd8 = 0; nd8 < DI / 8; ++nd8)
+          red_add_v2(dkI + (int64_t)rr * DI + nd8 * 8 + (lane & 3) * 2, acc[nd8][2 * i], acc[nd8][2 * i + 1]);
+      }
     }
     __syncthreads();
   }
@@ -312,10 +356,19 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
     for (int k = 0; k < kKeys; ++k) sacc += sA[h * kKeys + k];
     dw[(int64_t)row * H_I + h] = from_f32<TIn>(sacc);
   }
+  // dqI: fragment rows 0..7 (e = 0, 1) are the indexer heads
 #pragma unroll
-  for (int m = 0; m < kIterDQ; ++m) {
-    const int o = tid + m * kThreads;
-    if (o < 8 * DI && o / DI < H_I) dqI[(int64_t)row * H_I * DI + o] = from_f32<TIn>(dqp[m]);
+  for (int i = 0; i < kDQPerWarp; ++i) {
+    const int blk = warp + i * NW;
+    const int h = lane >> 2;
+    if (blk >= kDQB || h >= H_I) continue;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int col = blk * 16 + j * 8 + (lane & 3) * 2;
+      TIn* dst = dqI + ((int64_t)row * H_I + h) * DI + col;
+      dst[0] = from_f32<TIn>(dqf[i][j][0]);
+      dst[1] = from_f32<TIn>(dqf[i][j][1]);
+    }
   }
 }
 
@@ -324,7 +377,8 @@ static cudaError_t launch_kl_bwd_t(const KLBwdArgs& a, cudaStream_t stream) {
   constexpr int kStride = AttnSmem<D>::kStride;
   constexpr int kThreads = NW * 32;
   constexpr int kHK = 8 * kKeys;
-  const size_t smem = (size_t)(NW * 16 + 2 * kKeys) * kStride * 2 + (size_t)2 * kKeys * DI * 2 +
+  const size_t smem = (size_t)(NW * 16 + 2 * kKeys) * kStride * 2 +
+                      ((size_t)2 * kKeys * (DI + 8) + 16 * (DI + 8) + 16 * (kKeys + 8)) * 2 +
                       ((size_t)8 * DI + 8 + NW * kKeys + kHK + kKeys + (kHK > 2 * kThreads ? kHK : 2 * kThreads)) * 4;
   auto kern = indexer_kl_bwd_kernel<TIn, D, NW, DI>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

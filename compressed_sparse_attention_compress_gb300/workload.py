@@ -4,6 +4,7 @@ Per-unit figures ("DeepSeek-V4 Attention Training Systems", §2 phase table
 cost model, §5.5 replicated-state size):
   attention  4*H*d FLOPs per (query, candidate key)   QK^T + PV
   attn bwd   10*H*d FLOPs per (query, candidate key)  S recompute, dP, dQ, dK, dV
+  index bwd  2*H*d + 6*H_I*d_I FLOPs per (query, C_t entry)  teacher recompute (once), dw, dqI, dkI
   indexer    2*H_I*d_I FLOPs per (query, visible entry)
   teacher    2*H*d FLOPs per (query, C_t entry), counted once
   compress   read x and z (2 B each per channel) + write one row per r tokens;
@@ -63,6 +64,7 @@ def counts(wl) -> dict:
     else:
         out["teacher_pairs"] = 0
     out["teacher_flops"] = 2 * H * d * out["teacher_pairs"]
+    out["indexer_bwd_flops"] = (2 * H * d + 6 * wl.H_I * wl.d_I) * out["teacher_pairs"]
     comp = 0
     if wl.ratio > 0:
         comp += wl.T * 4 * d + wl.n_cmp * 2 * d + wl.span * d * 4
