@@ -18,6 +18,9 @@ from .oracle import (  # noqa: F401
     attention_bwd,
     indexer_kl,
     indexer_kl_bwd,
+    quantize_fp8,
+    dequantize_fp8,
+    e4m3_value,
     KIND_CSA,
     KIND_HCA,
     KIND_WINDOW,

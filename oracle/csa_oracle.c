@@ -677,3 +677,55 @@ void oracle_indexer_kl_bwd(const float* q, const float* kc, const float* qI,
     free(s); free(p); free(all_i); free(cj);
   }
 }
+
+/* FP8 (E4M3) quantisation of the indexer operands (§1 and §9: the FP8 indexer
+ * for the index-search term).  The E4M3 format of the OCP 8-bit floating
+ * point specification: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits,
+ * subnormals below 2^-6 in steps of 2^-9, largest finite value 448.
+ * Each row of x gets a power-of-two scale s = 2^e, the smallest with
+ * max|x| / s <= 448 (s = 1 for an all-zero row), and the code of x / s
+ * rounded to the nearest representable value, ties to even.  The scale
+ * decision takes max|x| / 448 in float32.  codes [rows, cols], scales [rows]. */
+static uint8_t e4m3_encode(double v) {
+  uint8_t sign = 0;
+  if (v < 0) { sign = 0x80; v = -v; }
+  if (v == 0.0) return sign;
+  if (v < 0.015625) {                       /* below 2^-6: subnormal steps of 2^-9 */
+    const double m = nearbyint(v * 512.0);  /* m == 8 is the smallest normal, code 0x08 */
+    return (uint8_t)(sign | (uint8_t)m);
+  }
+  int e;
+  const double f = frexp(v, &e);            /* v = f 2^e, f in [0.5, 1) */
+  int E = e - 1;                            /* v = (1 + mant) 2^E */
+  double m = nearbyint((2.0 * f - 1.0) * 8.0);
+  if (m == 8.0) { m = 0.0; E += 1; }
+  return (uint8_t)(sign | (uint8_t)((E + 7) << 3) | (uint8_t)m);
+}
+
+double oracle_e4m3_value(uint8_t code) {
+  const double s = (code & 0x80) ? -1.0 : 1.0;
+  const int ef = (code >> 3) & 15, m = code & 7;
+  if (ef == 15 && m == 7) return NAN;
+  if (ef == 0) return s * m * (1.0 / 512.0);
+  return s * ldexp(1.0 + m / 8.0, ef - 7);
+}
+
+void oracle_quantize_fp8(const float* x, int64_t rows, int cols, uint8_t* codes, float* scales) {
+  for (int64_t i = 0; i < rows; ++i) {
+    float amax = 0.f;
+    for (int c = 0; c < cols; ++c) {
+      const float a = fabsf(x[i * cols + c]);
+      if (a > amax) amax = a;
+    }
+    int e = 0;
+    if (amax > 0.f) {
+      const float ratio = amax / 448.0f;    /* float32, as the decision is specified */
+      int fe;
+      const float fm = frexpf(ratio, &fe);  /* ratio = fm 2^fe, fm in [0.5, 1) */
+      e = (fm == 0.5f) ? fe - 1 : fe;       /* smallest e with ratio <= 2^e */
+    }
+    scales[i] = ldexpf(1.0f, e);
+    const double inv = ldexp(1.0, -e);
+    for (int c = 0; c < cols; ++c) codes[i * cols + c] = e4m3_encode((double)x[i * cols + c] * inv);
+  }
+}

@@ -70,6 +70,9 @@ def _load():
                                           i32, f64, P, i32, P, P, P]
         lib.oracle_indexer_kl_bwd.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
                                               f64, f64, P, i32, P, P, P, P]
+        lib.oracle_quantize_fp8.argtypes = [P, i64, i32, P, P]
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_value.restype = f64
         _lib = lib
         return lib
 
@@ -304,3 +307,25 @@ def indexer_kl_bwd(q, k_cmp, qI, w, kI, cu_seqlens, ratio: int, scale: float, id
                                   _ptr(cu), _ptr(cu_cmp), cu.shape[0] - 1, H, d, H_I, dI, int(ratio), float(scale),
                                   float(grad_scale), _ptr(rows), nq, _ptr(dqI), _ptr(dw), _ptr(dkI), _ptr(err))
     return {"dqI": dqI, "dw": dw, "dkI": dkI, "err": err}
+
+
+def quantize_fp8(x):
+    """Per-row E4M3 codes (uint8 [rows, cols]) and power-of-two scales (float32 [rows])
+    of a float32 array viewed as [rows, cols] (cols = its last dimension)."""
+    x = _f32(x)
+    cols = x.shape[-1]
+    flat = x.reshape(-1, cols)
+    codes = np.zeros(flat.shape, np.uint8)
+    scales = np.zeros(flat.shape[0], np.float32)
+    _load().oracle_quantize_fp8(_ptr(flat), flat.shape[0], cols, _ptr(codes), _ptr(scales))
+    return codes.reshape(x.shape), scales.reshape(x.shape[:-1])
+
+
+def e4m3_value(code: int) -> float:
+    return float(_load().oracle_e4m3_value(int(code)))
+
+
+def dequantize_fp8(codes, scales) -> np.ndarray:
+    """codes * scale as float32 (exact: the scale is a power of two)."""
+    table = np.array([e4m3_value(c) for c in range(256)], np.float64)
+    return (table[np.asarray(codes)] * np.asarray(scales, np.float64)[..., None]).astype(np.float32)
