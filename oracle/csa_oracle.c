@@ -688,7 +688,7 @@ void oracle_indexer_kl_bwd(const float* q, const float* kc, const float* qI,
  * decision takes max|x| / 448 in float32.  codes [rows, cols], scales [rows]. */
 static uint8_t e4m3_encode(double v) {
   uint8_t sign = 0;
-  if (v < 0) { sign = 0x80; v = -v; }
+  if (signbit(v)) { sign = 0x80; v = -v; }   /* E4M3 has signed zeros: -0 -> 0x80 */
   if (v == 0.0) return sign;
   if (v < 0.015625) {                       /* below 2^-6: subnormal steps of 2^-9 */
     const double m = nearbyint(v * 512.0);  /* m == 8 is the smallest normal, code 0x08 */

@@ -42,6 +42,13 @@ def test_ties_round_to_even_and_subnormals():
     assert np.all(codes[0, 1:] % 2 == 0)
 
 
+def test_signed_zeros_keep_their_sign():
+    x = np.array([[-0.0, 0.0, -1e-30, 1e-30, 1.0]], np.float32)
+    codes, scales = oracle.quantize_fp8(x)
+    np.testing.assert_array_equal(codes, _torch_codes(x, scales))
+    assert codes[0, 0] == 0x80 and codes[0, 1] == 0x00
+
+
 def test_scale_is_the_smallest_power_of_two_that_fits():
     x = (rng.standard_normal((500, 32)) * np.exp(3 * rng.standard_normal((500, 1)))).astype(np.float32)
     _, scales = oracle.quantize_fp8(x)
