@@ -58,6 +58,8 @@ def _load():
         "hca_attn_bwd": [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P, P, P, P, P, P, P, P],
         "window_attn_bwd": [P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P, P, P, P, P, P, P],
         "csa_indexer_kl_bwd": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, F, I, P, P, P, P],
+        "csa_quantize_fp8": [P, P, ctypes.c_int64, I, I, P, P, P],
+        "csa_indexer_topk_fp8": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P],
         "csa_indexer_kl": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, P, Z, P],
         "csa_indexer_kl_static_scratch": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, P],
     }
@@ -265,3 +267,19 @@ def csa_indexer_kl_bwd(h: Handle, q, kv_cmp, qI, w, kI, cu_seqlens, cu_cmp, max_
         h.ptr, _p(q), _p(kv_cmp), _p(qI), _p(w), _p(kI), _p(idx), k_pad, _p(lse_cmp), _p(cu_seqlens), _p(cu_cmp),
         cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H, d, H_I, d_I, int(ratio), float(softmax_scale),
         float(grad_scale), _dtype(q), _p(dqI), _p(dw), _p(dkI), _stream(stream)))
+
+
+def csa_quantize_fp8(h: Handle, x, codes, scales, stream=None):
+    """E4M3 codes (uint8, x's shape) and per-row scales (float32, x.shape[:-1]) of x."""
+    cols = x.shape[-1]
+    return _check("csa_quantize_fp8", LIB.csa_quantize_fp8(
+        h.ptr, _p(x), x.numel() // cols, cols, _dtype(x), _p(codes), _p(scales), _stream(stream)))
+
+
+def csa_indexer_topk_fp8(h: Handle, qI, qI_scale, w, kI, kI_scale, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int,
+                         topk: int, idx, stream=None):
+    T_cap, H_I, d_I = qI.shape
+    return _check("csa_indexer_topk_fp8", LIB.csa_indexer_topk_fp8(
+        h.ptr, _p(qI), _p(qI_scale), _p(w), _p(kI), _p(kI_scale), _p(cu_seqlens), _p(cu_cmp),
+        cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H_I, d_I, int(ratio), int(topk), idx.shape[1],
+        _dtype(w), _p(idx), _stream(stream)))

@@ -336,6 +336,33 @@ csa_status_t csa_indexer_kl_bwd(csa_handle_t h, const void* q, const void* kv_cm
   return from_cuda(csa::launch_indexer_kl_bwd(a, dtype == CSA_FP32, stream));
 }
 
+csa_status_t csa_quantize_fp8(csa_handle_t h, const void* x, int64_t rows, int cols, csa_dtype_t dtype,
+                              uint8_t* codes, float* scales, cudaStream_t stream) {
+  if (!h || !x || !codes || !scales || rows < 0) return CSA_ERR_INVALID_ARG;
+  if (dtype != CSA_BF16 && dtype != CSA_FP32) return CSA_ERR_INVALID_ARG;
+  if (cols < 1 || cols > 256) return CSA_ERR_UNSUPPORTED;
+  DeviceGuard g(h->device);
+  if (!g.ok) return CSA_ERR_CUDA;
+  return from_cuda(csa::launch_quantize_fp8(x, rows, cols, dtype == CSA_FP32, codes, scales, stream));
+}
+
+csa_status_t csa_indexer_topk_fp8(csa_handle_t h, const uint8_t* qI, const float* qI_scale, const void* w,
+                                  const uint8_t* kI, const float* kI_scale, const int32_t* cu, const int32_t* cu_cmp,
+                                  int B, int T_cap, int max_seqlen, int H_I, int d_I, int ratio, int topk, int k_pad,
+                                  csa_dtype_t dtype, int32_t* idx, cudaStream_t stream) {
+  if (!h || !qI || !qI_scale || !w || !kI || !kI_scale || !cu_cmp || !idx || !packing_ok(cu, B, T_cap, max_seqlen))
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(qI) || !aligned16(kI) || !aligned16(idx)) return CSA_ERR_INVALID_ARG;
+  if (ratio < 1 || topk < 1 || k_pad < topk) return CSA_ERR_INVALID_ARG;
+  if (dtype != CSA_BF16 || H_I != 8 || d_I != 64 || k_pad > 8192) return CSA_ERR_UNSUPPORTED;
+  const int max_vis = max_seqlen / ratio;
+  if (!csa::indexer_topk_tc_supported(H_I, d_I, max_vis, false)) return CSA_ERR_UNSUPPORTED;
+  DeviceGuard g(h->device);
+  if (!g.ok) return CSA_ERR_CUDA;
+  return from_cuda(csa::launch_indexer_topk_fp8_full(qI, qI_scale, w, kI, kI_scale, cu, cu_cmp, B, T_cap, max_vis,
+                                                     ratio, topk, k_pad, idx, h->status, stream));
+}
+
 }  // extern "C"
 
 namespace csa {

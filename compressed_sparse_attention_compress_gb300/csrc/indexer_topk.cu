@@ -339,6 +339,17 @@ static cudaError_t launch_topk_t(const void* qI, const void* w, const void* kI, 
   return cudaGetLastError();
 }
 
+cudaError_t launch_indexer_topk_fp8_full(const uint8_t* qI, const float* qs, const void* w, const uint8_t* kI,
+                                         const float* ks, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap,
+                                         int max_vis, int r, int topk, int k_pad, int32_t* idx, int* status,
+                                         cudaStream_t stream) {
+  cudaError_t err = launch_indexer_topk_fp8(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx,
+                                            status, stream);
+  if (err != cudaSuccess || T_cap <= 0) return err;
+  topk_fill_capacity_kernel<<<152, 256, 0, stream>>>(cu, B, T_cap, k_pad, idx);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_indexer_topk(const void* qI, const void* w, const void* kI, const int32_t* cu,
                                 const int32_t* cu_cmp, int B, int T_cap, int max_vis, int H_I, int d_I, int r,
                                 int topk, int k_pad, bool fp32, int32_t* idx, int* status, cudaStream_t stream) {

@@ -115,12 +115,18 @@ __device__ __forceinline__ bool qblock_of(const int32_t* __restrict__ cu, const 
 
 }  // namespace
 
-template <int G, int CW>
+// kFp8: qI and kI are E4M3 codes with per-row power-of-two scales (qs per
+// query head, ks per compressed row); the scores are then
+// ks[j] * sum_h (w_h qs_h) ReLU(codes dot), the same as the dequantised
+// operands give since the scales are positive.
+template <int G, int CW, bool kFp8>
 __global__ void __launch_bounds__(TopkCfg<CW>::kThreads, TopkCfg<CW>::kCtasPerSm)
 indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_constant__ CUtensorMap map_ki,
-                       const __nv_bfloat16* __restrict__ w, const int32_t* __restrict__ cu,
+                       const __nv_bfloat16* __restrict__ w, const float* __restrict__ qs,
+                       const float* __restrict__ ks, const int32_t* __restrict__ cu,
                        const int32_t* __restrict__ cu_cmp, int B, int r, int topk, int k_pad, int max_vis,
                        int32_t* __restrict__ idx, int* status) {
+  constexpr uint32_t kRowBytes = kFp8 ? kDI : 2 * kDI;  // bytes of one operand row
   constexpr int kN = G * kHI;  // MMA N: query-head rows
   constexpr int kComputeWarps = CW;
   constexpr int kComputeThreads = 32 * CW;
@@ -182,12 +188,12 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
         if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk) || bk.ntiles == 0) continue;
         if (!mbar_wait_bounded(bar_qempty, (nblk & 1u) ^ 1u, status)) { s_abort = 1; break; }
         ++nblk;
-        mbar_arrive_expect_tx(bar_qfull, kN * 128);
+        mbar_arrive_expect_tx(bar_qfull, kN * kRowBytes);
         tma_load_2d(base + kQIOff, &map_qi, 0, (bk.seq0 + bk.q0) * kHI, bar_qfull);
         for (int i = 0; i < bk.ntiles; ++i, ++it) {
           const uint32_t s = it % kStages;
           if (!mbar_wait_bounded(bar_empty + 8 * s, ((it / kStages) & 1u) ^ 1u, status)) { s_abort = 1; break; }
-          mbar_arrive_expect_tx(bar_full + 8 * s, kTileBytes);
+          mbar_arrive_expect_tx(bar_full + 8 * s, kTK * kRowBytes);
           tma_load_2d(base + kStageOff + s * kTileBytes, &map_ki, 0, bk.cmp0 + i * kTK, bar_full + 8 * s);
         }
       }
@@ -195,7 +201,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   } else if (warp == kComputeWarps + 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t kId = tc::idesc_bf16(kTK, kN, 0, 0);
+      constexpr uint32_t kId = kFp8 ? tc::idesc_e4m3(kTK, kN) : tc::idesc_bf16(kTK, kN, 0, 0);
       uint32_t it = 0, nblk = 0;
       for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
         QBlock bk;
@@ -211,11 +217,20 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
           }
           tc::fence_after_sync();
           const uint32_t st = base + kStageOff + s * kTileBytes;
+          if constexpr (kFp8) {
 #pragma unroll
-          for (int ks = 0; ks < kDI / 16; ++ks) {
-            const uint64_t a = tc::smem_desc_sw128(st + ks * 32, 16, 1024);
-            const uint64_t bq = tc::smem_desc_sw128(base + kQIOff + ks * 32, 16, 1024);
-            tc::mma_bf16(tmem + d * 32, a, bq, kId, ks > 0 ? 1u : 0u);
+            for (int kq = 0; kq < kDI / 32; ++kq) {   // 32 one-byte elements (32 bytes) per K step
+              const uint64_t a = tc::smem_desc_sw64(st + kq * 32, 512);
+              const uint64_t bq = tc::smem_desc_sw64(base + kQIOff + kq * 32, 512);
+              tc::mma_e4m3(tmem + d * 32, a, bq, kId, kq > 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int kq = 0; kq < kDI / 16; ++kq) {   // 16 bf16 elements (32 bytes) per K step
+              const uint64_t a = tc::smem_desc_sw128(st + kq * 32, 16, 1024);
+              const uint64_t bq = tc::smem_desc_sw128(base + kQIOff + kq * 32, 16, 1024);
+              tc::mma_bf16(tmem + d * 32, a, bq, kId, kq > 0 ? 1u : 0u);
+            }
           }
           tc::mma_commit(bar_dfull + 8 * d);
           tc::mma_commit(bar_empty + 8 * s);
@@ -237,7 +252,10 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
       if (bk.score) {
         if (tid < G * kHI) {
           const int q = tid / kHI, h = tid % kHI;
-          s_w[q][h] = q < bk.nq ? __bfloat162float(w[(int64_t)(bk.seq0 + bk.q0 + q) * kHI + h]) : 0.f;
+          const int64_t wr = (int64_t)(bk.seq0 + bk.q0 + q) * kHI + h;
+          float wv = q < bk.nq ? __bfloat162float(w[wr]) : 0.f;
+          if constexpr (kFp8) wv = q < bk.nq ? wv * __ldg(qs + wr) : 0.f;
+          s_w[q][h] = wv;
         }
         named_sync(1, kComputeThreads);
         const bool active = g * kQPW < G;  // this warpgroup's queries exist in the tile
@@ -254,6 +272,8 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_dfree + 8 * d);
           const int j = i * kTK + rowl;
+          float kscale = 1.f;
+          if constexpr (kFp8) kscale = (active && j < bk.nvis_max) ? __ldg(ks + bk.cmp0 + j) : 0.f;
           if (active && j < bk.nvis_max) {
 #pragma unroll
             for (int qq = 0; qq < kQPW; ++qq) {
@@ -261,6 +281,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
               float sc = 0.f;
 #pragma unroll
               for (int h = 0; h < kHI; ++h) sc = fmaf(s_w[q][h], fmaxf(__uint_as_float(rv[qq * kHI + h]), 0.f), sc);
+              if constexpr (kFp8) sc *= kscale;
               sKey[(size_t)q * vstride + j] = order_key(sc);
             }
           }
@@ -466,17 +487,22 @@ bool indexer_topk_tc_supported(int H_I, int d_I, int max_vis, bool fp32) {
   return !fp32 && H_I == kHI && d_I == kDI && topk_tc_shape(max_vis).G > 0;
 }
 
-template <int G, int CW>
-static cudaError_t launch_topk_tc_t(const void* qI, const void* w, const void* kI, const int32_t* cu,
-                                    const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r, int topk, int k_pad,
-                                    int32_t* idx, int* status, cudaStream_t stream) {
+template <int G, int CW, bool kFp8>
+static cudaError_t launch_topk_tc_t(const void* qI, const float* qs, const void* w, const void* kI, const float* ks,
+                                    const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r,
+                                    int topk, int k_pad, int32_t* idx, int* status, cudaStream_t stream) {
   CUtensorMap mqi, mki;
   const uint64_t n_cmp_rows = (uint64_t)(T_cap / r > 0 ? T_cap / r : 1);
-  if (!make_tmap_bf16_sw128(&mqi, qI, (uint64_t)T_cap * kHI, kDI, G * kHI) ||
-      !make_tmap_bf16_sw128(&mki, kI, n_cmp_rows, kDI, kTK))
+  if (kFp8) {
+    if (!make_tmap_u8_sw64(&mqi, qI, (uint64_t)T_cap * kHI, kDI, G * kHI) ||
+        !make_tmap_u8_sw64(&mki, kI, n_cmp_rows, kDI, kTK))
+      return cudaErrorInvalidValue;
+  } else if (!make_tmap_bf16_sw128(&mqi, qI, (uint64_t)T_cap * kHI, kDI, G * kHI) ||
+             !make_tmap_bf16_sw128(&mki, kI, n_cmp_rows, kDI, kTK)) {
     return cudaErrorInvalidValue;
+  }
   const size_t smem = 1024 + TopkCfg<CW>::kKeysOff + (size_t)G * ((max_vis + 3) & ~3) * 4;
-  auto kern = indexer_topk_tc_kernel<G, CW>;
+  auto kern = indexer_topk_tc_kernel<G, CW, kFp8>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   int dev = 0, sms = 0;
@@ -485,23 +511,43 @@ static cudaError_t launch_topk_tc_t(const void* qI, const void* w, const void* k
   const int blocks = T_cap / G + B + 1;
   const int slots = sms * TopkCfg<CW>::kCtasPerSm;
   const int grid = blocks < slots ? blocks : slots;
-  kern<<<grid, TopkCfg<CW>::kThreads, smem, stream>>>(mqi, mki, static_cast<const __nv_bfloat16*>(w), cu, cu_cmp, B,
-                                                      r, topk, k_pad, max_vis, idx, status);
+  kern<<<grid, TopkCfg<CW>::kThreads, smem, stream>>>(mqi, mki, static_cast<const __nv_bfloat16*>(w), qs, ks, cu,
+                                                      cu_cmp, B, r, topk, k_pad, max_vis, idx, status);
   return cudaGetLastError();
+}
+
+template <bool kFp8>
+static cudaError_t launch_topk_tc_any(const void* qI, const float* qs, const void* w, const void* kI, const float* ks,
+                                      const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r,
+                                      int topk, int k_pad, int32_t* idx, int* status, cudaStream_t stream) {
+  if (T_cap <= 0) return cudaSuccess;
+  const TopkShape sh = topk_tc_shape(max_vis);
+  if (sh.G == 4 && sh.CW == 8)
+    return launch_topk_tc_t<4, 8, kFp8>(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status,
+                                        stream);
+  if (sh.G == 2 && sh.CW == 8)
+    return launch_topk_tc_t<2, 8, kFp8>(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status,
+                                        stream);
+  if (sh.G == 4)
+    return launch_topk_tc_t<4, 16, kFp8>(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx,
+                                         status, stream);
+  return launch_topk_tc_t<2, 16, kFp8>(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status,
+                                       stream);
 }
 
 cudaError_t launch_indexer_topk_tc(const void* qI, const void* w, const void* kI, const int32_t* cu,
                                    const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r, int topk, int k_pad,
                                    int32_t* idx, int* status, cudaStream_t stream) {
-  if (T_cap <= 0) return cudaSuccess;
-  const TopkShape sh = topk_tc_shape(max_vis);
-  if (sh.G == 4 && sh.CW == 8)
-    return launch_topk_tc_t<4, 8>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
-  if (sh.G == 2 && sh.CW == 8)
-    return launch_topk_tc_t<2, 8>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
-  if (sh.G == 4)
-    return launch_topk_tc_t<4, 16>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
-  return launch_topk_tc_t<2, 16>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status, stream);
+  return launch_topk_tc_any<false>(qI, nullptr, w, kI, nullptr, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx,
+                                   status, stream);
+}
+
+cudaError_t launch_indexer_topk_fp8(const uint8_t* qI, const float* qs, const void* w, const uint8_t* kI,
+                                    const float* ks, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap,
+                                    int max_vis, int r, int topk, int k_pad, int32_t* idx, int* status,
+                                    cudaStream_t stream) {
+  return launch_topk_tc_any<true>(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status,
+                                  stream);
 }
 
 }  // namespace csa

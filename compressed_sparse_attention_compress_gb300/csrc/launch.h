@@ -29,6 +29,19 @@ cudaError_t launch_indexer_topk_tc(const void* qI, const void* w, const void* kI
                                    const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r, int topk, int k_pad,
                                    int32_t* idx, int* status, cudaStream_t stream);
 
+// FP8 indexer: E4M3 quantisation and the tcgen05 scoring + top-k on codes.
+cudaError_t launch_quantize_fp8(const void* x, int64_t rows, int cols, bool fp32, uint8_t* codes, float* scales,
+                                cudaStream_t stream);
+cudaError_t launch_indexer_topk_fp8(const uint8_t* qI, const float* qs, const void* w, const uint8_t* kI,
+                                    const float* ks, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap,
+                                    int max_vis, int r, int topk, int k_pad, int32_t* idx, int* status,
+                                    cudaStream_t stream);
+
+cudaError_t launch_indexer_topk_fp8_full(const uint8_t* qI, const float* qs, const void* w, const uint8_t* kI,
+                                         const float* ks, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap,
+                                         int max_vis, int r, int topk, int k_pad, int32_t* idx, int* status,
+                                         cudaStream_t stream);
+
 // Attention kinds.
 enum AttnKind { kAttnCSA = 0, kAttnHCA = 1, kAttnWindow = 2 };
 

@@ -14,6 +14,10 @@ namespace csa {
 // `rows` read as zeros.  Returns false if the driver refuses the encoding.
 bool make_tmap_bf16_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
+// The same over a row-major 8-bit array [rows, cols] (E4M3 codes): boxes of
+// box_rows x 64 bytes, 64-byte swizzle.
+bool make_tmap_u8_sw64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(

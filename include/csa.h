@@ -166,6 +166,31 @@ csa_status_t csa_indexer_topk(csa_handle_t handle, const void* qI, const void* w
                               int H_I, int d_I, int ratio, int topk, int k_pad,
                               csa_dtype_t dtype, int32_t* idx, cudaStream_t stream);
 
+/* FP8 indexer (§1 and §9: FP8 q^I / k^I for the index-search term; the pages
+ * fix no format).  csa_quantize_fp8 turns x [rows, cols] (dtype, cols <= 256)
+ * into E4M3 codes [rows, cols] (uint8) with one power-of-two scale per row
+ * (float32 [rows]): s = 2^e the smallest with max|x| / s <= 448 (decided on
+ * max|x| / 448 in float32; s = 1 for a zero row) and code = E4M3(x / s)
+ * rounded to nearest even.  Quantise qI as [T_cap * H_I, d_I] rows and the
+ * compressed indexer keys kI as [rows, d_I]. */
+csa_status_t csa_quantize_fp8(csa_handle_t handle, const void* x, int64_t rows, int cols,
+                              csa_dtype_t dtype, uint8_t* codes, float* scales,
+                              cudaStream_t stream);
+
+/* csa_indexer_topk on FP8 operands: qI codes [T_cap, H_I, d_I] with scales
+ * qI_scale [T_cap, H_I], kI codes [., d_I] with scales kI_scale [.] (from
+ * csa_quantize_fp8), w [T_cap, H_I] (bf16).  The indexer logit is that of the
+ * dequantised operands,
+ *   i_{t,j} = sum_h w[t,h] ReLU(qI_scale[t,h] kI_scale[j] sum_c qI[t,h,c] kI[j,c]),
+ * the dot of codes on the tensor cores (E4M3 x E4M3, fp32 accumulation);
+ * selection, ties, output and padding as csa_indexer_topk.  H_I = 8,
+ * d_I = 64, dtype CSA_BF16 (for w) only; CSA_ERR_UNSUPPORTED otherwise. */
+csa_status_t csa_indexer_topk_fp8(csa_handle_t handle, const uint8_t* qI, const float* qI_scale,
+                                  const void* w, const uint8_t* kI, const float* kI_scale,
+                                  const int32_t* cu_seqlens, const int32_t* cu_cmp, int B,
+                                  int T_cap, int max_seqlen, int H_I, int d_I, int ratio, int topk,
+                                  int k_pad, csa_dtype_t dtype, int32_t* idx, cudaStream_t stream);
+
 /* Selected-entry attention forward, CSA (§2 phase table "top-k compressed
  * entries + local window", §8.2 selected MQA attention returning output and
  * LSE, compressed ids combined with window ids, §9 FP32 attention sink).
