@@ -8,7 +8,7 @@ dense teacher over every visible entry), the shape of the DeepSeek-V4 CSA
 layers in "DeepSeek-V4 Attention Training Systems" (§2 phase table).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-                    [--compressor plain|v4] [--backward]
+                    [--compressor plain|v4] [--indexer bf16|fp8] [--backward]
 
 Prints one JSON line (rank 0).  Multi-GPU: one process per GPU under
 torch.distributed.run; each rank runs its own copy of the workload (the path
@@ -327,7 +327,7 @@ def run_ours(args, wl):
         "data": "synthetic",
         "config": {"workload": wl.name, "global_batch": wl.B * ws, "seq_len": max(wl.lengths),
                    "tokens_per_gpu": wl.T, "ratio": wl.ratio, "heads": wl.H, "head_dim": wl.d, "topk": wl.topk,
-                   "window": wl.window, "kl": wl.kl_mode, "compressor": wl.compressor,
+                   "window": wl.window, "kl": wl.kl_mode, "compressor": wl.compressor, "indexer": wl.indexer,
                    "backward": bool(args.backward),
                    "parallelism": f"replicas{ws}",
                    "l2": "inputs larger than L2 (q alone is %.0f MB)" % (wl.T_cap * wl.H * wl.d * 2 / 1e6)},
@@ -366,6 +366,8 @@ def f_launches(wl) -> int:
         n += 1 + 1 + (1 if wl.separate_v else 0) + (1 if wl.H_I > 0 else 0)   # offsets + compress calls
         if wl.H_I > 0:
             n += 2                                                              # top-k + capacity fill
+            if wl.indexer == "fp8":
+                n += 2                                                          # quantise qI and kI
     ws_attn = not wl.io_fp32 and wl.H == 64 and wl.d == 128 and not wl.separate_v
     n += 2 if ws_attn else 1                                                    # (capacity rows) + attention
     if wl.kl_mode != "none":
@@ -397,12 +399,16 @@ def main():
     ap.add_argument("--backward", action="store_true",
                     help="add the attention backward (dq, dKV from the saved output and LSE) and, with an "
                          "indexer loss, the indexer backward to every step")
+    ap.add_argument("--indexer", default="bf16", choices=["bf16", "fp8"],
+                    help="fp8: E4M3 indexer operands (quantised in the step) for the scoring + top-k")
     ap.add_argument("--compressor", default="plain", choices=["plain", "v4"],
                     help="v4: previous-half stream + RMSNorm + RoPE fused into both compressors")
     args = ap.parse_args()
     wl = I.WORKLOADS[args.workload]
     if args.compressor != "plain":
         wl = dataclasses.replace(wl, compressor=args.compressor)
+    if args.indexer != "bf16":
+        wl = dataclasses.replace(wl, indexer=args.indexer)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -76,6 +76,17 @@ class Forward:
 
     def topk(self, stream=None):
         wl, x = self.wl, self.x
+        if wl.indexer == "fp8":
+            if getattr(self, "qI8", None) is None:
+                self.qI8 = torch.empty(x["qI"].shape, dtype=torch.uint8, device=self.dev)
+                self.qIs = torch.empty(x["qI"].shape[:-1], dtype=torch.float32, device=self.dev)
+                self.kI8 = torch.empty(self.kI.shape, dtype=torch.uint8, device=self.dev)
+                self.kIs = torch.empty(self.kI.shape[:-1], dtype=torch.float32, device=self.dev)
+            api.csa_quantize_fp8(self.h, x["qI"], self.qI8, self.qIs, stream)
+            api.csa_quantize_fp8(self.h, self.kI, self.kI8, self.kIs, stream)
+            api.csa_indexer_topk_fp8(self.h, self.qI8, self.qIs, x["w"], self.kI8, self.kIs, self.cu, self.cu_cmp,
+                                     self.max_seqlen, wl.ratio, wl.topk, self.idx, stream)
+            return
         api.csa_indexer_topk(self.h, x["qI"], x["w"], self.kI, self.cu, self.cu_cmp, self.max_seqlen, wl.ratio,
                              wl.topk, self.idx, stream)
 

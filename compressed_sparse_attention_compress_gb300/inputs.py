@@ -70,6 +70,7 @@ class Workload:
     kl_mode: str = "none"    # "sparse" (selected set), "dense" (all visible) or "none"
     cap_align: int = 1       # T_cap = total rounded up to this
     compressor: str = "plain"  # "plain" gate only; "v4": previous-half stream + RMSNorm + RoPE
+    indexer: str = "bf16"      # "bf16" or "fp8" (E4M3 operands with per-row scales) for scoring + top-k
     notes: str = ""
     extra: dict = field(default_factory=dict)
 
