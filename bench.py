@@ -270,7 +270,7 @@ def run_ours(args, wl):
                 f.indexer_backward(stream=stream)
         res_host.copy_(res, non_blocking=True)
 
-    for _ in range(2):
+    for _ in range(max(3, args.warmup)):   # the first steps after pinning pay a one-time mapping cost
         e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
