@@ -360,7 +360,9 @@ static cudaError_t launch_bwd_all(AttnKind kind, const AttnBwdArgs& a, cudaStrea
   attn_bwd_delta_kernel<TIn><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(
       static_cast<const TIn*>(a.out), static_cast<const TIn*>(a.dout), a.cu, a.B, a.T_cap, a.H, a.d, a.delta);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  if (a.d == 64) err = bwd_dispatch_heads<TIn, TIn, 64>(kind, a, stream);
+  // 64 heads x 128 dims in bf16 with K = V run on tcgen05; other shapes on the warp-level kernel
+  if (attention_bwd_tc_supported(a, sizeof(TIn) == 4)) err = launch_attention_bwd_tc(kind, a, stream);
+  else if (a.d == 64) err = bwd_dispatch_heads<TIn, TIn, 64>(kind, a, stream);
   else err = bwd_dispatch_heads<TIn, TIn, 128>(kind, a, stream);
   if (err != cudaSuccess) return err;
   if (a.sink && a.dsink) {

@@ -99,6 +99,8 @@ struct AttnBwdArgs {
   int* status;
 };
 cudaError_t launch_attention_bwd(AttnKind kind, const AttnBwdArgs& a, bool fp32, cudaStream_t stream);
+bool attention_bwd_tc_supported(const AttnBwdArgs& a, bool fp32);
+cudaError_t launch_attention_bwd_tc(AttnKind kind, const AttnBwdArgs& a, cudaStream_t stream);
 
 struct KLArgs {
   const void* q;
