@@ -51,6 +51,7 @@ constexpr int kMmaWarp = kProdWarp + 1;                // warp 13
 constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr int kSoftThreads = 32 * kSoftWarps;
 constexpr int kRowsPerLane = kTK / 32;                 // producer rows per lane
+constexpr int kStages = 4;                             // key-tile ring
 
 constexpr uint32_t kQRegion = kNH * 128;               // 8 KB: 64 rows x 64 dims
 constexpr uint32_t kQBytes = 2 * kQRegion;             // 16 KB
@@ -58,10 +59,10 @@ constexpr uint32_t kTileRegion = kTK * 128;            // 16 KB
 constexpr uint32_t kTileBytes = 2 * kTileRegion;       // 32 KB
 constexpr uint32_t kQOff = 0;
 constexpr uint32_t kGOff = kQBytes;                    // dO
-constexpr uint32_t kStageOff = 2 * kQBytes;            // 2 stages
-constexpr uint32_t kPOff = kStageOff + 2 * kTileBytes; // P^T [key][head]
+constexpr uint32_t kStageOff = 2 * kQBytes;            // kStages stages
+constexpr uint32_t kPOff = kStageOff + kStages * kTileBytes;  // P^T [key][head]
 constexpr uint32_t kDSOff = kPOff + kTK * 128;         // scale dS^T [key][head]
-constexpr uint32_t kSmem = kDSOff + kTK * 128;         // 128 KB
+constexpr uint32_t kSmem = kDSOff + kTK * 128;         // 192 KB
 
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColKV = 256;
 
@@ -89,10 +90,10 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
                         int* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t s_full[2], s_empty[2], s_kvfull[2], s_kvfree[2];
+  __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_kvfull[2], s_kvfree[2];
   __shared__ __align__(8) uint64_t s_qfull, s_qempty, s_sfull, s_sfree, s_pfull, s_pfree, s_dqdone, s_dqfree;
-  __shared__ Meta s_meta[2];
-  __shared__ int s_rows[2][kTK];
+  __shared__ Meta s_meta[kStages];
+  __shared__ int s_rows[kStages][kTK];
   __shared__ float s_lse2[kNH], s_D[kNH];
   __shared__ int s_abort;
 
@@ -106,9 +107,11 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 64);        // 32 cp.async arrivals + the warp's release
       mbar_init(bar_empty + 8 * s, 1 + kEpiWarps);  // MMA done with the tile + each epilogue warp done with its rows
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar_kvfull + 8 * s, 1);
       mbar_init(bar_kvfree + 8 * s, kEpiWarps);
     }
@@ -193,8 +196,8 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
         }
         prefetch(it + 1);
         if (it < nct && !__any_sync(0xffffffffu, any)) continue;  // empty compressed tile
-        const uint32_t st = n & 1u;
-        bool ok = mbar_wait_bounded(bar_empty + 8 * st, ((n >> 1) & 1u) ^ 1u, status);
+        const uint32_t st = n % kStages;
+        bool ok = mbar_wait_bounded(bar_empty + 8 * st, ((n / kStages) & 1u) ^ 1u, status);
         if (first && nq > 0) ok = ok && mbar_wait_bounded(smem_u32(&s_qempty), (nq - 1) & 1u, status);
         if (__any_sync(0xffffffffu, !ok || *abort_flag != 0)) {
           *abort_flag = 1;
@@ -240,8 +243,8 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
       }
     }
     if (alive) {  // end-of-stream marker
-      const uint32_t st = n & 1u;
-      const bool ok = mbar_wait_bounded(bar_empty + 8 * st, ((n >> 1) & 1u) ^ 1u, status);
+      const uint32_t st = n % kStages;
+      const bool ok = mbar_wait_bounded(bar_empty + 8 * st, ((n / kStages) & 1u) ^ 1u, status);
       if (__any_sync(0xffffffffu, !ok)) {
         *abort_flag = 1;
       } else {
@@ -277,10 +280,11 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
       while (!(end && kp == kq)) {
         bool progress = false;
         if (kp < kq && mbar_test(pfull, kp & 1u)) {
-          const uint32_t sp = kp & 1u;           // stage of tile kp; also its dKV buffer
+          const uint32_t sp = kp % kStages;      // stage of tile kp
+          const uint32_t bkv = kp & 1u;          // its dKV buffer
           const int flags = s_meta[sp].flags;
           const bool first = (flags & kFirst) != 0;
-          const bool kv_ok = kp < 2 || mbar_test(bar_kvfree + 8 * sp, ((kp >> 1) - 1) & 1u);
+          const bool kv_ok = kp < 2 || mbar_test(bar_kvfree + 8 * bkv, ((kp >> 1) - 1) & 1u);
           const bool dq_ok = !first || nqp == 0 || mbar_test(dqfree, (nqp - 1) & 1u);
           if (kv_ok && dq_ok) {
             if (first) ++nqp;
@@ -291,7 +295,7 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
               const uint32_t off = (ks * 2048) >> 4;
               tc::mma_bf16(tmem + kColDQ, dkt + off, dds_b + off, kIdDQ, (first && ks == 0) ? 0u : 1u);
             }
-            const uint32_t tkv = tmem + kColKV + sp * 128;
+            const uint32_t tkv = tmem + kColKV + bkv * 128;
 #pragma unroll
             for (int kh = 0; kh < kNH / 16; ++kh)    // dS^T Q over the heads, 16 at a time
               tc::mma_bf16(tkv, dds_a + ((kh * 32) >> 4), dq_mn + ((kh * 2048) >> 4), kIdKV, kh > 0 ? 1u : 0u);
@@ -299,7 +303,7 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
             for (int kh = 0; kh < kNH / 16; ++kh)    // + P^T dO
               tc::mma_bf16(tkv, dp_a + ((kh * 32) >> 4), dg_mn + ((kh * 2048) >> 4), kIdKV, 1u);
             tc::mma_commit(smem_u32(&s_pfree));
-            tc::mma_commit(bar_kvfull + 8 * sp);
+            tc::mma_commit(bar_kvfull + 8 * bkv);
             tc::mma_commit(bar_empty + 8 * sp);
             if (flags & kLast) {
               tc::mma_commit(smem_u32(&s_dqdone));
@@ -309,8 +313,8 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
             progress = true;
           }
         }
-        if (!end && kq < kp + 2 && mbar_test(bar_full + 8 * (kq & 1u), (kq >> 1) & 1u)) {
-          const uint32_t st = kq & 1u;
+        if (!end && kq < kp + 2 && mbar_test(bar_full + 8 * (kq % kStages), (kq / kStages) & 1u)) {
+          const uint32_t st = kq % kStages;
           const int flags = s_meta[st].flags;
           if (flags & kDone) {
             end = true;
@@ -347,7 +351,7 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
             break;
           }
           if (kp < kq) mbar_sleep(pfull, kp & 1u, 500);
-          else if (!end) mbar_sleep(bar_full + 8 * (kq & 1u), (kq >> 1) & 1u, 500);
+          else if (!end) mbar_sleep(bar_full + 8 * (kq % kStages), (kq / kStages) & 1u, 500);
           else __nanosleep(64);
         }
       }
@@ -366,8 +370,8 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
     uint32_t k = 0, nq = 0;
     int row = -1;
     for (uint32_t n = 0;; ++n) {
-      const uint32_t st = n & 1u;
-      const bool okf = mbar_wait_bounded(bar_full + 8 * st, (n >> 1) & 1u, status);
+      const uint32_t st = n % kStages;
+      const bool okf = mbar_wait_bounded(bar_full + 8 * st, (n / kStages) & 1u, status);
       if (bar_or(kBar, kSoftThreads, !okf || *abort_flag != 0)) {
         *abort_flag = 1;
         break;
@@ -450,8 +454,8 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
     const int key = ew * 32 + lane;
     const uint32_t lane_off = (uint32_t)(ew * 32) << 16;
     for (uint32_t n = 0;; ++n) {
-      const uint32_t st = n & 1u;
-      bool ok = mbar_wait_bounded(bar_full + 8 * st, (n >> 1) & 1u, status);
+      const uint32_t st = n % kStages, bkv = n & 1u;
+      bool ok = mbar_wait_bounded(bar_full + 8 * st, (n / kStages) & 1u, status);
       if (__any_sync(0xffffffffu, !ok || *abort_flag != 0)) {
         *abort_flag = 1;
         break;
@@ -461,7 +465,7 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
       const int rr = s_rows[st][key];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * st);  // the rows are read; the MMA frees the tile
-      ok = mbar_wait_bounded(bar_kvfull + 8 * st, (n >> 1) & 1u, status);
+      ok = mbar_wait_bounded(bar_kvfull + 8 * bkv, (n >> 1) & 1u, status);
       if (__any_sync(0xffffffffu, !ok)) {
         *abort_flag = 1;
         break;
@@ -471,7 +475,7 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
 #pragma unroll 1
       for (int c0 = 0; c0 < kDim; c0 += 32) {
         uint32_t v[32];
-        tc::tmem_ld32_sync(tmem + lane_off + kColKV + st * 128 + c0, v);
+        tc::tmem_ld32_sync(tmem + lane_off + kColKV + bkv * 128 + c0, v);
         if (rr >= 0) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -481,7 +485,7 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_kvfree + 8 * st);
+      if (lane == 0) mbar_arrive(bar_kvfree + 8 * bkv);
     }
   }
 
