@@ -213,6 +213,7 @@ def run_ours(args, wl):
     if wl.kl_mode != "none":
         stages.append(("indexer_kl", f.kl))
     dout = None
+    f.keep_stats = bool(args.backward)   # the KL forward hands its normalisers to the indexer backward
     if args.backward:
         # upstream gradient of the attention output: bf16 N(0,1), its own seeded stream
         g = np.random.default_rng(np.random.SeedSequence(args.seed).spawn(len(I.STREAMS) + 1)[-1])

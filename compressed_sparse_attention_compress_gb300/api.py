@@ -57,7 +57,8 @@ def _load():
                                 P, P, P],
         "hca_attn_bwd": [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P, P, P, P, P, P, P, P],
         "window_attn_bwd": [P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P, P, P, P, P, P, P],
-        "csa_indexer_kl_bwd": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, F, I, P, P, P, P],
+        "csa_indexer_kl_bwd": [P, P, P, P, P, P, P, I, P, P, P, P, I, I, I, I, I, I, I, I, F, F, I, P, P, P, P],
+        "csa_indexer_kl_ex": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, P, Z, P, P, P],
         "csa_quantize_fp8": [P, P, ctypes.c_int64, I, I, P, P, P],
         "csa_indexer_topk_fp8": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P],
         "csa_indexer_kl": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, P, Z, P],
@@ -243,6 +244,19 @@ def csa_indexer_kl(h: Handle, q, kv_cmp, qI, w, kI, cu_seqlens, cu_cmp, max_seql
         ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def csa_indexer_kl_ex(h: Handle, q, kv_cmp, qI, w, kI, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int,
+                      softmax_scale: float, kl_sum, ws, teacher_lse=None, student_lse=None, idx=None, lse_cmp=None,
+                      kl_per_query=None, n_valid=None, stream=None):
+    T_cap, H, d = q.shape
+    _, H_I, d_I = qI.shape
+    k_pad = idx.shape[1] if idx is not None else 0
+    return _check("csa_indexer_kl_ex", LIB.csa_indexer_kl_ex(
+        h.ptr, _p(q), _p(kv_cmp), _p(qI), _p(w), _p(kI), _p(idx), k_pad, _p(lse_cmp), _p(cu_seqlens),
+        _p(cu_cmp), cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H, d, H_I, d_I, int(ratio),
+        float(softmax_scale), _dtype(q), _p(kl_sum), _p(kl_per_query), _p(n_valid), _p(ws),
+        ws.numel() * ws.element_size(), _p(teacher_lse), _p(student_lse), _stream(stream)))
+
+
 def csa_indexer_kl_static_scratch(h: Handle, q, kv_cmp, qI, w, kI, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int,
                                   softmax_scale: float, kl_sum, idx=None, lse_cmp=None, kl_per_query=None,
                                   n_valid=None, stream=None):
@@ -259,14 +273,14 @@ def csa_indexer_kl_static_scratch(h: Handle, q, kv_cmp, qI, w, kI, cu_seqlens, c
 
 def csa_indexer_kl_bwd(h: Handle, q, kv_cmp, qI, w, kI, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int,
                        softmax_scale: float, dqI, dw, dkI, idx=None, lse_cmp=None, grad_scale: float = 1.0,
-                       stream=None):
+                       student_lse=None, stream=None):
     T_cap, H, d = q.shape
     _, H_I, d_I = qI.shape
     k_pad = idx.shape[1] if idx is not None else 0
     return _check("csa_indexer_kl_bwd", LIB.csa_indexer_kl_bwd(
-        h.ptr, _p(q), _p(kv_cmp), _p(qI), _p(w), _p(kI), _p(idx), k_pad, _p(lse_cmp), _p(cu_seqlens), _p(cu_cmp),
-        cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H, d, H_I, d_I, int(ratio), float(softmax_scale),
-        float(grad_scale), _dtype(q), _p(dqI), _p(dw), _p(dkI), _stream(stream)))
+        h.ptr, _p(q), _p(kv_cmp), _p(qI), _p(w), _p(kI), _p(idx), k_pad, _p(lse_cmp), _p(student_lse),
+        _p(cu_seqlens), _p(cu_cmp), cu_seqlens.numel() - 1, T_cap, int(max_seqlen), H, d, H_I, d_I, int(ratio),
+        float(softmax_scale), float(grad_scale), _dtype(q), _p(dqI), _p(dw), _p(dkI), _stream(stream)))
 
 
 def csa_quantize_fp8(h: Handle, x, codes, scales, stream=None):

@@ -291,11 +291,12 @@ size_t csa_indexer_kl_workspace(int T_cap) {
   return ((size_t)T_cap * 8 + 255) & ~(size_t)255;  // float kl[T_cap] + int32 csize[T_cap]
 }
 
-csa_status_t csa_indexer_kl(csa_handle_t h, const void* q, const void* kv_cmp, const void* qI, const void* w,
+static csa_status_t indexer_kl_common(csa_handle_t h, const void* q, const void* kv_cmp, const void* qI, const void* w,
                             const void* kI, const int32_t* idx, int k_pad, const float* lse_cmp, const int32_t* cu,
                             const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H, int d, int H_I,
                             int d_I, int ratio, float scale, csa_dtype_t dtype, float* kl_sum, float* kl_per_query,
-                            int32_t* n_valid, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                            int32_t* n_valid, void* ws, size_t ws_bytes, float* teacher_lse, float* student_lse,
+                                       cudaStream_t stream) {
   if (!h || !q || !kv_cmp || !qI || !w || !kI || !cu_cmp || !kl_sum || !packing_ok(cu, B, T_cap, max_seqlen))
     return CSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv_cmp) || !aligned16(qI) || !aligned16(kI)) return CSA_ERR_INVALID_ARG;
@@ -308,14 +309,36 @@ csa_status_t csa_indexer_kl(csa_handle_t h, const void* q, const void* kv_cmp, c
   if (!g.ok) return CSA_ERR_CUDA;
   float* kl_rows = kl_per_query ? kl_per_query : static_cast<float*>(ws);
   int32_t* csize = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + (size_t)T_cap * 4);
+  if (!opt_aligned16(teacher_lse) || !opt_aligned16(student_lse)) return CSA_ERR_INVALID_ARG;
   csa::KLArgs a{q, kv_cmp, qI, w, kI, idx, k_pad, lse_cmp, cu, cu_cmp, B, T_cap, H, d, H_I, d_I, ratio,
-                scale, kl_rows, csize, kl_sum, n_valid, h->status};
+                scale, kl_rows, csize, kl_sum, n_valid, h->status, teacher_lse, student_lse};
   return from_cuda(csa::launch_indexer_kl(a, dtype == CSA_FP32, stream));
+}
+
+csa_status_t csa_indexer_kl(csa_handle_t h, const void* q, const void* kv_cmp, const void* qI, const void* w,
+                            const void* kI, const int32_t* idx, int k_pad, const float* lse_cmp, const int32_t* cu,
+                            const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H, int d, int H_I,
+                            int d_I, int ratio, float scale, csa_dtype_t dtype, float* kl_sum, float* kl_per_query,
+                            int32_t* n_valid, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return indexer_kl_common(h, q, kv_cmp, qI, w, kI, idx, k_pad, lse_cmp, cu, cu_cmp, B, T_cap, max_seqlen, H, d, H_I,
+                           d_I, ratio, scale, dtype, kl_sum, kl_per_query, n_valid, ws, ws_bytes, nullptr, nullptr,
+                           stream);
+}
+
+csa_status_t csa_indexer_kl_ex(csa_handle_t h, const void* q, const void* kv_cmp, const void* qI, const void* w,
+                               const void* kI, const int32_t* idx, int k_pad, const float* lse_cmp, const int32_t* cu,
+                               const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H, int d, int H_I,
+                               int d_I, int ratio, float scale, csa_dtype_t dtype, float* kl_sum,
+                               float* kl_per_query, int32_t* n_valid, void* ws, size_t ws_bytes,
+                               float* teacher_lse, float* student_lse, cudaStream_t stream) {
+  return indexer_kl_common(h, q, kv_cmp, qI, w, kI, idx, k_pad, lse_cmp, cu, cu_cmp, B, T_cap, max_seqlen, H, d, H_I,
+                           d_I, ratio, scale, dtype, kl_sum, kl_per_query, n_valid, ws, ws_bytes, teacher_lse,
+                           student_lse, stream);
 }
 
 csa_status_t csa_indexer_kl_bwd(csa_handle_t h, const void* q, const void* kv_cmp, const void* qI, const void* w,
                                 const void* kI, const int32_t* idx, int k_pad, const float* lse_cmp,
-                                const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H,
+                                const float* student_lse, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H,
                                 int d, int H_I, int d_I, int ratio, float scale, float grad_scale,
                                 csa_dtype_t dtype, void* dqI, void* dw, float* dkI, cudaStream_t stream) {
   if (!h || !q || !kv_cmp || !qI || !w || !kI || !cu_cmp || !dqI || !dw || !dkI ||
@@ -331,7 +354,7 @@ csa_status_t csa_indexer_kl_bwd(csa_handle_t h, const void* q, const void* kv_cm
     return CSA_ERR_UNSUPPORTED;
   DeviceGuard g(h->device);
   if (!g.ok) return CSA_ERR_CUDA;
-  csa::KLBwdArgs a{q, kv_cmp, qI, w, kI, idx, k_pad, lse_cmp, cu, cu_cmp, B, T_cap, H, d, H_I, d_I, ratio,
+  csa::KLBwdArgs a{q, kv_cmp, qI, w, kI, idx, k_pad, lse_cmp, student_lse, cu, cu_cmp, B, T_cap, H, d, H_I, d_I, ratio,
                    T_cap / ratio, scale, grad_scale, dqI, dw, dkI, h->status};
   return from_cuda(csa::launch_indexer_kl_bwd(a, dtype == CSA_FP32, stream));
 }

@@ -30,7 +30,8 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
                   const TIn* __restrict__ w, const TIn* __restrict__ kI, const int32_t* __restrict__ idx,
                   int k_pad, const float* __restrict__ lse_cmp, const int32_t* __restrict__ cu,
                   const int32_t* __restrict__ cu_cmp, int B, int H, int H_I, int r, float scale_log2,
-                  float* __restrict__ kl_rows, int32_t* __restrict__ csize, int* status) {
+                  float* __restrict__ kl_rows, int32_t* __restrict__ csize, int* status,
+                  float* __restrict__ teacher_lse, float* __restrict__ student_lse) {
   constexpr int kStride = AttnSmem<D>::kStride;
   constexpr int kRows = NW * 16;
   constexpr int kThreads = NW * 32;
@@ -51,7 +52,13 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
   const int row = blockIdx.x;
   const int b = owner_sequence(cu, B, row);
   if (b < 0) {
-    if (tid == 0) { kl_rows[row] = 0.f; csize[row] = 0; }
+    if (tid == 0) {
+      kl_rows[row] = 0.f;
+      csize[row] = 0;
+      if (student_lse) student_lse[row] = -INFINITY;
+    }
+    if (teacher_lse)
+      for (int h = tid; h < H; h += kThreads) teacher_lse[(int64_t)row * H + h] = -INFINITY;
     return;
   }
   const int t = row - __ldg(cu + b);
@@ -166,6 +173,13 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
       lse2[i] = (l > 0.f && h < H) ? m_run[i] + __log2f(l) : -INFINITY;  // padding heads add nothing
     }
   }
+  if (teacher_lse != nullptr && (lane & 3) == 0) {  // natural units, for the indexer backward
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int h = warp * 16 + (lane >> 2) + i * 8;
+      if (h < H) teacher_lse[(int64_t)row * H + h] = lse2[i] * kLn2;
+    }
+  }
 
   // ---- pass 2: teacher p(j), student logits, KL accumulators ----
   float accA = 0.f, accB = 0.f;            // sum p ln p, sum p i    (threads < kKeys)
@@ -256,6 +270,7 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
     const float kl = n > 0 ? A - Bs + (M + __logf(Ls)) : 0.f;
     kl_rows[row] = kl;
     csize[row] = n;
+    if (student_lse) student_lse[row] = n > 0 ? M + __logf(Ls) : -INFINITY;
   }
   (void)kLn2;
 }
@@ -301,7 +316,8 @@ static cudaError_t launch_kl_t(const KLArgs& a, cudaStream_t stream) {
     kern<<<a.T_cap, NW * 32, smem, stream>>>(
         static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k_cmp), static_cast<const TIn*>(a.qI),
         static_cast<const TIn*>(a.w), static_cast<const TIn*>(a.kI), a.idx, a.k_pad, a.lse_cmp, a.cu,
-        a.cu_cmp, a.B, a.H, a.H_I, a.r, a.scale * kLog2e, a.kl_rows, a.csize, a.status);
+        a.cu_cmp, a.B, a.H, a.H_I, a.r, a.scale * kLog2e, a.kl_rows, a.csize, a.status, a.teacher_lse,
+        a.student_lse);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }

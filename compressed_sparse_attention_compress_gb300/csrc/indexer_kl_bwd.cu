@@ -37,7 +37,8 @@ template <typename TIn, int D, int NW, int DI>
 __global__ void __launch_bounds__(NW * 32)
 indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, const TIn* __restrict__ qI,
                       const TIn* __restrict__ w, const TIn* __restrict__ kI, const int32_t* __restrict__ idx,
-                      int k_pad, const float* __restrict__ lse_cmp, const int32_t* __restrict__ cu,
+                      int k_pad, const float* __restrict__ lse_cmp, const float* __restrict__ student_lse,
+                      const int32_t* __restrict__ cu,
                       const int32_t* __restrict__ cu_cmp, int B, int H, int H_I, int r, float scale_log2,
                       float grad_scale, TIn* __restrict__ dqI, TIn* __restrict__ dw, float* __restrict__ dkI,
                       int* status) {
@@ -155,9 +156,11 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
     }
   };
 
-  // ---- pass 1: per-head teacher log-sum-exp and the student's over C_t ----
+  // ---- pass 1: per-head teacher log-sum-exp and the student's over C_t (skipped when
+  // the forward handed both over) ----
   float lse2[2] = {-INFINITY, -INFINITY};
-  const bool have_lse = (!dense) && lse_cmp != nullptr;
+  const bool have_lse = lse_cmp != nullptr;
+  const bool one_pass = have_lse && student_lse != nullptr;
   if (have_lse) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -167,11 +170,12 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
   }
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   float mi = -INFINITY, li = 0.f;  // student log-sum-exp (natural units), per key thread
-  if (ntiles > 0) { resolve(0, 0); __syncthreads(); issue(0); }
+  const int ntiles1 = one_pass ? 0 : ntiles;
+  if (ntiles1 > 0) { resolve(0, 0); __syncthreads(); issue(0); }
   cp_async_commit();
-  for (int it = 0; it < ntiles; ++it) {
+  for (int it = 0; it < ntiles1; ++it) {
     const int buf = it & 1;
-    if (it + 1 < ntiles) { resolve(it + 1, buf ^ 1); __syncthreads(); issue(buf ^ 1); }
+    if (it + 1 < ntiles1) { resolve(it + 1, buf ^ 1); __syncthreads(); issue(buf ^ 1); }
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
@@ -231,7 +235,7 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
     float Ls = 0.f;
     for (int k = 0; k < kThreads; ++k)
       if (sRed[k] != -INFINITY) Ls += sRed[kThreads + k] * __expf(sRed[k] - M);
-    s_lse_i = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
+    s_lse_i = one_pass ? __ldg(student_lse + row) : (Ls > 0.f ? M + __logf(Ls) : -INFINITY);
   }
   __syncthreads();
   const float lse_i = s_lse_i;
@@ -386,7 +390,8 @@ static cudaError_t launch_kl_bwd_t(const KLBwdArgs& a, cudaStream_t stream) {
   constexpr float kLog2e = 1.4426950408889634f;
   kern<<<a.T_cap, kThreads, smem, stream>>>(
       static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k_cmp), static_cast<const TIn*>(a.qI),
-      static_cast<const TIn*>(a.w), static_cast<const TIn*>(a.kI), a.idx, a.k_pad, a.lse_cmp, a.cu, a.cu_cmp, a.B,
+      static_cast<const TIn*>(a.w), static_cast<const TIn*>(a.kI), a.idx, a.k_pad, a.lse_cmp, a.student_lse, a.cu,
+      a.cu_cmp, a.B,
       a.H, a.H_I, a.r, a.scale * kLog2e, a.grad_scale, static_cast<TIn*>(a.dqI), static_cast<TIn*>(a.dw), a.dkI,
       a.status);
   return cudaGetLastError();

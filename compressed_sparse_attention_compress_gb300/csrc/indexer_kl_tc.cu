@@ -129,7 +129,8 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
                            const __grid_constant__ CUtensorMap map_qi, const __grid_constant__ CUtensorMap map_ki,
                            const __nv_bfloat16* __restrict__ w, const int32_t* __restrict__ cu,
                            const int32_t* __restrict__ cu_cmp, int B, int r, float scale_log2,
-                           float* __restrict__ kl_rows, int32_t* __restrict__ csize, int* status) {
+                           float* __restrict__ kl_rows, int32_t* __restrict__ csize, int* status,
+                           float* __restrict__ teacher_lse, float* __restrict__ student_lse) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
@@ -366,6 +367,9 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
           const float mx = fmaxf(m, m2);
           const float ls = (mx == -INFINITY) ? 0.f : l * ex2(m - mx) + l2 * ex2(m2 - mx);
           s_L[q][h] = (ls > 0.f) ? -(mx + __log2f(ls)) : -INFINITY;  // negated; -inf: contributes nothing
+          if (teacher_lse != nullptr && q < bk.nq)  // natural units, for the indexer backward
+            teacher_lse[(int64_t)(bk.seq0 + bk.q0 + q) * kNH + h] =
+                (ls > 0.f) ? (mx + __log2f(ls)) * 0.6931471805599453f : -INFINITY;
         }
         KL_ADD(9, c_m);
       }
@@ -475,6 +479,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         }
         const int nvis = (bk.q0 + qq + 1) / r;
         kl_rows[bk.seq0 + bk.q0 + qq] = nvis > 0 ? a - bs + (mm + __logf(ll)) : 0.f;
+        if (student_lse != nullptr) student_lse[bk.seq0 + bk.q0 + qq] = nvis > 0 ? mm + __logf(ll) : -INFINITY;
         csize[bk.seq0 + bk.q0 + qq] = nvis;
       }
       named_sync(1, kComputeThreads);
@@ -507,11 +512,17 @@ bool indexer_kl_dense_tc_supported(const KLArgs& a, bool fp32) {
   return !fp32 && a.idx == nullptr && a.H == kNH && a.d == kDim && a.H_I == kHI && a.d_I == kDI;
 }
 
-__global__ void kl_zero_rows_kernel(float* __restrict__ kl_rows, int32_t* __restrict__ csize, int T_cap) {
+__global__ void kl_zero_rows_kernel(float* __restrict__ kl_rows, int32_t* __restrict__ csize, int T_cap,
+                                    float* __restrict__ teacher_lse, int H, float* __restrict__ student_lse) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T_cap; i += gridDim.x * blockDim.x) {
     kl_rows[i] = 0.f;
     csize[i] = 0;
+    if (student_lse) student_lse[i] = -INFINITY;  // rows without a C_t keep -inf
   }
+  if (teacher_lse)
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)T_cap * H;
+         i += (int64_t)gridDim.x * blockDim.x)
+      teacher_lse[i] = -INFINITY;
 }
 
 cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream) {
@@ -524,7 +535,7 @@ cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream) {
       !make_tmap_bf16_sw128(&mqi, a.qI, (uint64_t)a.T_cap * kHI, kDI, kQB * kHI) ||
       !make_tmap_bf16_sw128(&mki, a.kI, n_cmp_rows, kDI, kTK))
     return cudaErrorInvalidValue;
-  kl_zero_rows_kernel<<<152, 256, 0, stream>>>(a.kl_rows, a.csize, a.T_cap);
+  kl_zero_rows_kernel<<<152, 256, 0, stream>>>(a.kl_rows, a.csize, a.T_cap, a.teacher_lse, a.H, a.student_lse);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t smem = kSmemBytes + 1024;
@@ -538,7 +549,7 @@ cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream) {
   constexpr float kLog2e = 1.4426950408889634f;
   indexer_kl_dense_tc_kernel<<<grid, kThreads, smem, stream>>>(
       mq, mk, mqi, mki, static_cast<const __nv_bfloat16*>(a.w), a.cu, a.cu_cmp, a.B, a.r, a.scale * kLog2e,
-      a.kl_rows, a.csize, a.status);
+      a.kl_rows, a.csize, a.status, a.teacher_lse, a.student_lse);
   return cudaGetLastError();
 }
 

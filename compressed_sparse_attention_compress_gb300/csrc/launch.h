@@ -120,6 +120,8 @@ struct KLArgs {
   float* kl_sum;
   int32_t* n_valid;
   int* status;
+  float* teacher_lse = nullptr;  // optional [T_cap, H]: per-head log normaliser of the teacher over C_t
+  float* student_lse = nullptr;  // optional [T_cap]: log normaliser of the indexer logits over C_t
 };
 cudaError_t launch_indexer_kl(const KLArgs& a, bool fp32, cudaStream_t stream);
 bool indexer_kl_dense_tc_supported(const KLArgs& a, bool fp32);
@@ -135,7 +137,8 @@ struct KLBwdArgs {
   const void* kI;
   const int32_t* idx;   // nullptr: dense teacher
   int k_pad;
-  const float* lse_cmp; // optional per-head normaliser over C_t (sparse mode)
+  const float* lse_cmp; // optional per-head teacher normaliser over C_t (either mode)
+  const float* student_lse;  // optional student normaliser over C_t: with lse_cmp, one pass
   const int32_t* cu;
   const int32_t* cu_cmp;
   int B, T_cap, H, d, H_I, d_I, r;

@@ -105,13 +105,27 @@ class Forward:
                              wl.ratio, wl.window, self.scale, self.out, self.lse, self.lse_cmp,
                              v_cmp=self.v_cmp, v_raw=v_raw, sink=sink, stream=stream)
 
-    def kl(self, stream=None):
+    keep_stats = False   # kl() keeps the normalisers for indexer_backward by default
+
+    def kl(self, stream=None, save_stats: bool | None = None):
+        """The indexer KL loss; with ``save_stats`` (default ``keep_stats``) it also
+        keeps the teacher's and the student's log normalisers for
+        ``indexer_backward``, which then takes one pass instead of two."""
         wl, x = self.wl, self.x
+        save_stats = self.keep_stats if save_stats is None else save_stats
         sparse = wl.kl_mode == "sparse"
-        api.csa_indexer_kl(self.h, x["q"], self.kv_cmp, x["qI"], x["w"], self.kI, self.cu, self.cu_cmp,
-                           self.max_seqlen, wl.ratio, self.scale, self.kl_sum, self.ws,
-                           idx=self.idx if sparse else None, lse_cmp=self.lse_cmp if sparse else None,
-                           kl_per_query=self.kl_rows, n_valid=self.n_valid, stream=stream)
+        kw = dict(idx=self.idx if sparse else None, lse_cmp=self.lse_cmp if sparse else None,
+                  kl_per_query=self.kl_rows, n_valid=self.n_valid, stream=stream)
+        if not save_stats:
+            api.csa_indexer_kl(self.h, x["q"], self.kv_cmp, x["qI"], x["w"], self.kI, self.cu, self.cu_cmp,
+                               self.max_seqlen, wl.ratio, self.scale, self.kl_sum, self.ws, **kw)
+            return
+        if getattr(self, "teacher_lse", None) is None:
+            self.teacher_lse = torch.empty(wl.T_cap, wl.H, dtype=torch.float32, device=self.dev)
+            self.student_lse = torch.empty(wl.T_cap, dtype=torch.float32, device=self.dev)
+        api.csa_indexer_kl_ex(self.h, x["q"], self.kv_cmp, x["qI"], x["w"], self.kI, self.cu, self.cu_cmp,
+                              self.max_seqlen, wl.ratio, self.scale, self.kl_sum, self.ws,
+                              teacher_lse=self.teacher_lse, student_lse=self.student_lse, **kw)
 
     def backward(self, dout, stream=None, sink=None, dsink=None):
         """Gradients of the attention stage for upstream ``dout`` [T_cap, H, d],
@@ -155,9 +169,12 @@ class Forward:
             self.dw = torch.empty_like(x["w"])
             self.dkI = torch.empty(max(1, wl.T_cap // wl.ratio), wl.d_I, dtype=torch.float32, device=self.dev)
         sparse = wl.kl_mode == "sparse"
+        stats = getattr(self, "teacher_lse", None) is not None   # normalisers kept by kl(save_stats=True)
         api.csa_indexer_kl_bwd(self.h, x["q"], self.kv_cmp, x["qI"], x["w"], self.kI, self.cu, self.cu_cmp,
                                self.max_seqlen, wl.ratio, self.scale, self.dqI, self.dw, self.dkI,
-                               idx=self.idx if sparse else None, lse_cmp=self.lse_cmp if sparse else None,
+                               idx=self.idx if sparse else None,
+                               lse_cmp=self.teacher_lse if stats else (self.lse_cmp if sparse else None),
+                               student_lse=self.student_lse if stats else None,
                                grad_scale=grad_scale, stream=stream)
 
     def run(self, stream=None, sink=None):

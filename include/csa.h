@@ -235,6 +235,21 @@ csa_status_t window_attn_fwd(csa_handle_t handle, const void* q, const void* kv_
                              float softmax_scale, csa_dtype_t dtype, void* out, float* lse,
                              cudaStream_t stream);
 
+/* csa_indexer_kl that also writes the two log normalisers the indexer backward
+ * needs (the page runs that backward eagerly with the forward, §8.2):
+ * teacher_lse [T_cap, H] = log sum_{j in C_t} exp(softmax_scale q[t,h,:].kv_cmp[j,:])
+ * and student_lse [T_cap] = log sum_{j in C_t} exp(i_{t,j}), natural units,
+ * float32, -inf for capacity rows and rows with an empty C_t.  Either may be
+ * NULL.  Other arguments and results as csa_indexer_kl. */
+csa_status_t csa_indexer_kl_ex(csa_handle_t handle, const void* q, const void* kv_cmp,
+                               const void* qI, const void* w, const void* kI, const int32_t* idx,
+                               int k_pad, const float* lse_cmp, const int32_t* cu_seqlens,
+                               const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H,
+                               int d, int H_I, int d_I, int ratio, float softmax_scale,
+                               csa_dtype_t dtype, float* kl_sum, float* kl_per_query,
+                               int32_t* n_valid, void* ws, size_t ws_bytes, float* teacher_lse,
+                               float* student_lse, cudaStream_t stream);
+
 /* Attention backward, CSA (§8.2 "main attention backward": consumes the saved
  * output and LSE and produces Q, KV and attention-sink gradients without
  * materializing a dense attention matrix; §9 FP32 sink and softmax math).
@@ -351,10 +366,15 @@ csa_status_t csa_indexer_kl_static_scratch(csa_handle_t handle, const void* q, c
  * be passed here or applied later).  dqI [T_cap, H_I, d_I] and dw [T_cap, H_I]
  * (dtype) are written (0 for capacity rows and rows with an empty C_t); dkI
  * [floor(T_cap/ratio), d_I] float32 is zeroed and accumulated with float32
- * atomic additions.  idx / lse_cmp as in csa_indexer_kl.  Same limits. */
+ * atomic additions.  idx as in csa_indexer_kl.  lse_cmp (may be NULL): the
+ * teacher's per-head log normaliser over C_t -- csa_sparse_attn_fwd's lse_cmp
+ * in sparse mode, or the teacher_lse of csa_indexer_kl_ex in either mode;
+ * student_lse (may be NULL): the student's, from csa_indexer_kl_ex.  With both
+ * the call takes one pass over C_t instead of two.  Same limits. */
 csa_status_t csa_indexer_kl_bwd(csa_handle_t handle, const void* q, const void* kv_cmp,
                                 const void* qI, const void* w, const void* kI, const int32_t* idx,
-                                int k_pad, const float* lse_cmp, const int32_t* cu_seqlens,
+                                int k_pad, const float* lse_cmp, const float* student_lse,
+                                const int32_t* cu_seqlens,
                                 const int32_t* cu_cmp, int B, int T_cap, int max_seqlen, int H,
                                 int d, int H_I, int d_I, int ratio, float softmax_scale,
                                 float grad_scale, csa_dtype_t dtype, void* dqI, void* dw,

@@ -37,7 +37,7 @@ def _close(name, got, ref, quant=0.0):
 
 
 def _run(lengths, mode, H=64, d=128, H_I=8, d_I=64, ratio=4, topk=96, k_pad=128, fp32=False, seed=0,
-         grad_scale=1.0, cap_align=64, rows=None, check_kI=True):
+         grad_scale=1.0, cap_align=64, rows=None, check_kI=True, stats=False):
     sparse = mode != "dense"
     a = I.generate_indexer_bwd(lengths, H, d, H_I, d_I, ratio, topk if sparse else 0, k_pad, seed, cap_align)
     cu_np = a["cu_seqlens"]
@@ -58,11 +58,22 @@ def _run(lengths, mode, H=64, d=128, H_I=8, d_I=64, ratio=4, topk=96, k_pad=128,
         lse = torch.empty(T_cap, H, dtype=torch.float32, device="cuda")
         lse_cmp = torch.empty_like(lse)
         api.csa_sparse_attn_fwd(h, q, kc, kr, idx, cu, cu_cmp, ms, ratio, 128, scale, out, lse, lse_cmp)
+    student_lse = None
+    if stats:   # the KL forward keeps both normalisers; the backward then takes one pass
+        teacher_lse = torch.full((T_cap, H), 7.0, dtype=torch.float32, device="cuda")
+        student_lse = torch.full((T_cap,), 7.0, dtype=torch.float32, device="cuda")
+        kl_sum = torch.zeros(1, device="cuda")
+        ws = torch.empty(api.csa_indexer_kl_workspace(T_cap), dtype=torch.uint8, device="cuda")
+        api.csa_indexer_kl_ex(h, q, kc, qI, w, kI, cu, cu_cmp, ms, ratio, scale, kl_sum, ws, teacher_lse=teacher_lse,
+                              student_lse=student_lse, idx=idx, lse_cmp=lse_cmp)
+        torch.cuda.synchronize()
+        _check_stats(a, cu_np, ratio, scale, idx, teacher_lse, student_lse)
+        lse_cmp = teacher_lse
     dqI = torch.full_like(qI, 5.0)
     dw = torch.full_like(w, 5.0)
     dkI = torch.full((max(1, T_cap // ratio), d_I), 3.0, dtype=torch.float32, device="cuda")
     api.csa_indexer_kl_bwd(h, q, kc, qI, w, kI, cu, cu_cmp, ms, ratio, scale, dqI, dw, dkI, idx=idx,
-                           lse_cmp=lse_cmp, grad_scale=grad_scale)
+                           lse_cmp=lse_cmp, student_lse=student_lse, grad_scale=grad_scale)
     torch.cuda.synchronize()
     assert h.device_status() == 0
     T = int(cu_np[-1])
@@ -80,12 +91,48 @@ def _run(lengths, mode, H=64, d=128, H_I=8, d_I=64, ratio=4, topk=96, k_pad=128,
     return dict(dqI=dqI, dw=dw, dkI=dkI, qI=qI, w=w, kI=kI, n_c=int(cmp_np[-1]))
 
 
+def _check_stats(a, cu_np, ratio, scale, idx, teacher_lse, student_lse):
+    """teacher_lse against the attention oracle's compressed-only normaliser (the
+    same logsumexp over C_t), student_lse against logsumexp of the oracle's
+    indexer logits over C_t."""
+    T_cap = a["q"].shape[0]
+    T = int(cu_np[-1])
+    idx_np = idx.cpu().numpy() if idx is not None else None
+    kind = oracle.KIND_CSA if idx_np is not None else oracle.KIND_HCA
+    _, _, ref_t, _ = oracle.attention(kind, a["q"], a["k_cmp"], None, a["k_raw"], None, cu_np, ratio, 1, scale,
+                                      idx=idx_np)
+    got_t = ph.np32(teacher_lse)
+    fin = np.isfinite(ref_t)
+    assert np.array_equal(fin, np.isfinite(got_t))
+    np.testing.assert_allclose(got_t[fin], ref_t[fin], rtol=0, atol=1e-2)
+    max_vis = max(1, int(np.diff(cu_np).max()) // ratio)
+    logits, nvis = oracle.indexer_logits(a["qI"], a["w"], a["k_I"], cu_np, ratio, None, max_vis)
+    cmp_np = oracle.compressed_offsets(cu_np, ratio)
+    got_s = ph.np32(student_lse)
+    for row in range(T_cap):
+        if row >= T:
+            assert got_s[row] == -np.inf
+            continue
+        b = int(np.searchsorted(cu_np, row, side="right") - 1)
+        js = (np.arange(nvis[row]) if idx_np is None else idx_np[row][idx_np[row] >= 0] - cmp_np[b])
+        if js.size == 0:
+            assert got_s[row] == -np.inf
+            continue
+        ref = np.logaddexp.reduce(logits[row, js])
+        assert abs(got_s[row] - ref) <= 1e-3 * max(1.0, abs(ref)), (row, got_s[row], ref)
+
+
 RAGGED = [700, 0, 301, 1029, 5]
 
 
 @pytest.mark.parametrize("mode", ["sparse", "sparse_lse", "dense"])
 def test_64_heads_bf16_ragged(mode):
     _run(RAGGED, mode)
+
+
+@pytest.mark.parametrize("mode", ["sparse", "dense"])
+def test_one_pass_with_the_forward_normalisers(mode):
+    _run(RAGGED, mode, stats=True, seed=4)
 
 
 @pytest.mark.parametrize("mode", ["sparse", "dense"])
