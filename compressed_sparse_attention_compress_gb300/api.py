@@ -46,6 +46,7 @@ def _load():
         "csa_create": [I, P],
         "csa_destroy": [P],
         "csa_get_device_status": [P, P, P],
+        "csa_set_position_offsets": [P, P, I],
         "csa_compressed_offsets": [P, P, I, I, P, P],
         "csa_compress": [P, P, P, P, P, P, I, I, I, I, I, I, I, P, P],
         "csa_compress_ex": [P, P, P, P, P, P, P, F, I, F, I, I, P, P, I, I, I, I, I, I, I, P, P],
@@ -122,6 +123,11 @@ class Handle:
         v = ctypes.c_int(0)
         _check("csa_get_device_status", LIB.csa_get_device_status(self._h, _stream(stream), ctypes.byref(v)))
         return v.value
+
+    def set_position_offsets(self, pos0=None, cmp_rows: int = 0):
+        """Per-sequence position of the first packed row (device int32 [B]) for the
+        query calls made with this handle from now on; None restores 0."""
+        _check("csa_set_position_offsets", LIB.csa_set_position_offsets(self._h, _p(pos0), int(cmp_rows)))
 
     def close(self):
         if self._h:

@@ -10,7 +10,9 @@
 struct csa_handle_s {
   int device;
   int sm_count;
-  int* status;  // one int32 device word
+  int* status;               // one int32 device word
+  const int32_t* pos0;       // per-sequence position of the first row (csa_set_position_offsets), or null
+  int cmp_rows;              // rows of the compressed arrays when pos0 is set (0: T_cap / ratio)
 };
 
 namespace {
@@ -85,6 +87,14 @@ const char* csa_status_string(int s) {
     case CSA_ERR_DEVICE_BOUNDS: return "CSA_ERR_DEVICE_BOUNDS";
     default: return "CSA_UNKNOWN_STATUS";
   }
+}
+
+csa_status_t csa_set_position_offsets(csa_handle_t h, const int32_t* pos0, int cmp_rows) {
+  if (!h || cmp_rows < 0 || (pos0 != nullptr && (reinterpret_cast<uintptr_t>(pos0) & 3u) != 0))
+    return CSA_ERR_INVALID_ARG;
+  h->pos0 = pos0;
+  h->cmp_rows = pos0 != nullptr ? cmp_rows : 0;
+  return CSA_OK;
 }
 
 csa_status_t csa_get_device_status(csa_handle_t h, cudaStream_t stream, int* status) {
@@ -169,7 +179,7 @@ csa_status_t csa_indexer_topk(csa_handle_t h, const void* qI, const void* w, con
   DeviceGuard g(h->device);
   if (!g.ok) return CSA_ERR_CUDA;
   return from_cuda(csa::launch_indexer_topk(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, H_I, d_I, ratio, topk, k_pad,
-                                            fp32, idx, h->status, stream));
+                                            fp32, idx, h->status, stream, h->pos0, h->cmp_rows));
 }
 
 static csa_status_t attn_common(csa::AttnKind kind, csa_handle_t h, const void* q, const void* kv_cmp,
@@ -190,7 +200,7 @@ static csa_status_t attn_common(csa::AttnKind kind, csa_handle_t h, const void* 
   DeviceGuard g(h->device);
   if (!g.ok) return CSA_ERR_CUDA;
   csa::AttnArgs a{q, kv_cmp, v_cmp, kv_raw, v_raw, idx, k_pad, sink, cu, cu_cmp, B, T_cap, H, d,
-                  ratio, window, scale, out, lse, lse_cmp, h->status};
+                  ratio, window, scale, out, lse, lse_cmp, h->status, h->pos0};
   return from_cuda(csa::launch_attention(kind, a, dtype == CSA_FP32, stream));
 }
 
@@ -245,11 +255,11 @@ static csa_status_t attn_bwd_common(csa::AttnKind kind, csa_handle_t h, const vo
   if ((d != 64 && d != 128) || !pow2_in(H, 4, 128)) return CSA_ERR_UNSUPPORTED;
   DeviceGuard g(h->device);
   if (!g.ok) return CSA_ERR_CUDA;
-  const int n_cmp_cap = kind == csa::kAttnWindow ? 0 : T_cap / ratio;
+  const int n_cmp_cap = kind == csa::kAttnWindow ? 0 : (h->cmp_rows > T_cap / ratio ? h->cmp_rows : T_cap / ratio);
   csa::AttnBwdArgs a{q, kv_cmp, v_cmp, kv_raw, v_raw, idx, k_pad, sink, cu, cu_cmp, B, T_cap, H, d,
                      kind == csa::kAttnWindow ? 0 : ratio, window, n_cmp_cap, scale, out, lse, dout, dq,
                      kind == csa::kAttnWindow ? nullptr : dkv_cmp, kind == csa::kAttnWindow ? nullptr : dv_cmp,
-                     dkv_raw, dv_raw, dsink, delta, h->status};
+                     dkv_raw, dv_raw, dsink, delta, h->status, h->pos0};
   return from_cuda(csa::launch_attention_bwd(kind, a, dtype == CSA_FP32, stream));
 }
 
@@ -311,7 +321,7 @@ static csa_status_t indexer_kl_common(csa_handle_t h, const void* q, const void*
   int32_t* csize = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + (size_t)T_cap * 4);
   if (!opt_aligned16(teacher_lse) || !opt_aligned16(student_lse)) return CSA_ERR_INVALID_ARG;
   csa::KLArgs a{q, kv_cmp, qI, w, kI, idx, k_pad, lse_cmp, cu, cu_cmp, B, T_cap, H, d, H_I, d_I, ratio,
-                scale, kl_rows, csize, kl_sum, n_valid, h->status, teacher_lse, student_lse};
+                scale, kl_rows, csize, kl_sum, n_valid, h->status, teacher_lse, student_lse, h->pos0, h->cmp_rows};
   return from_cuda(csa::launch_indexer_kl(a, dtype == CSA_FP32, stream));
 }
 
@@ -355,7 +365,8 @@ csa_status_t csa_indexer_kl_bwd(csa_handle_t h, const void* q, const void* kv_cm
   DeviceGuard g(h->device);
   if (!g.ok) return CSA_ERR_CUDA;
   csa::KLBwdArgs a{q, kv_cmp, qI, w, kI, idx, k_pad, lse_cmp, student_lse, cu, cu_cmp, B, T_cap, H, d, H_I, d_I, ratio,
-                   T_cap / ratio, scale, grad_scale, dqI, dw, dkI, h->status};
+                   h->cmp_rows > T_cap / ratio ? h->cmp_rows : T_cap / ratio, scale, grad_scale, dqI, dw, dkI,
+                   h->status, h->pos0};
   return from_cuda(csa::launch_indexer_kl_bwd(a, dtype == CSA_FP32, stream));
 }
 
@@ -383,7 +394,8 @@ csa_status_t csa_indexer_topk_fp8(csa_handle_t h, const uint8_t* qI, const float
   DeviceGuard g(h->device);
   if (!g.ok) return CSA_ERR_CUDA;
   return from_cuda(csa::launch_indexer_topk_fp8_full(qI, qI_scale, w, kI, kI_scale, cu, cu_cmp, B, T_cap, max_vis,
-                                                     ratio, topk, k_pad, idx, h->status, stream));
+                                                     ratio, topk, k_pad, idx, h->status, stream, h->pos0,
+                                                     h->cmp_rows));
 }
 
 }  // extern "C"

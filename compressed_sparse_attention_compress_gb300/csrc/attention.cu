@@ -34,7 +34,8 @@ attention_kernel(int kind, const TIn* __restrict__ q, const TIn* __restrict__ k_
                  const float* __restrict__ sink, const int32_t* __restrict__ cu,
                  const int32_t* __restrict__ cu_cmp, int B, int H, int r, int window, float scale_log2,
                  TOut* __restrict__ out, float* __restrict__ lse, float* __restrict__ lse_cmp,
-                 int* status) {
+                 int* status,
+                 const int32_t* __restrict__ pos0) {
   constexpr int kStride = AttnSmem<D>::kStride;
   constexpr int kRows = NW * 16;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -60,7 +61,8 @@ attention_kernel(int kind, const TIn* __restrict__ q, const TIn* __restrict__ k_
   }
   const int seq0 = __ldg(cu + b);
   const int t = row - seq0;
-  const int nvis = (kind == kAttnWindow || r <= 0) ? 0 : (t + 1) / r;
+  const int p0 = pos0 ? __ldg(pos0 + b) : 0;  // position of the sequence's first row here
+  const int nvis = (kind == kAttnWindow || r <= 0) ? 0 : (t + p0 + 1) / r;
   const int cmp0 = (kind == kAttnWindow) ? 0 : __ldg(cu_cmp + b);
   const int w0 = max(0, t - window + 1);
   const int n_win = t - w0 + 1;
@@ -269,7 +271,7 @@ static cudaError_t launch_attention_t(AttnKind kind, const AttnArgs& a, cudaStre
       (int)kind, static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k_cmp), static_cast<const TIn*>(a.v_cmp),
       static_cast<const TIn*>(a.k_raw), static_cast<const TIn*>(a.v_raw), a.idx, a.k_pad, a.sink, a.cu,
       a.cu_cmp, a.B, a.H, a.r, a.window, a.scale * kLog2e, static_cast<TOut*>(a.out), a.lse, a.lse_cmp,
-      a.status);
+      a.status, a.pos0);
   return cudaGetLastError();
 }
 

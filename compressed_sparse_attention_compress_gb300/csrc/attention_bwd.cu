@@ -107,7 +107,8 @@ attention_bwd_kernel(int kind, const TIn* __restrict__ q, const TIn* __restrict_
                      float scale_log2, const float* __restrict__ lse, const float* __restrict__ delta,
                      const TIn* __restrict__ dout, TOut* __restrict__ dq, float* __restrict__ dk_cmp,
                      float* __restrict__ dv_cmp, float* __restrict__ dk_raw, float* __restrict__ dv_raw,
-                     int* status) {
+                     int* status,
+                     const int32_t* __restrict__ pos0) {
   constexpr int kStride = AttnSmem<D>::kStride;
   constexpr int kRows = NW * 16;
   constexpr float kLog2e = 1.4426950408889634f;
@@ -133,7 +134,8 @@ attention_bwd_kernel(int kind, const TIn* __restrict__ q, const TIn* __restrict_
   }
   const int seq0 = __ldg(cu + b);
   const int t = row - seq0;
-  const int nvis = (kind == kAttnWindow || r <= 0) ? 0 : (t + 1) / r;
+  const int p0 = pos0 ? __ldg(pos0 + b) : 0;  // position of the sequence's first row here
+  const int nvis = (kind == kAttnWindow || r <= 0) ? 0 : (t + p0 + 1) / r;
   const int cmp0 = (kind == kAttnWindow) ? 0 : __ldg(cu_cmp + b);
   const int w0 = max(0, t - window + 1);
   const int n_win = t - w0 + 1;
@@ -332,7 +334,7 @@ static cudaError_t launch_bwd_t(AttnKind kind, const AttnBwdArgs& a, cudaStream_
       (int)kind, static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k_cmp), static_cast<const TIn*>(a.v_cmp),
       static_cast<const TIn*>(a.k_raw), static_cast<const TIn*>(a.v_raw), a.idx, a.k_pad, a.cu, a.cu_cmp, a.B, a.H,
       a.r, a.window, a.scale, a.scale * kLog2e, a.lse, a.delta, static_cast<const TIn*>(a.dout),
-      static_cast<TOut*>(a.dq), a.dk_cmp, a.dv_cmp, a.dk_raw, a.dv_raw, a.status);
+      static_cast<TOut*>(a.dq), a.dk_cmp, a.dv_cmp, a.dk_raw, a.dv_raw, a.status, a.pos0);
   return cudaGetLastError();
 }
 

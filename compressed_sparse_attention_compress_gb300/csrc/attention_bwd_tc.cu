@@ -87,7 +87,8 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
                         int window, float scale, float scale_log2, const float* __restrict__ lse,
                         const float* __restrict__ delta, const __nv_bfloat16* __restrict__ dout,
                         __nv_bfloat16* __restrict__ dq, float* __restrict__ dkv_cmp, float* __restrict__ dkv_raw,
-                        int* status) {
+                        int* status,
+                        const int32_t* __restrict__ pos0) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_kvfull[2], s_kvfree[2];
@@ -147,7 +148,8 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
       if (b < 0) continue;             // capacity rows are written by another kernel
       const int seq0 = __ldg(cu + b);
       const int t = row - seq0;
-      const int nvis = (kind == kAttnWindow || r <= 0) ? 0 : (t + 1) / r;
+      const int p0 = pos0 ? __ldg(pos0 + b) : 0;  // position of the sequence's first row here
+      const int nvis = (kind == kAttnWindow || r <= 0) ? 0 : (t + p0 + 1) / r;
       const int cmp0 = kind == kAttnWindow ? 0 : __ldg(cu_cmp + b);
       const int w0 = max(0, t - window + 1);
       const int nwin = t - w0 + 1;
@@ -526,7 +528,7 @@ cudaError_t launch_attention_bwd_tc(AttnKind kind, const AttnBwdArgs& a, cudaStr
       (int)kind, static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cmp),
       static_cast<const __nv_bfloat16*>(a.k_raw), a.idx, a.k_pad, a.cu, a.cu_cmp, a.B, a.T_cap, a.r, a.window,
       a.scale, a.scale * kLog2e, a.lse, a.delta, static_cast<const __nv_bfloat16*>(a.dout),
-      static_cast<__nv_bfloat16*>(a.dq), a.dk_cmp, a.dk_raw, a.status);
+      static_cast<__nv_bfloat16*>(a.dq), a.dk_cmp, a.dk_raw, a.status, a.pos0);
   return cudaGetLastError();
 }
 

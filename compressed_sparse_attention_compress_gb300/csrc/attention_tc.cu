@@ -98,7 +98,8 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
                     const float* __restrict__ sink, const int32_t* __restrict__ cu,
                     const int32_t* __restrict__ cu_cmp, int B, int T_cap, int r, int window, float scale_log2,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ lse_cmp,
-                    int* status) {
+                    int* status,
+                    const int32_t* __restrict__ pos0) {
   using L = Layout<SEPV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
@@ -152,7 +153,8 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
     }
     const int seq0 = __ldg(cu + b);
     const int t = row - seq0;
-    const int nvis = (kind == kAttnWindow || r <= 0) ? 0 : (t + 1) / r;
+    const int p0 = pos0 ? __ldg(pos0 + b) : 0;  // position of the sequence's first row here
+    const int nvis = (kind == kAttnWindow || r <= 0) ? 0 : (t + p0 + 1) / r;
     const int cmp0 = kind == kAttnWindow ? 0 : __ldg(cu_cmp + b);
     const int w0 = max(0, t - window + 1);
     const int n_win = t - w0 + 1;
@@ -462,7 +464,7 @@ static cudaError_t launch_tc_t(AttnKind kind, const AttnArgs& a, cudaStream_t st
       (int)kind, static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cmp),
       static_cast<const __nv_bfloat16*>(a.v_cmp), static_cast<const __nv_bfloat16*>(a.k_raw),
       static_cast<const __nv_bfloat16*>(a.v_raw), a.idx, a.k_pad, a.sink, a.cu, a.cu_cmp, a.B, a.T_cap, a.r,
-      a.window, a.scale * kLog2e, static_cast<__nv_bfloat16*>(a.out), a.lse, a.lse_cmp, a.status);
+      a.window, a.scale * kLog2e, static_cast<__nv_bfloat16*>(a.out), a.lse, a.lse_cmp, a.status, a.pos0);
   return cudaGetLastError();
 }
 

@@ -121,7 +121,8 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
                     const float* __restrict__ sink, const int32_t* __restrict__ cu,
                     const int32_t* __restrict__ cu_cmp, int B, int T_cap, int r, int window, float scale_log2,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ lse_cmp,
-                    int* status) {
+                    int* status,
+                    const int32_t* __restrict__ pos0) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[2][2], s_empty[2][2];
@@ -192,7 +193,8 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       if (b < 0) continue;             // capacity rows are written by another kernel
       const int seq0 = __ldg(cu + b);
       const int t = row - seq0;
-      const int nvis = (kind == kAttnWindow || r <= 0) ? 0 : (t + 1) / r;
+      const int p0 = pos0 ? __ldg(pos0 + b) : 0;  // position of the sequence's first row here
+      const int nvis = (kind == kAttnWindow || r <= 0) ? 0 : (t + p0 + 1) / r;
       const int cmp0 = kind == kAttnWindow ? 0 : __ldg(cu_cmp + b);
       const int w0 = max(0, t - window + 1);
       const int nwin = t - w0 + 1;
@@ -697,7 +699,7 @@ cudaError_t launch_attention_ws(AttnKind kind, const AttnArgs& a, cudaStream_t s
   attention_ws_kernel<<<grid, kThreads, smem, stream>>>(
       (int)kind, static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cmp),
       static_cast<const __nv_bfloat16*>(a.k_raw), a.idx, a.k_pad, a.sink, a.cu, a.cu_cmp, a.B, a.T_cap, a.r,
-      a.window, a.scale * kLog2e, static_cast<__nv_bfloat16*>(a.out), a.lse, a.lse_cmp, a.status);
+      a.window, a.scale * kLog2e, static_cast<__nv_bfloat16*>(a.out), a.lse, a.lse_cmp, a.status, a.pos0);
   return cudaGetLastError();
 }
 

@@ -31,7 +31,8 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
                   int k_pad, const float* __restrict__ lse_cmp, const int32_t* __restrict__ cu,
                   const int32_t* __restrict__ cu_cmp, int B, int H, int H_I, int r, float scale_log2,
                   float* __restrict__ kl_rows, int32_t* __restrict__ csize, int* status,
-                  float* __restrict__ teacher_lse, float* __restrict__ student_lse) {
+                  float* __restrict__ teacher_lse, float* __restrict__ student_lse,
+                  const int32_t* __restrict__ pos0) {
   constexpr int kStride = AttnSmem<D>::kStride;
   constexpr int kRows = NW * 16;
   constexpr int kThreads = NW * 32;
@@ -62,7 +63,8 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
     return;
   }
   const int t = row - __ldg(cu + b);
-  const int nvis = r > 0 ? (t + 1) / r : 0;
+  const int p0 = pos0 ? __ldg(pos0 + b) : 0;  // position of the sequence's first row here
+  const int nvis = r > 0 ? (t + p0 + 1) / r : 0;
   const int cmp0 = __ldg(cu_cmp + b);
   const bool dense = idx == nullptr;
   const int n_slots = dense ? nvis : k_pad;
@@ -317,7 +319,7 @@ static cudaError_t launch_kl_t(const KLArgs& a, cudaStream_t stream) {
         static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k_cmp), static_cast<const TIn*>(a.qI),
         static_cast<const TIn*>(a.w), static_cast<const TIn*>(a.kI), a.idx, a.k_pad, a.lse_cmp, a.cu,
         a.cu_cmp, a.B, a.H, a.H_I, a.r, a.scale * kLog2e, a.kl_rows, a.csize, a.status, a.teacher_lse,
-        a.student_lse);
+        a.student_lse, a.pos0);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }

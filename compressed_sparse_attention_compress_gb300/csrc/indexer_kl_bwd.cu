@@ -41,7 +41,8 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
                       const int32_t* __restrict__ cu,
                       const int32_t* __restrict__ cu_cmp, int B, int H, int H_I, int r, float scale_log2,
                       float grad_scale, TIn* __restrict__ dqI, TIn* __restrict__ dw, float* __restrict__ dkI,
-                      int* status) {
+                      int* status,
+                      const int32_t* __restrict__ pos0) {
   constexpr int kStride = AttnSmem<D>::kStride;
   constexpr int kRows = NW * 16;
   constexpr int kThreads = NW * 32;
@@ -76,7 +77,8 @@ indexer_kl_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, 
   };
   if (b < 0) { write_zero(); return; }
   const int t = row - __ldg(cu + b);
-  const int nvis = r > 0 ? (t + 1) / r : 0;
+  const int p0 = pos0 ? __ldg(pos0 + b) : 0;  // position of the sequence's first row here
+  const int nvis = r > 0 ? (t + p0 + 1) / r : 0;
   const int cmp0 = __ldg(cu_cmp + b);
   const bool dense = idx == nullptr;
   const int n_slots = dense ? nvis : k_pad;
@@ -393,7 +395,7 @@ static cudaError_t launch_kl_bwd_t(const KLBwdArgs& a, cudaStream_t stream) {
       static_cast<const TIn*>(a.w), static_cast<const TIn*>(a.kI), a.idx, a.k_pad, a.lse_cmp, a.student_lse, a.cu,
       a.cu_cmp, a.B,
       a.H, a.H_I, a.r, a.scale * kLog2e, a.grad_scale, static_cast<TIn*>(a.dqI), static_cast<TIn*>(a.dw), a.dkI,
-      a.status);
+      a.status, a.pos0);
   return cudaGetLastError();
 }
 

@@ -86,13 +86,13 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 struct Block {
-  int b, q0, nq, seq0, cmp0, nvis_max, ntiles;
+  int b, q0, nq, seq0, cmp0, p0, nvis_max, ntiles;
 };
 
 // Blocks of kQB consecutive queries of one sequence, handed out heaviest
 // (latest in the buffer) first.  Block k counts from the end.
 __device__ __forceinline__ bool block_of(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_cmp, int B,
-                                         int r, int total, int k, Block& out) {
+                                         int r, int total, int k, Block& out, const int32_t* __restrict__ pos0) {
   int c = total - 1 - k;
   for (int bb = 0; bb < B; ++bb) {
     const int L = max(0, __ldg(cu + bb + 1) - __ldg(cu + bb));
@@ -103,7 +103,8 @@ __device__ __forceinline__ bool block_of(const int32_t* __restrict__ cu, const i
       out.nq = min(kQB, L - c * kQB);
       out.seq0 = __ldg(cu + bb);
       out.cmp0 = __ldg(cu_cmp + bb);
-      out.nvis_max = (out.q0 + out.nq) / r;
+      out.p0 = pos0 ? __ldg(pos0 + bb) : 0;  // position of the sequence's first row here
+      out.nvis_max = (out.q0 + out.nq + out.p0) / r;
       out.ntiles = (out.nvis_max + kTK - 1) / kTK;
       return true;
     }
@@ -130,7 +131,8 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
                            const __nv_bfloat16* __restrict__ w, const int32_t* __restrict__ cu,
                            const int32_t* __restrict__ cu_cmp, int B, int r, float scale_log2,
                            float* __restrict__ kl_rows, int32_t* __restrict__ csize, int* status,
-                           float* __restrict__ teacher_lse, float* __restrict__ student_lse) {
+                           float* __restrict__ teacher_lse, float* __restrict__ student_lse,
+                           const int32_t* __restrict__ pos0) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
@@ -188,7 +190,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
       uint32_t it = 0, nblk = 0;
       for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
         Block bk;
-        if (!block_of(cu, cu_cmp, B, r, total, k, bk) || bk.ntiles == 0) continue;
+        if (!block_of(cu, cu_cmp, B, r, total, k, bk, pos0) || bk.ntiles == 0) continue;
         if (!mbar_wait_bounded(bar_qempty, (nblk & 1u) ^ 1u, status)) { s_abort = 1; break; }
         ++nblk;
         mbar_arrive_expect_tx(bar_qfull, 2 * kQRegion + kQB * kHI * 128);
@@ -223,7 +225,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
       uint32_t it = 0, nblk = 0, p1 = 0, nf0 = 0, nf1 = 0;
       for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
         Block bk;
-        if (!block_of(cu, cu_cmp, B, r, total, k, bk) || bk.ntiles == 0) continue;
+        if (!block_of(cu, cu_cmp, B, r, total, k, bk, pos0) || bk.ntiles == 0) continue;
         if (!mbar_wait_bounded(bar_qfull, nblk & 1u, status)) { s_abort = 1; break; }
         ++nblk;
         for (int pass = 0; pass < 2; ++pass) {
@@ -288,7 +290,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
     uint32_t p1 = 0, nf0 = 0, nf1 = 0;       // score-buffer uses, as counted by the MMA warp
     for (int k = blockIdx.x; k < total; k += gridDim.x) {
       Block bk;
-      if (!block_of(cu, cu_cmp, B, r, total, k, bk)) continue;
+      if (!block_of(cu, cu_cmp, B, r, total, k, bk, pos0)) continue;
       if (bk.ntiles == 0) {
         if (tid < bk.nq) {
           kl_rows[bk.seq0 + bk.q0 + tid] = 0.f;
@@ -304,7 +306,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
       {
         const int mt = wg >> 1, half = wg & 1;
         const int q = 2 * mt + (rowl >> 6), h = rowl & 63;
-        const int nvis = (bk.q0 + q + 1) / r;
+        const int nvis = (bk.q0 + q + bk.p0 + 1) / r;
         float m = -INFINITY, l = 0.f;
         for (int i = 0; i < bk.ntiles; ++i) {
           const uint32_t d = p1++ & 1u;
@@ -377,7 +379,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
       if (*(volatile int*)&s_abort) break;  // uniform: read after the barrier
       // ---- pass 2: one thread per key, warpgroup q = query q ----
       const int q = wg;
-      const int nvis_q = (bk.q0 + q + 1) / r;
+      const int nvis_q = (bk.q0 + q + bk.p0 + 1) / r;
       const bool q_ok = q < bk.nq;
       float A = 0.f, Bs = 0.f, mI = -INFINITY, lI = 0.f;
       for (int i = 0; i < bk.ntiles; ++i) {
@@ -477,7 +479,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
           const float m2 = s_red[qq * 4 + ww][2];
           if (m2 != -INFINITY) ll += s_red[qq * 4 + ww][3] * __expf(m2 - mm);
         }
-        const int nvis = (bk.q0 + qq + 1) / r;
+        const int nvis = (bk.q0 + qq + bk.p0 + 1) / r;
         kl_rows[bk.seq0 + bk.q0 + qq] = nvis > 0 ? a - bs + (mm + __logf(ll)) : 0.f;
         if (student_lse != nullptr) student_lse[bk.seq0 + bk.q0 + qq] = nvis > 0 ? mm + __logf(ll) : -INFINITY;
         csize[bk.seq0 + bk.q0 + qq] = nvis;
@@ -529,7 +531,8 @@ cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream) {
   if (a.T_cap <= 0) return cudaSuccess;
   CUtensorMap mq, mk, mqi, mki;
   // the compressed arrays hold at most T_cap / r rows
-  const uint64_t n_cmp_rows = (uint64_t)(a.T_cap / a.r > 0 ? a.T_cap / a.r : 1);
+  const int rows_c = a.cmp_rows > a.T_cap / a.r ? a.cmp_rows : a.T_cap / a.r;
+  const uint64_t n_cmp_rows = (uint64_t)(rows_c > 0 ? rows_c : 1);
   if (!make_tmap_bf16_sw128(&mq, a.q, (uint64_t)a.T_cap * kNH, kDim, 128) ||
       !make_tmap_bf16_sw128(&mk, a.k_cmp, n_cmp_rows, kDim, kTK) ||
       !make_tmap_bf16_sw128(&mqi, a.qI, (uint64_t)a.T_cap * kHI, kDI, kQB * kHI) ||
@@ -549,7 +552,7 @@ cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream) {
   constexpr float kLog2e = 1.4426950408889634f;
   indexer_kl_dense_tc_kernel<<<grid, kThreads, smem, stream>>>(
       mq, mk, mqi, mki, static_cast<const __nv_bfloat16*>(a.w), a.cu, a.cu_cmp, a.B, a.r, a.scale * kLog2e,
-      a.kl_rows, a.csize, a.status, a.teacher_lse, a.student_lse);
+      a.kl_rows, a.csize, a.status, a.teacher_lse, a.student_lse, a.pos0);
   return cudaGetLastError();
 }
 

@@ -68,7 +68,8 @@ template <typename TIn, int DI>
 __global__ void __launch_bounds__(kThreads)
 indexer_topk_kernel(const TIn* __restrict__ qI, const TIn* __restrict__ w, const TIn* __restrict__ kI,
                     const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_cmp, int B, int H_I,
-                    int G, int max_vis, int r, int topk, int k_pad, int32_t* __restrict__ idx, int* status) {
+                    int G, int max_vis, int r, int topk, int k_pad, int32_t* __restrict__ idx, int* status,
+                    const int32_t* __restrict__ pos0) {
   constexpr int kAStride = DI + 8;
   extern __shared__ __align__(128) uint8_t smem[];
   const int vstride = (max_vis + 3) & ~3;                                              // 16-byte rows
@@ -104,10 +105,11 @@ indexer_topk_kernel(const TIn* __restrict__ qI, const TIn* __restrict__ w, const
   const int q0 = s_q0, nq = s_nq;
   const int seq0 = __ldg(cu + b);
   const int cmp0 = __ldg(cu_cmp + b);
-  const int n_b = (__ldg(cu + b + 1) - seq0) / r;
+  const int p0 = pos0 ? __ldg(pos0 + b) : 0;  // position of the sequence's first row here
+  const int n_b = (__ldg(cu + b + 1) - seq0 + p0) / r;
   const int rows = G * H_I;
   const int mtiles = (rows + 15) / 16;
-  const int vis_last = (q0 + nq) / r;  // visible entries of the chunk's last query
+  const int vis_last = (q0 + nq + p0) / r;  // visible entries of the chunk's last query
   const int ntiles = (vis_last + kTileN - 1) / kTileN;
 
   // A operand: indexer query rows (g, h) -> row g*H_I + h; zero past nq.
@@ -193,7 +195,7 @@ indexer_topk_kernel(const TIn* __restrict__ qI, const TIn* __restrict__ w, const
   for (int g = 0; g < nq; ++g) {
     const int t = q0 + g;
     const int64_t orow = (int64_t)(seq0 + t) * k_pad;
-    const int n = (t + 1) / r;
+    const int n = (t + p0 + 1) / r;
     const int m = min(topk, n);
     const uint32_t* keys = sKey + (size_t)g * vstride;
     uint32_t thr = 0;
@@ -321,7 +323,8 @@ bool indexer_topk_supported(int H_I, int d_I, int max_vis, int k_pad, int in_byt
 template <typename TIn, int DI>
 static cudaError_t launch_topk_t(const void* qI, const void* w, const void* kI, const int32_t* cu,
                                  const int32_t* cu_cmp, int B, int T_cap, int max_vis, int H_I, int r,
-                                 int topk, int k_pad, int32_t* idx, int* status, cudaStream_t stream) {
+                                 int topk, int k_pad, int32_t* idx, int* status, cudaStream_t stream,
+                                 const int32_t* pos0) {
   const int G = topk_group(H_I, max_vis);
   const size_t smem = topk_smem(G, max_vis, DI);
   auto kern = indexer_topk_kernel<TIn, DI>;
@@ -331,7 +334,7 @@ static cudaError_t launch_topk_t(const void* qI, const void* w, const void* kI, 
   if (T_cap > 0) {
     kern<<<(unsigned)grid, kThreads, smem, stream>>>(static_cast<const TIn*>(qI), static_cast<const TIn*>(w),
                                                      static_cast<const TIn*>(kI), cu, cu_cmp, B, H_I, G, max_vis,
-                                                     r, topk, k_pad, idx, status);
+                                                     r, topk, k_pad, idx, status, pos0);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     topk_fill_capacity_kernel<<<152, 256, 0, stream>>>(cu, B, T_cap, k_pad, idx);
@@ -342,9 +345,9 @@ static cudaError_t launch_topk_t(const void* qI, const void* w, const void* kI, 
 cudaError_t launch_indexer_topk_fp8_full(const uint8_t* qI, const float* qs, const void* w, const uint8_t* kI,
                                          const float* ks, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap,
                                          int max_vis, int r, int topk, int k_pad, int32_t* idx, int* status,
-                                         cudaStream_t stream) {
+                                         cudaStream_t stream, const int32_t* pos0, int cmp_rows) {
   cudaError_t err = launch_indexer_topk_fp8(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx,
-                                            status, stream);
+                                            status, stream, pos0, cmp_rows);
   if (err != cudaSuccess || T_cap <= 0) return err;
   topk_fill_capacity_kernel<<<152, 256, 0, stream>>>(cu, B, T_cap, k_pad, idx);
   return cudaGetLastError();
@@ -352,11 +355,12 @@ cudaError_t launch_indexer_topk_fp8_full(const uint8_t* qI, const float* qs, con
 
 cudaError_t launch_indexer_topk(const void* qI, const void* w, const void* kI, const int32_t* cu,
                                 const int32_t* cu_cmp, int B, int T_cap, int max_vis, int H_I, int d_I, int r,
-                                int topk, int k_pad, bool fp32, int32_t* idx, int* status, cudaStream_t stream) {
+                                int topk, int k_pad, bool fp32, int32_t* idx, int* status, cudaStream_t stream,
+                                const int32_t* pos0, int cmp_rows) {
   // indexer 8 heads x 64 dims in bf16 scores on tcgen05 with TMA-fed tiles
   if (indexer_topk_tc_supported(H_I, d_I, max_vis, fp32)) {
     cudaError_t err = launch_indexer_topk_tc(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status,
-                                             stream);
+                                             stream, pos0, cmp_rows);
     if (err != cudaSuccess || T_cap <= 0) return err;
     topk_fill_capacity_kernel<<<152, 256, 0, stream>>>(cu, B, T_cap, k_pad, idx);
     return cudaGetLastError();
@@ -364,15 +368,15 @@ cudaError_t launch_indexer_topk(const void* qI, const void* w, const void* kI, c
   if (fp32) {
     if (d_I == 32)
       return launch_topk_t<float, 32>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, H_I, r, topk, k_pad, idx, status,
-                                      stream);
+                                      stream, pos0);
     return launch_topk_t<float, 64>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, H_I, r, topk, k_pad, idx, status,
-                                    stream);
+                                    stream, pos0);
   }
   if (d_I == 32)
     return launch_topk_t<__nv_bfloat16, 32>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, H_I, r, topk, k_pad, idx,
-                                            status, stream);
+                                            status, stream, pos0);
   return launch_topk_t<__nv_bfloat16, 64>(qI, w, kI, cu, cu_cmp, B, T_cap, max_vis, H_I, r, topk, k_pad, idx,
-                                          status, stream);
+                                          status, stream, pos0);
 }
 
 }  // namespace csa

@@ -81,7 +81,7 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 }
 
 struct QBlock {
-  int q0, nq, seq0, cmp0, nvis_max, ntiles;
+  int q0, nq, seq0, cmp0, p0, nvis_max, ntiles;
   bool score;  // some query sees more than k entries
 };
 
@@ -93,7 +93,8 @@ __device__ __forceinline__ int total_qblocks(const int32_t* __restrict__ cu, int
 
 // Block k counted from the end of the buffer (latest queries, most entries, first).
 __device__ __forceinline__ bool qblock_of(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_cmp, int B,
-                                          int r, int G, int topk, int max_vis, int total, int k, QBlock& o) {
+                                          int r, int G, int topk, int max_vis, int total, int k, QBlock& o,
+                                          const int32_t* __restrict__ pos0) {
   int c = total - 1 - k;
   for (int bb = 0; bb < B; ++bb) {
     const int L = max(0, __ldg(cu + bb + 1) - __ldg(cu + bb));
@@ -103,7 +104,8 @@ __device__ __forceinline__ bool qblock_of(const int32_t* __restrict__ cu, const 
       o.nq = min(G, L - c * G);
       o.seq0 = __ldg(cu + bb);
       o.cmp0 = __ldg(cu_cmp + bb);
-      o.nvis_max = min((o.q0 + o.nq) / r, max_vis);
+      o.p0 = pos0 ? __ldg(pos0 + bb) : 0;  // position of the sequence's first row here
+      o.nvis_max = min((o.q0 + o.nq + o.p0) / r, max_vis);
       o.score = o.nvis_max > topk;
       o.ntiles = o.score ? (o.nvis_max + kTK - 1) / kTK : 0;
       return true;
@@ -125,7 +127,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
                        const __nv_bfloat16* __restrict__ w, const float* __restrict__ qs,
                        const float* __restrict__ ks, const int32_t* __restrict__ cu,
                        const int32_t* __restrict__ cu_cmp, int B, int r, int topk, int k_pad, int max_vis,
-                       int32_t* __restrict__ idx, int* status) {
+                       int32_t* __restrict__ idx, int* status, const int32_t* __restrict__ pos0) {
   constexpr uint32_t kRowBytes = kFp8 ? kDI : 2 * kDI;  // bytes of one operand row
   constexpr int kN = G * kHI;  // MMA N: query-head rows
   constexpr int kComputeWarps = CW;
@@ -185,7 +187,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
       uint32_t it = 0, nblk = 0;
       for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
         QBlock bk;
-        if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk) || bk.ntiles == 0) continue;
+        if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk, pos0) || bk.ntiles == 0) continue;
         if (!mbar_wait_bounded(bar_qempty, (nblk & 1u) ^ 1u, status)) { s_abort = 1; break; }
         ++nblk;
         mbar_arrive_expect_tx(bar_qfull, kN * kRowBytes);
@@ -205,7 +207,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
       uint32_t it = 0, nblk = 0;
       for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
         QBlock bk;
-        if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk) || bk.ntiles == 0) continue;
+        if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk, pos0) || bk.ntiles == 0) continue;
         if (!mbar_wait_bounded(bar_qfull, nblk & 1u, status)) { s_abort = 1; break; }
         ++nblk;
         for (int i = 0; i < bk.ntiles; ++i, ++it) {
@@ -246,8 +248,8 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
     uint32_t it = 0;
     for (int k = blockIdx.x; k < total; k += gridDim.x) {
       QBlock bk;
-      if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk)) continue;
-      if (tid == 0 && (bk.q0 + bk.nq) / r > max_vis) raise_status(status, CSA_ERR_DEVICE_BOUNDS);
+      if (!qblock_of(cu, cu_cmp, B, r, G, topk, max_vis, total, k, bk, pos0)) continue;
+      if (tid == 0 && (bk.q0 + bk.nq + bk.p0) / r > max_vis) raise_status(status, CSA_ERR_DEVICE_BOUNDS);
       TK_T0(tk_sc);
       if (bk.score) {
         if (tid < G * kHI) {
@@ -294,7 +296,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
       for (int q = 0; q < bk.nq; ++q) {
         const int t = bk.q0 + q;
         const int64_t orow = (int64_t)(bk.seq0 + t) * k_pad;
-        const int n = min((t + 1) / r, max_vis);
+        const int n = min((t + bk.p0 + 1) / r, max_vis);
         const int m = min(topk, n);
         const uint32_t* keys = sKey + (size_t)q * vstride;
         const bool all = n <= topk;
@@ -490,9 +492,11 @@ bool indexer_topk_tc_supported(int H_I, int d_I, int max_vis, bool fp32) {
 template <int G, int CW, bool kFp8>
 static cudaError_t launch_topk_tc_t(const void* qI, const float* qs, const void* w, const void* kI, const float* ks,
                                     const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r,
-                                    int topk, int k_pad, int32_t* idx, int* status, cudaStream_t stream) {
+                                    int topk, int k_pad, int32_t* idx, int* status, cudaStream_t stream,
+                                    const int32_t* pos0, int cmp_rows) {
   CUtensorMap mqi, mki;
-  const uint64_t n_cmp_rows = (uint64_t)(T_cap / r > 0 ? T_cap / r : 1);
+  const int rows_c = cmp_rows > T_cap / r ? cmp_rows : T_cap / r;  // rows of the compressed array
+  const uint64_t n_cmp_rows = (uint64_t)(rows_c > 0 ? rows_c : 1);
   if (kFp8) {
     if (!make_tmap_u8_sw64(&mqi, qI, (uint64_t)T_cap * kHI, kDI, G * kHI) ||
         !make_tmap_u8_sw64(&mki, kI, n_cmp_rows, kDI, kTK))
@@ -512,42 +516,44 @@ static cudaError_t launch_topk_tc_t(const void* qI, const float* qs, const void*
   const int slots = sms * TopkCfg<CW>::kCtasPerSm;
   const int grid = blocks < slots ? blocks : slots;
   kern<<<grid, TopkCfg<CW>::kThreads, smem, stream>>>(mqi, mki, static_cast<const __nv_bfloat16*>(w), qs, ks, cu,
-                                                      cu_cmp, B, r, topk, k_pad, max_vis, idx, status);
+                                                      cu_cmp, B, r, topk, k_pad, max_vis, idx, status, pos0);
   return cudaGetLastError();
 }
 
 template <bool kFp8>
 static cudaError_t launch_topk_tc_any(const void* qI, const float* qs, const void* w, const void* kI, const float* ks,
                                       const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r,
-                                      int topk, int k_pad, int32_t* idx, int* status, cudaStream_t stream) {
+                                      int topk, int k_pad, int32_t* idx, int* status, cudaStream_t stream,
+                                      const int32_t* pos0, int cmp_rows) {
   if (T_cap <= 0) return cudaSuccess;
   const TopkShape sh = topk_tc_shape(max_vis);
   if (sh.G == 4 && sh.CW == 8)
     return launch_topk_tc_t<4, 8, kFp8>(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status,
-                                        stream);
+                                        stream, pos0, cmp_rows);
   if (sh.G == 2 && sh.CW == 8)
     return launch_topk_tc_t<2, 8, kFp8>(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status,
-                                        stream);
+                                        stream, pos0, cmp_rows);
   if (sh.G == 4)
     return launch_topk_tc_t<4, 16, kFp8>(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx,
-                                         status, stream);
+                                         status, stream, pos0, cmp_rows);
   return launch_topk_tc_t<2, 16, kFp8>(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status,
-                                       stream);
+                                       stream, pos0, cmp_rows);
 }
 
 cudaError_t launch_indexer_topk_tc(const void* qI, const void* w, const void* kI, const int32_t* cu,
                                    const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r, int topk, int k_pad,
-                                   int32_t* idx, int* status, cudaStream_t stream) {
+                                   int32_t* idx, int* status, cudaStream_t stream, const int32_t* pos0,
+                                   int cmp_rows) {
   return launch_topk_tc_any<false>(qI, nullptr, w, kI, nullptr, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx,
-                                   status, stream);
+                                   status, stream, pos0, cmp_rows);
 }
 
 cudaError_t launch_indexer_topk_fp8(const uint8_t* qI, const float* qs, const void* w, const uint8_t* kI,
                                     const float* ks, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap,
                                     int max_vis, int r, int topk, int k_pad, int32_t* idx, int* status,
-                                    cudaStream_t stream) {
+                                    cudaStream_t stream, const int32_t* pos0, int cmp_rows) {
   return launch_topk_tc_any<true>(qI, qs, w, kI, ks, cu, cu_cmp, B, T_cap, max_vis, r, topk, k_pad, idx, status,
-                                  stream);
+                                  stream, pos0, cmp_rows);
 }
 
 }  // namespace csa

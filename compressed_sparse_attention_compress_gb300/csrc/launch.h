@@ -22,12 +22,14 @@ bool indexer_topk_supported(int H_I, int d_I, int max_vis, int k_pad, int in_byt
 cudaError_t launch_indexer_topk(const void* qI, const void* w, const void* kI, const int32_t* cu,
                                 const int32_t* cu_cmp, int B, int T_cap, int max_vis, int H_I,
                                 int d_I, int r, int topk, int k_pad, bool fp32, int32_t* idx,
-                                int* status, cudaStream_t stream);
+                                int* status, cudaStream_t stream, const int32_t* pos0 = nullptr,
+                                int cmp_rows = 0);
 
 bool indexer_topk_tc_supported(int H_I, int d_I, int max_vis, bool fp32);
 cudaError_t launch_indexer_topk_tc(const void* qI, const void* w, const void* kI, const int32_t* cu,
                                    const int32_t* cu_cmp, int B, int T_cap, int max_vis, int r, int topk, int k_pad,
-                                   int32_t* idx, int* status, cudaStream_t stream);
+                                   int32_t* idx, int* status, cudaStream_t stream, const int32_t* pos0 = nullptr,
+                                int cmp_rows = 0);
 
 // FP8 indexer: E4M3 quantisation and the tcgen05 scoring + top-k on codes.
 cudaError_t launch_quantize_fp8(const void* x, int64_t rows, int cols, bool fp32, uint8_t* codes, float* scales,
@@ -35,12 +37,14 @@ cudaError_t launch_quantize_fp8(const void* x, int64_t rows, int cols, bool fp32
 cudaError_t launch_indexer_topk_fp8(const uint8_t* qI, const float* qs, const void* w, const uint8_t* kI,
                                     const float* ks, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap,
                                     int max_vis, int r, int topk, int k_pad, int32_t* idx, int* status,
-                                    cudaStream_t stream);
+                                    cudaStream_t stream, const int32_t* pos0 = nullptr,
+                                int cmp_rows = 0);
 
 cudaError_t launch_indexer_topk_fp8_full(const uint8_t* qI, const float* qs, const void* w, const uint8_t* kI,
                                          const float* ks, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap,
                                          int max_vis, int r, int topk, int k_pad, int32_t* idx, int* status,
-                                         cudaStream_t stream);
+                                         cudaStream_t stream, const int32_t* pos0 = nullptr,
+                                int cmp_rows = 0);
 
 // Attention kinds.
 enum AttnKind { kAttnCSA = 0, kAttnHCA = 1, kAttnWindow = 2 };
@@ -62,6 +66,7 @@ struct AttnArgs {
   float* lse;
   float* lse_cmp;
   int* status;
+  const int32_t* pos0 = nullptr;  // optional [B]: position of each sequence's first row (context parallel)
 };
 cudaError_t launch_attention(AttnKind kind, const AttnArgs& a, bool fp32, cudaStream_t stream);
 bool attention_ws_supported(const AttnArgs& a, bool fp32);
@@ -97,6 +102,7 @@ struct AttnBwdArgs {
   float* dsink;
   float* delta;           // [T_cap, H] scratch: dout . out
   int* status;
+  const int32_t* pos0 = nullptr;
 };
 cudaError_t launch_attention_bwd(AttnKind kind, const AttnBwdArgs& a, bool fp32, cudaStream_t stream);
 bool attention_bwd_tc_supported(const AttnBwdArgs& a, bool fp32);
@@ -122,6 +128,8 @@ struct KLArgs {
   int* status;
   float* teacher_lse = nullptr;  // optional [T_cap, H]: per-head log normaliser of the teacher over C_t
   float* student_lse = nullptr;  // optional [T_cap]: log normaliser of the indexer logits over C_t
+  const int32_t* pos0 = nullptr;
+  int cmp_rows = 0;              // rows of the compressed arrays (0: T_cap / r)
 };
 cudaError_t launch_indexer_kl(const KLArgs& a, bool fp32, cudaStream_t stream);
 bool indexer_kl_dense_tc_supported(const KLArgs& a, bool fp32);
@@ -148,6 +156,7 @@ struct KLBwdArgs {
   void* dw;
   float* dkI;
   int* status;
+  const int32_t* pos0 = nullptr;
 };
 cudaError_t launch_indexer_kl_bwd(const KLBwdArgs& a, bool fp32, cudaStream_t stream);
 

@@ -94,6 +94,20 @@ csa_status_t csa_get_device_status(csa_handle_t handle, cudaStream_t stream, int
 csa_status_t csa_compressed_offsets(csa_handle_t handle, const int32_t* cu_seqlens, int B,
                                     int ratio, int32_t* cu_cmp, cudaStream_t stream);
 
+/* Position offsets for context-parallel layouts (§5 contiguous CP: a rank
+ * holds a contiguous range of each sequence's queries plus the raw rows just
+ * left of it, and all compressed rows of the sequence after the all-gather).
+ * pos0 [B] int32 (device; NULL restores the default 0) is the position, in
+ * its sequence, of the first packed row of each sequence segment: the query
+ * calls made with this handle afterwards (top-k, attention, KL and their
+ * backwards) see entry j of sequence b once r(j+1)-1 <= (row - cu[b]) + pos0[b],
+ * while the window stays within the packed rows.  cmp_rows: rows of the
+ * compressed arrays the caller passes from then on (they may exceed
+ * floor(T_cap / ratio) after an all-gather); max_seqlen must bound the
+ * positions, (row - cu[b]) + pos0[b] < max_seqlen.  The compressor is not
+ * affected.  Not thread-safe with concurrent calls on the same handle. */
+csa_status_t csa_set_position_offsets(csa_handle_t handle, const int32_t* pos0, int cmp_rows);
+
 /* Learned-score block compression (§4 reset list, §5.1 spans D_compress = 8 for
  * overlapping ratio 4 and 128 for ratio-128 HCA, §8.2 "C4/C128 compression",
  * §9 FP32 compressor positional parameter).
