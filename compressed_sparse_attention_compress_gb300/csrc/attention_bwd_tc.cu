@@ -96,6 +96,7 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
   __shared__ Meta s_meta[kStages];
   __shared__ int s_rows[kStages][kTK];
   __shared__ float s_lse2[kNH], s_D[kNH];
+  __shared__ float s_tr[kEpiWarps][32 * 33];    // epilogue: a 32 x 32 block, transposed for whole-row reductions
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -473,17 +474,27 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
         break;
       }
       tc::fence_after_sync();
-      float* dst = ((mt.flags & kCmp) ? dkv_cmp : dkv_raw) + (int64_t)(rr < 0 ? 0 : rr) * kDim;
+      // thread = key row in tensor memory; each 32-column block goes through shared
+      // memory so that one reduction instruction covers four whole 128-byte row
+      // segments (lane = (key, 16-byte chunk)) instead of 32 scattered rows
+      float* dstb = (mt.flags & kCmp) ? dkv_cmp : dkv_raw;
+      float* tb = s_tr[ew];
 #pragma unroll 1
       for (int c0 = 0; c0 < kDim; c0 += 32) {
         uint32_t v[32];
         tc::tmem_ld32_sync(tmem + lane_off + kColKV + bkv * 128 + c0, v);
-        if (rr >= 0) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            red_add_v4(dst + c0 + 4 * i, __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                       __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+        for (int i = 0; i < 32; ++i) tb[lane * 33 + i] = __uint_as_float(v[i]);
+        __syncwarp();
+        const int ch = lane & 7;
+#pragma unroll
+        for (int st4 = 0; st4 < 8; ++st4) {
+          const int kl = 4 * st4 + (lane >> 3);               // key within this warp's 32
+          const int rk = __shfl_sync(0xffffffffu, rr, kl);
+          const float* src = tb + kl * 33 + 4 * ch;
+          if (rk >= 0) red_add_v4(dstb + (int64_t)rk * kDim + c0 + 4 * ch, src[0], src[1], src[2], src[3]);
         }
+        __syncwarp();
       }
       tc::fence_before_sync();
       __syncwarp();
