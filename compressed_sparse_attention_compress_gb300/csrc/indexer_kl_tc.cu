@@ -30,6 +30,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "tcgen05.cuh"
+#include "kl_blocks.cuh"
 #include "tma.cuh"
 
 namespace csa {
@@ -85,39 +86,7 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-struct Block {
-  int b, q0, nq, seq0, cmp0, p0, nvis_max, ntiles;
-};
-
-// Blocks of kQB consecutive queries of one sequence, handed out heaviest
-// (latest in the buffer) first.  Block k counts from the end.
-__device__ __forceinline__ bool block_of(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_cmp, int B,
-                                         int r, int total, int k, Block& out, const int32_t* __restrict__ pos0) {
-  int c = total - 1 - k;
-  for (int bb = 0; bb < B; ++bb) {
-    const int L = max(0, __ldg(cu + bb + 1) - __ldg(cu + bb));
-    const int nb = (L + kQB - 1) / kQB;
-    if (c < nb) {
-      out.b = bb;
-      out.q0 = c * kQB;
-      out.nq = min(kQB, L - c * kQB);
-      out.seq0 = __ldg(cu + bb);
-      out.cmp0 = __ldg(cu_cmp + bb);
-      out.p0 = pos0 ? __ldg(pos0 + bb) : 0;  // position of the sequence's first row here
-      out.nvis_max = (out.q0 + out.nq + out.p0) / r;
-      out.ntiles = (out.nvis_max + kTK - 1) / kTK;
-      return true;
-    }
-    c -= nb;
-  }
-  return false;
-}
-
-__device__ __forceinline__ int total_blocks(const int32_t* __restrict__ cu, int B) {
-  int n = 0;
-  for (int bb = 0; bb < B; ++bb) n += (max(0, __ldg(cu + bb + 1) - __ldg(cu + bb)) + kQB - 1) / kQB;
-  return n;
-}
+using klb::Block;
 
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
@@ -178,7 +147,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
-  const int total = total_blocks(cu, B);
+  const int total = klb::total_blocks<kQB>(cu, B);
 
   if (warp == kComputeWarps) {
     // ---------------- TMA producer ----------------
@@ -190,7 +159,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
       uint32_t it = 0, nblk = 0;
       for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
         Block bk;
-        if (!block_of(cu, cu_cmp, B, r, total, k, bk, pos0) || bk.ntiles == 0) continue;
+        if (!klb::block_of<kQB, kTK>(cu, cu_cmp, B, r, total, k, bk, pos0) || bk.ntiles == 0) continue;
         if (!mbar_wait_bounded(bar_qempty, (nblk & 1u) ^ 1u, status)) { s_abort = 1; break; }
         ++nblk;
         mbar_arrive_expect_tx(bar_qfull, 2 * kQRegion + kQB * kHI * 128);
@@ -225,7 +194,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
       uint32_t it = 0, nblk = 0, p1 = 0, nf0 = 0, nf1 = 0;
       for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
         Block bk;
-        if (!block_of(cu, cu_cmp, B, r, total, k, bk, pos0) || bk.ntiles == 0) continue;
+        if (!klb::block_of<kQB, kTK>(cu, cu_cmp, B, r, total, k, bk, pos0) || bk.ntiles == 0) continue;
         if (!mbar_wait_bounded(bar_qfull, nblk & 1u, status)) { s_abort = 1; break; }
         ++nblk;
         for (int pass = 0; pass < 2; ++pass) {
@@ -290,7 +259,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
     uint32_t p1 = 0, nf0 = 0, nf1 = 0;       // score-buffer uses, as counted by the MMA warp
     for (int k = blockIdx.x; k < total; k += gridDim.x) {
       Block bk;
-      if (!block_of(cu, cu_cmp, B, r, total, k, bk, pos0)) continue;
+      if (!klb::block_of<kQB, kTK>(cu, cu_cmp, B, r, total, k, bk, pos0)) continue;
       if (bk.ntiles == 0) {
         if (tid < bk.nq) {
           kl_rows[bk.seq0 + bk.q0 + tid] = 0.f;

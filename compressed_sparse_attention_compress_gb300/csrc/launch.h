@@ -159,5 +159,9 @@ struct KLBwdArgs {
   const int32_t* pos0 = nullptr;
 };
 cudaError_t launch_indexer_kl_bwd(const KLBwdArgs& a, bool fp32, cudaStream_t stream);
+// tcgen05 one-pass backward of the dense teacher (64 x 128 heads, indexer 8 x 64,
+// bf16, both normalisers given); launch_indexer_kl_bwd dispatches to it.
+bool indexer_kl_bwd_tc_supported(const KLBwdArgs& a, bool fp32);
+cudaError_t launch_indexer_kl_bwd_tc(const KLBwdArgs& a, cudaStream_t stream);
 
 }  // namespace csa

@@ -37,7 +37,7 @@ def _close(name, got, ref, quant=0.0):
 
 
 def _run(lengths, mode, H=64, d=128, H_I=8, d_I=64, ratio=4, topk=96, k_pad=128, fp32=False, seed=0,
-         grad_scale=1.0, cap_align=64, rows=None, check_kI=True, stats=False):
+         grad_scale=1.0, cap_align=64, rows=None, check_kI=True, stats=False, check_stats=True):
     sparse = mode != "dense"
     a = I.generate_indexer_bwd(lengths, H, d, H_I, d_I, ratio, topk if sparse else 0, k_pad, seed, cap_align)
     cu_np = a["cu_seqlens"]
@@ -67,7 +67,8 @@ def _run(lengths, mode, H=64, d=128, H_I=8, d_I=64, ratio=4, topk=96, k_pad=128,
         api.csa_indexer_kl_ex(h, q, kc, qI, w, kI, cu, cu_cmp, ms, ratio, scale, kl_sum, ws, teacher_lse=teacher_lse,
                               student_lse=student_lse, idx=idx, lse_cmp=lse_cmp)
         torch.cuda.synchronize()
-        _check_stats(a, cu_np, ratio, scale, idx, teacher_lse, student_lse)
+        if check_stats:
+            _check_stats(a, cu_np, ratio, scale, idx, teacher_lse, student_lse)
         lse_cmp = teacher_lse
     dqI = torch.full_like(qI, 5.0)
     dw = torch.full_like(w, 5.0)
@@ -145,14 +146,24 @@ def test_head_counts(H, H_I):
     _run([517, 64], "sparse", H=H, H_I=H_I, topk=50, k_pad=64, seed=5, grad_scale=-3.0)
 
 
-def test_full_size_dense_warmup_layer_sampled():
-    # the dense teacher at L = 32768: dqI and dw on sampled rows against the
+@pytest.mark.parametrize("grad_scale", [1.0, -3.0])
+def test_one_pass_dense_tensor_core_path_ragged(grad_scale):
+    # the dense teacher with both forward normalisers at 64 x 128 heads and an
+    # 8 x 64 indexer runs the tcgen05 kernel: blocks of 4 queries, ragged ends,
+    # an empty sequence, prefixes of 1 to 9 tiles
+    _run([1029, 3, 0, 517, 130, 4600], "dense", stats=True, seed=6, grad_scale=grad_scale)
+
+
+@pytest.mark.parametrize("stats", [False, True])
+def test_full_size_dense_warmup_layer_sampled(stats):
+    # the dense teacher at L = 32768 (with the forward's normalisers: the
+    # one-pass tensor-core kernel): dqI and dw on sampled rows against the
     # oracle; dkI through the homogeneity identity sum kI.dkI = sum w.dw, which
     # holds for the whole tensors at any size
     L = 32768
     rng = np.random.default_rng(1)
     rows = np.sort(np.concatenate([rng.choice(L, 24, replace=False), [3, 4, 8191, L - 1]]))
-    res = _run([L], "dense", rows=rows, check_kI=False, cap_align=128)
+    res = _run([L], "dense", rows=rows, check_kI=False, cap_align=128, stats=stats, check_stats=False)
     f64 = lambda t: t.double()  # noqa: E731
     lhs = (f64(res["dkI"][:res["n_c"]]) * f64(res["kI"][:res["n_c"]])).sum()
     rhs = (f64(res["dw"]) * f64(res["w"])).sum()
