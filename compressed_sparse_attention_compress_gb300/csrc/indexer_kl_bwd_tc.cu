@@ -86,9 +86,19 @@ __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+__device__ __forceinline__ void red_add_v2(float* p, uint32_t a, uint32_t b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};\n" ::"l"(p), "f"(__uint_as_float(a)), "f"(__uint_as_float(b))
                : "memory");
+}
+
+// 16 lanes x 16 columns of tensor memory: thread t gets lanes t/4 and 8 + t/4,
+// columns 2 (t % 4) + {0, 1} and 8 + 2 (t % 4) + {0, 1} (the mma.sync
+// accumulator arrangement, two 8-column repetitions): four threads hold 32
+// contiguous bytes of a row, so each reduction below fills whole sectors.
+__device__ __forceinline__ void tmem_ld16x256_x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
 }
 
 __device__ __forceinline__ int rotated_tile(int ii, int rot, int ntiles) {
@@ -282,24 +292,33 @@ indexer_kl_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid
     const int rowl = quad * 32 + lane;       // tensor-memory lane: entry of the tile
     constexpr float kLog2e = 1.4426950408889634f;
     uint32_t t = 0, nblk = 0;
-    // the dkI epilogue of tile tp: this thread's 16 dims of entry row `rowg`
-    auto epilogue = [&](uint32_t tp, int64_t rowg, bool valid) -> bool {
+    // the dkI epilogue of tile tp: rows row0 + [0, nvalid) of the gradient,
+    // this warpgroup's 16 dims, this warp's 32 lanes as two 16-lane halves
+    auto epilogue = [&](uint32_t tp, int64_t row0, int nvalid) -> bool {
       const uint32_t buf = tp & 1u;
       const bool okw = mbar_wait_bounded(bar_kvfull + 8 * buf, (tp >> 1) & 1u, status);
       if (__any_sync(0xffffffffu, !okw)) return false;
       tc::fence_after_sync();
-      uint32_t v[16];
-      tc::tmem_ld16_sync(tmem + lane_off + kColKI + buf * kDI + q * 16, v);
+      uint32_t v[2][8];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        tmem_ld16x256_x2(tmem + ((uint32_t)(quad * 32 + hf * 16) << 16) + kColKI + buf * kDI + q * 16, v[hf]);
+      tc::tmem_wait_ld();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_kvfree + 8 * buf);
-      if (valid) {
-        float* dst = dkI + rowg * kDI + q * 16;
+      const int c = q * 16 + 2 * (lane & 3);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          red_add_v4(dst + 4 * i, __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-      }
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int rl = quad * 32 + hf * 16 + e * 8 + (lane >> 2);  // lane of the tile = entry
+          if (rl < nvalid) {
+            float* dst = dkI + (row0 + rl) * kDI + c;
+            red_add_v2(dst, v[hf][2 * e], v[hf][2 * e + 1]);
+            red_add_v2(dst + 8, v[hf][4 + 2 * e], v[hf][4 + 2 * e + 1]);
+          }
+        }
       return true;
     };
     for (int k = blockIdx.x; k < total; k += gridDim.x) {
@@ -326,41 +345,49 @@ indexer_kl_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid
 #pragma unroll
       for (int h = 0; h < kHI; ++h) dwa[h] = 0.f;
       bool fail = false;
-      int64_t prev_row = 0;
-      bool prev_valid = false;
+      int64_t prev_row0 = 0;
+      int prev_nvalid = 0;
       for (int ii = 0; ii < bk.ntiles; ++ii, ++t) {
-        const int j = rotated_tile(ii, rot, bk.ntiles) * kTK + rowl;  // entry index within the sequence
+        const int tj = rotated_tile(ii, rot, bk.ntiles) * kTK;
+        const int j = tj + rowl;  // entry index within the sequence
         bool okw = mbar_wait_bounded(bar_sfull, t & 1u, status);
         if (__any_sync(0xffffffffu, !okw)) { fail = true; break; }
         tc::fence_after_sync();
-        float x[kNH];
+        // the scores in two 32-head halves (the second read before the first is
+        // used would need 64 registers per thread)
         uint32_t ri[kHI];
-#pragma unroll
-        for (int c0 = 0; c0 < kNH; c0 += 32) {
-          uint32_t rs[32];
-          tc::tmem_ld32_sync(tmem + lane_off + kColS + q * kNH + c0, rs);
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) x[c0 + jj] = __uint_as_float(rs[jj]);
-        }
+        uint32_t xs[32];
         tc::tmem_ld8_sync(tmem + lane_off + kColI + q * kHI, ri);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfree);
-        float g = 0.f;
-        if (q_ok && j < nvis_q) {
-          // teacher p(j): the mean over heads of exp2(s scale log2e - lse_h log2e)
-          const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
-          uint64_t pa = f2_pack(0.f, 0.f), pb = pa;
-          const float4* L4 = reinterpret_cast<const float4*>(&s_L[q][0]);
+        tc::tmem_ld32_sync(tmem + lane_off + kColS + q * kNH, xs);
+        const bool live = q_ok && j < nvis_q;
+        const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+        uint64_t pa = f2_pack(0.f, 0.f), pb = pa;
+        const float4* L4 = reinterpret_cast<const float4*>(&s_L[q][0]);
 #pragma unroll
-          for (int h4 = 0; h4 < kNH / 4; ++h4) {
-            const float4 L = L4[h4];
-            float a0, a1, a2, a3;
-            f2_unpack(f2_fma(f2_pack(x[4 * h4 + 0], x[4 * h4 + 1]), sc2, f2_pack(L.x, L.y)), a0, a1);
-            f2_unpack(f2_fma(f2_pack(x[4 * h4 + 2], x[4 * h4 + 3]), sc2, f2_pack(L.z, L.w)), a2, a3);
-            pa = f2_add(pa, f2_pack(ex2(a0), ex2(a1)));
-            pb = f2_add(pb, f2_pack(ex2(a2), ex2(a3)));
+        for (int hh = 0; hh < 2; ++hh) {
+          if (hh == 1) {
+            tc::tmem_ld32_sync(tmem + lane_off + kColS + q * kNH + 32, xs);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_sfree);
           }
+          if (live) {
+            // teacher p(j): the mean over heads of exp2(s scale log2e - lse_h log2e)
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+              const float4 L = L4[hh * 8 + h4];
+              float a0, a1, a2, a3;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(xs[4 * h4 + 0]), __uint_as_float(xs[4 * h4 + 1])), sc2,
+                               f2_pack(L.x, L.y)), a0, a1);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(xs[4 * h4 + 2]), __uint_as_float(xs[4 * h4 + 3])), sc2,
+                               f2_pack(L.z, L.w)), a2, a3);
+              pa = f2_add(pa, f2_pack(ex2(a0), ex2(a1)));
+              pb = f2_add(pb, f2_pack(ex2(a2), ex2(a3)));
+            }
+          }
+        }
+        float g = 0.f;
+        if (live) {
           float p0, p1, p2, p3;
           f2_unpack(pa, p0, p1);
           f2_unpack(pb, p2, p3);
@@ -389,11 +416,11 @@ indexer_kl_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_cfull);
-        if (ii > 0 && !epilogue(t - 1, prev_row, prev_valid)) { fail = true; break; }
-        prev_row = (int64_t)bk.cmp0 + j;
-        prev_valid = j < bk.nvis_max;
+        if (ii > 0 && !epilogue(t - 1, prev_row0, prev_nvalid)) { fail = true; break; }
+        prev_row0 = (int64_t)bk.cmp0 + tj;
+        prev_nvalid = bk.nvis_max - tj;
       }
-      if (!fail && !epilogue(t - 1, prev_row, prev_valid)) fail = true;
+      if (!fail && !epilogue(t - 1, prev_row0, prev_nvalid)) fail = true;
       // dw: the per-entry partials summed over the warpgroup's 128 threads
 #pragma unroll
       for (int h = 0; h < kHI; ++h) {
