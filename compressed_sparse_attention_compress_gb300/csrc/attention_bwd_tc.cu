@@ -27,8 +27,9 @@
 //     the previous scores are read; dQ^T and dKV once P^T / dS^T are written;
 //   softmax (8 warps, thread = (key, 32 heads)): P = exp2(S scale log2e - lse),
 //     scale dS, the two bf16 tiles; at the end of a query dQ^T -> dq;
-//   epilogue (4 warps, thread = key row): each dKV tile added to the float32
-//     gradient rows with red.global.add.v4 while the next tile is computed.
+//   epilogue (4 warps): each dKV tile added to the float32 gradient rows with
+//     red.global.add.v2, four threads per 32-byte row piece (the 16x256b
+//     tensor-memory read), while the next tile is computed.
 // Every wait is bounded (CSA_ERR_DEVICE_TIMEOUT and a uniform abort).
 #include <math.h>
 
@@ -73,9 +74,19 @@ struct Meta {
   int flags;
 };
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+__device__ __forceinline__ void red_add_v2(float* p, uint32_t a, uint32_t b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};\n" ::"l"(p), "f"(__uint_as_float(a)), "f"(__uint_as_float(b))
                : "memory");
+}
+
+// 16 lanes x 16 columns of tensor memory: thread t gets lanes t/4 and 8 + t/4,
+// columns 2 (t % 4) + {0, 1} and 8 + 2 (t % 4) + {0, 1} (the mma.sync
+// accumulator arrangement, two 8-column repetitions): four threads hold 32
+// contiguous bytes of a row, so each reduction fills whole sectors.
+__device__ __forceinline__ void tmem_ld16x256_x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
 }
 
 }  // namespace
@@ -96,7 +107,6 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
   __shared__ Meta s_meta[kStages];
   __shared__ int s_rows[kStages][kTK];
   __shared__ float s_lse2[kNH], s_D[kNH];
-  __shared__ float s_tr[kEpiWarps][32 * 33];    // epilogue: a 32 x 32 block, transposed for whole-row reductions
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -474,27 +484,32 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
         break;
       }
       tc::fence_after_sync();
-      // thread = key row in tensor memory; each 32-column block goes through shared
-      // memory so that one reduction instruction covers four whole 128-byte row
-      // segments (lane = (key, 16-byte chunk)) instead of 32 scattered rows
+      // the warp's 32 key rows as two 16-lane halves: thread = (two keys, two
+      // 8-byte column pairs per 16 columns); four threads cover 32 contiguous
+      // bytes of a gradient row, so each reduction instruction fills 8 sectors
       float* dstb = (mt.flags & kCmp) ? dkv_cmp : dkv_raw;
-      float* tb = s_tr[ew];
+      int rk[2][2];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) rk[hf][e] = __shfl_sync(0xffffffffu, rr, hf * 16 + e * 8 + (lane >> 2));
+      const int cc = 2 * (lane & 3);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kDim; c0 += 32) {
-        uint32_t v[32];
-        tc::tmem_ld32_sync(tmem + lane_off + kColKV + bkv * 128 + c0, v);
+      for (int c0 = 0; c0 < kDim; c0 += 16) {
+        uint32_t v[2][8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) tb[lane * 33 + i] = __uint_as_float(v[i]);
-        __syncwarp();
-        const int ch = lane & 7;
+        for (int hf = 0; hf < 2; ++hf)
+          tmem_ld16x256_x2(tmem + ((uint32_t)(ew * 32 + hf * 16) << 16) + kColKV + bkv * 128 + c0, v[hf]);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int st4 = 0; st4 < 8; ++st4) {
-          const int kl = 4 * st4 + (lane >> 3);               // key within this warp's 32
-          const int rk = __shfl_sync(0xffffffffu, rr, kl);
-          const float* src = tb + kl * 33 + 4 * ch;
-          if (rk >= 0) red_add_v4(dstb + (int64_t)rk * kDim + c0 + 4 * ch, src[0], src[1], src[2], src[3]);
-        }
-        __syncwarp();
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (rk[hf][e] >= 0) {
+              float* dst = dstb + (int64_t)rk[hf][e] * kDim + c0 + cc;
+              red_add_v2(dst, v[hf][2 * e], v[hf][2 * e + 1]);
+              red_add_v2(dst + 8, v[hf][4 + 2 * e], v[hf][4 + 2 * e + 1]);
+            }
       }
       tc::fence_before_sync();
       __syncwarp();
