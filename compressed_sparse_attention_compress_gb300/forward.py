@@ -192,24 +192,35 @@ class Forward:
     _STAGE_INPUTS = (("cu_seqlens", "x_kv", "z_kv", "P_kv", "x_I", "z_I", "P_I", "v", "x_kv_prev", "z_kv_prev",
                       "x_I_prev", "z_I_prev", "g_kv", "g_I"), ("qI", "w"), ("q",))
 
+    attend_chunks = 4   # run_from_host: selected attention in up to this many row chunks
+
     def run_from_host(self, host: dict, stream=None, copy_stream=None):
         """The forward with its inputs still in (pinned) host memory.
 
         The inputs are copied into this object's device buffers on
         ``copy_stream`` in the order the stages need them, and each stage
-        waits only for its own inputs, so the 537 MB of queries at the headline
-        size arrive while the compressor and the top-k run.  The previous
-        forward on ``stream`` must be done with the buffers before they are
-        overwritten: the copy stream waits for it first.
+        waits only for its own inputs: the compressor's and the indexer's
+        inputs first, then the queries (537 MB at the 32K layer) in row
+        chunks, last rows first.  The selected attention runs chunk by chunk
+        as the queries arrive (``_attention_chunks``); the KL loss, which
+        needs all of them, follows.  The previous forward on ``stream`` must
+        be done with the buffers before they are overwritten: the copy stream
+        waits for it first.
         """
         main = stream if stream is not None else torch.cuda.current_stream()
         cs = copy_stream if copy_stream is not None else self._copy_stream()
         cs.wait_stream(main)
+        chunks = self._attention_chunks()
         ready = []
         with torch.cuda.stream(cs):
-            for names in self._STAGE_INPUTS:
+            for si, names in enumerate(self._STAGE_INPUTS):
+                if si == 2 and chunks:   # the queries, chunk by chunk (each row once)
+                    for c in chunks:
+                        self.x["q"][c["copy"][0]:c["copy"][1]].copy_(host["q"][c["copy"][0]:c["copy"][1]],
+                                                                    non_blocking=True)
+                        c["ready"].record(cs)
                 for k in names:
-                    if k in host and k in self.x:
+                    if k in host and k in self.x and not (si == 2 and chunks):
                         self.x[k].copy_(host[k], non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(cs)
@@ -222,15 +233,94 @@ class Forward:
                     main.wait_event(ready[1])
                     self.topk(main)
             main.wait_event(ready[1])
+            if chunks:
+                for c in chunks:
+                    main.wait_event(c["ready"])
+                    self._attend_rows(c, main)
+            else:
+                main.wait_event(ready[2])
+                self.attend(main)
             main.wait_event(ready[2])
-            self.attend(main)
             if self.wl.kl_mode != "none":
                 self.kl(main)
+
+    def _attention_chunks(self):
+        """Row chunks of the selected attention for ``run_from_host``, last first.
+
+        Chunk k owns the packed rows [a_k, a_{k+1}) (the last one up to T_cap,
+        so it also writes the capacity rows).  Its call sees the rows
+        [lo_k, a_{k+1}) with lo_k up to W rows earlier inside a_k's sequence:
+        the raw rows of its first queries' windows.  That view is a packing of
+        its own -- one segment per sequence, each with the position of its
+        first row (csa_set_position_offsets), the global compressed offsets and
+        the global top-k rows -- so its queries see exactly what they see in
+        the whole call ("DeepSeek-V4 Attention Training Systems" §5: the
+        contiguous context-parallel layout with a boundary of W raw rows).  The
+        rows [lo_k, a_k) are computed again with a truncated window; the chunks
+        run last to first, so their owner (the next chunk run) writes them
+        after.  Queries are copied as [lo_k, lo_{k+1}): each row once, before
+        the first chunk that reads it.  Empty when chunking does not apply."""
+        wl = self.wl
+        if getattr(self, "_chunks", None) is not None:
+            return self._chunks
+        self._chunks = []
+        if wl.ratio <= 0 or wl.H_I <= 0 or wl.separate_v or wl.k_pad % 4 != 0:
+            return self._chunks
+        cu = [int(v) for v in self.cu.cpu().tolist()]
+        for c in attention_chunk_plan(cu, wl.T_cap, wl.window, int(self.attend_chunks)):
+            self._chunks.append(dict(
+                lo=c["lo"], hi=c["hi"], copy=c["copy"], max_len=c["max_len"],
+                cu=torch.tensor(c["cu"], dtype=torch.int32, device=self.dev),
+                pos0=torch.tensor(c["pos0"], dtype=torch.int32, device=self.dev),
+                ready=torch.cuda.Event()))
+        return self._chunks
+
+    def _attend_rows(self, c, stream):
+        """The selected attention of one chunk of ``_attention_chunks``."""
+        wl, x = self.wl, self.x
+        lo, hi = c["lo"], c["hi"]
+        self.h.set_position_offsets(c["pos0"], self.kv_cmp.shape[0])
+        try:
+            api.csa_sparse_attn_fwd(self.h, x["q"][lo:hi], self.kv_cmp, x["x_kv"][lo:hi], self.idx[lo:hi], c["cu"],
+                                    self.cu_cmp, c["max_len"], wl.ratio, wl.window, self.scale, self.out[lo:hi],
+                                    self.lse[lo:hi], self.lse_cmp[lo:hi], stream=stream)
+        finally:
+            self.h.set_position_offsets(None)
 
     def _copy_stream(self):
         if getattr(self, "_cs", None) is None:
             self._cs = torch.cuda.Stream(device=self.dev)
         return self._cs
+
+
+def attention_chunk_plan(cu: list, T_cap: int, W: int, n: int) -> list:
+    """Host plan of ``Forward._attention_chunks``, in the order the chunks run
+    (last rows first).  ``cu``: the packing's offsets [B + 1].  Each chunk:
+    ``lo``, ``hi`` (the rows its call sees), ``own`` (the rows whose outputs it
+    leaves in place), ``copy`` (the query rows copied for
+    it), ``cu`` (its own packing, one segment per sequence), ``pos0`` (each
+    segment's first position in its sequence) and ``max_len``.  Chunk starts
+    are multiples of 16 rows; fewer than 8 W rows per chunk: no chunks."""
+    T = cu[-1]
+    B = len(cu) - 1
+    if n < 2 or T < n * 8 * max(W, 16):
+        return []
+    a = [((T * k) // n) // 16 * 16 for k in range(n)] + [T_cap]
+    los = [0]
+    for k in range(1, n):
+        b0 = max(b for b in range(B) if cu[b] <= a[k])   # the sequence holding row a_k
+        los.append(max(cu[b0], a[k] - W))
+    plan = []
+    for k in reversed(range(n)):
+        lo, hi = los[k], a[k + 1]
+        seg = [max(0, min(hi, cu[b + 1]) - max(lo, cu[b])) for b in range(B)]
+        cu_l = [0]
+        for L in seg:
+            cu_l.append(cu_l[-1] + L)
+        plan.append(dict(lo=lo, hi=hi, own=(a[k], hi), copy=(los[k], los[k + 1] if k + 1 < n else T_cap), cu=cu_l,
+                         pos0=[max(lo, cu[b]) - cu[b] if seg[b] > 0 else 0 for b in range(B)],
+                         max_len=max(seg + [1])))
+    return plan
 
 
 def to_device(arrs: dict, io_fp32: bool, device: int = 0) -> dict:
