@@ -265,7 +265,8 @@ def run_ours(args, wl):
         # inputs copied in stage order on a side stream; each stage waits for its own
         f.run_from_host(host, stream)
         if dout_host is not None:
-            dout.copy_(dout_host, non_blocking=True)
+            # the upstream gradient follows the queries on the copy stream, under the forward
+            stream.wait_event(f.copy_from_host(dout, dout_host))
             f.backward(dout, stream)
             if wl.kl_mode != "none":
                 f.indexer_backward(stream=stream)
@@ -349,8 +350,7 @@ def run_ours(args, wl):
                          / peaks["bf16_tflops_sustained"]} if args.backward and wl.kl_mode != "none" else None),
         "e2e": {"value": ws * wl.T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * (f_launches(wl) + ((2 + (1 if wl.kl_mode != "none" else 0))
-                                                        if args.backward else 0)),
+        "gpu_launches": args.steps * (f_launches(wl) + (b_launches(wl) if args.backward else 0)),
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and ws >= 1:
@@ -376,6 +376,14 @@ def f_launches(wl) -> int:
                     and wl.H_I == 8 and wl.d_I == 64)
         n += 3 if dense_tc else 2                                               # (zero) + KL + finalize
     return n
+
+
+def b_launches(wl) -> int:
+    """Kernels of ours launched per backward step (mirrors the dispatch in csrc/):
+    attention backward = delta + (tcgen05: capacity rows + kernel | warp-level kernel),
+    indexer backward = one kernel (its zero fills are memsets)."""
+    tc = not wl.io_fp32 and wl.H == 64 and wl.d == 128 and not wl.separate_v
+    return (3 if tc else 2) + (1 if wl.kl_mode != "none" else 0)
 
 
 def _traffic(kernel: str, workload: str):

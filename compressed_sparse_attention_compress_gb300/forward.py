@@ -287,6 +287,19 @@ class Forward:
         finally:
             self.h.set_position_offsets(None)
 
+    def copy_from_host(self, dst, src):
+        """Queue a host-to-device copy on the copy stream, behind the inputs
+        ``run_from_host`` queued there (so it overlaps the forward's compute),
+        and return the event a consumer waits for.  An upstream gradient for
+        ``backward`` is the use: the next ``run_from_host`` waits for the
+        stream it was given before the copy stream rewrites anything."""
+        cs = self._copy_stream()
+        with torch.cuda.stream(cs):
+            dst.copy_(src, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(cs)
+        return ev
+
     def _copy_stream(self):
         if getattr(self, "_cs", None) is None:
             self._cs = torch.cuda.Stream(device=self.dev)
