@@ -25,8 +25,9 @@
 // of dqI^T.  dqI^T accumulates in tensor memory over the block; each dkI tile
 // (two tensor-memory buffers) is added to the float32 gradient rows with
 // red.global.add by the compute threads while the next tile's scores run.
-// Each block visits its tiles in a rotated order so that concurrent blocks add
-// to different rows.
+// Each block visits its tiles in an order rotated by its position, so that
+// concurrent blocks add to different rows while a query's gradients stay
+// independent of how the rows are packed or split.
 // Warps 0-15 compute (warpgroup = query, thread = entry of the tile), warp 16
 // issues the TMA loads, warp 17 allocates tensor memory and issues the MMAs.
 // Every wait is bounded (CSA_ERR_DEVICE_TIMEOUT and a uniform abort).
@@ -197,7 +198,7 @@ indexer_kl_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid
             tma_load_2d(base + kQOff + rg * kQRegion + m * 16384, &map_q, rg * 64, (bk.seq0 + bk.q0) * kNH + m * 128,
                         bar_qfull);
         tma_load_2d(base + kQIOff, &map_qi, 0, (bk.seq0 + bk.q0) * kHI, bar_qfull);
-        const int rot = k % bk.ntiles;
+        const int rot = ((bk.q0 + bk.p0) / kQB) % bk.ntiles;  // by position: results do not depend on the packing
         for (int ii = 0; ii < bk.ntiles; ++ii, ++t) {
           const int row = bk.cmp0 + rotated_tile(ii, rot, bk.ntiles) * kTK;
           const uint32_t sk = t % kKStages, si = t % kIStages;
@@ -340,7 +341,7 @@ indexer_kl_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid
       const int nvis_q = (bk.q0 + q + bk.p0 + 1) / r;
       const bool q_ok = q < bk.nq && isfinite(s_lseI[q]);
       const float lseI = s_lseI[q];
-      const int rot = k % bk.ntiles;
+      const int rot = ((bk.q0 + bk.p0) / kQB) % bk.ntiles;  // by position: results do not depend on the packing
       float dwa[kHI];
 #pragma unroll
       for (int h = 0; h < kHI; ++h) dwa[h] = 0.f;
