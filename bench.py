@@ -155,7 +155,7 @@ def cpu_baseline(wl, arrs, seconds_target=15.0, max_rows=None):
     # rate: sampled rows through the per-query steps + the sample's share of compression
     total = dt + t_comp * len(rows) / wl.T
     return {"value": len(rows) / total, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{len(rows)} query rows strided over the {wl.T}-token workload (every {stride}th), "
+            "sample": f"{len(rows)} query rows strided over the {wl.T}-token workload (one in every {stride}), "
                       f"plus the rows' share of the full-sequence compression; fp64 C oracle, OpenMP"}
 
 

@@ -168,3 +168,15 @@ def test_full_size_dense_warmup_layer_sampled(stats):
     lhs = (f64(res["dkI"][:res["n_c"]]) * f64(res["kI"][:res["n_c"]])).sum()
     rhs = (f64(res["dw"]) * f64(res["w"])).sum()
     assert abs(float(lhs - rhs)) <= 2e-2 * max(1e-3, float((f64(res["dw"]).abs() * f64(res["w"]).abs()).sum()))
+
+
+def test_one_pass_dense_tensor_core_path_tiny_sequences():
+    # many sequences of 0-9 tokens (blocks of 1-4 queries, prefixes of 0-2
+    # entries: empty blocks, partial tiles) around one of three tiles
+    _run([1, 2, 3, 4, 5, 0, 6, 7, 8, 9, 1500, 3, 4, 2], "dense", stats=True, seed=8)
+
+
+def test_one_pass_dense_tensor_core_path_zero_upstream_gradient():
+    res = _run([900, 77], "dense", stats=True, seed=2, grad_scale=0.0)
+    for k in ("dqI", "dw", "dkI"):
+        assert not bool(res[k].float().abs().sum()), k
