@@ -205,7 +205,8 @@ class Forward:
         as the queries arrive (``_attention_chunks``); the KL loss, which
         needs all of them, follows.  The previous forward on ``stream`` must
         be done with the buffers before they are overwritten: the copy stream
-        waits for it first.
+        waits for it first.  ``host`` holds this workload's inputs (the same
+        packing as ``wl``; the chunks are planned from it).
         """
         main = stream if stream is not None else torch.cuda.current_stream()
         cs = copy_stream if copy_stream is not None else self._copy_stream()
@@ -266,7 +267,7 @@ class Forward:
         self._chunks = []
         if wl.ratio <= 0 or wl.H_I <= 0 or wl.separate_v or wl.k_pad % 4 != 0:
             return self._chunks
-        cu = [int(v) for v in self.cu.cpu().tolist()]
+        cu = [int(v) for v in wl.cu_seqlens]   # the workload's packing: no device read
         for c in attention_chunk_plan(cu, wl.T_cap, wl.window, int(self.attend_chunks)):
             self._chunks.append(dict(
                 lo=c["lo"], hi=c["hi"], copy=c["copy"], max_len=c["max_len"],
