@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import dataclasses
+import datetime
 import json
 import os
 import statistics
@@ -56,28 +57,46 @@ def _dist():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks / throttle reasons, sampled every 20 ms from before the
+    warm-up on; each sample carries nvidia-smi's timestamp, and the summary keeps
+    the samples inside the marked timed regions."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.windows = []
+        self.lines = []
+        self.t_start = time.time()
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        self.t_start = time.time()
         return self
 
-    def __exit__(self, *a):
-        self.lines = []
+    def settle(self, seconds: float = 0.5):
+        """Give nvidia-smi time to start sampling before a timed region."""
+        left = seconds - (time.time() - self.t_start)
+        if self.proc is not None and left > 0:
+            time.sleep(left)
+
+    @staticmethod
+    def now():
+        return datetime.datetime.now()
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -90,16 +109,21 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        slack = datetime.timedelta(milliseconds=20)
+        for l in self.lines:
             parts = [p.strip() for p in l.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                clk, cmax = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[3:7]):
+            if not any(a - slack <= ts <= b + slack for a, b in self.windows):
+                continue
+            sm.append(clk)
+            mx.append(cmax)
+            for n, v in zip(names, parts[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
@@ -223,21 +247,24 @@ def run_ours(args, wl):
         if wl.kl_mode != "none":
             stages.append(("indexer_bwd", f.indexer_backward))
 
+    clk = ClockSampler(local).start()   # sampling from before the warm-up; samples kept per timed region
     for _ in range(max(args.warmup, 3)):
         f.run()
     torch.cuda.synchronize()
     assert f.h.device_status() == 0, "device status raised during warm-up"
+    clk.settle()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        for s in range(args.steps):
-            ev[s][0].record(stream)
-            for i, (_, fn) in enumerate(stages):
-                fn()
-                ev[s][i + 1].record(stream)
-        torch.cuda.synchronize()
+    t_dev0 = clk.now()
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        for i, (_, fn) in enumerate(stages):
+            fn()
+            ev[s][i + 1].record(stream)
+    torch.cuda.synchronize()
+    clk.mark(t_dev0, clk.now())
     barrier()
     total_ms = sum(ev[s][0].elapsed_time(ev[s][-1]) for s in range(args.steps))
     stage_ms = {name: sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)) / args.steps
@@ -277,11 +304,15 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
+    torch.cuda.synchronize()
+    t_e2e0 = clk.now()
     e0.record(stream)
     for _ in range(args.steps):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
+    clk.mark(t_e2e0, clk.now())
+    clk.stop()
     e2e_ms = e0.elapsed_time(e1) / args.steps
     if ws > 1:
         t = torch.tensor([e2e_ms], device="cuda")
