@@ -104,6 +104,7 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_kvfull[2], s_kvfree[2];
   __shared__ __align__(8) uint64_t s_qfull, s_qempty, s_sfull, s_sfree, s_pfull, s_pfree, s_dqdone, s_dqfree;
+  __shared__ __align__(8) uint64_t s_drain;  // the MMA thread's last commit, before tensor memory is freed
   __shared__ Meta s_meta[kStages];
   __shared__ int s_rows[kStages][kTK];
   __shared__ float s_lse2[kNH], s_D[kNH];
@@ -135,6 +136,7 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
     mbar_init(smem_u32(&s_pfree), 1);
     mbar_init(smem_u32(&s_dqdone), 1);
     mbar_init(smem_u32(&s_dqfree), kSoftWarps);
+    mbar_init(smem_u32(&s_drain), 1);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -368,6 +370,9 @@ attention_bwd_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __n
           else __nanosleep(64);
         }
       }
+      // every MMA this thread issued has completed before tensor memory is freed (also after an abort)
+      tc::mma_commit(smem_u32(&s_drain));
+      mbar_wait_bounded(smem_u32(&s_drain), 0, status);
     }
   } else if (warp < kSoftWarps) {
     // =================== softmax: warp = (head half, lane quadrant), thread = (key, 32 heads) ===================

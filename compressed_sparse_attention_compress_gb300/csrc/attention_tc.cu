@@ -103,7 +103,7 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
   using L = Layout<SEPV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t s_bar[2];  // 0: S ready, 1: O (PV) done
+  __shared__ __align__(8) uint64_t s_bar[3];  // 0: S ready, 1: O (PV) done, 2: the issuer's last commit
   __shared__ int s_rows[2][kTK];
   __shared__ __align__(16) float s_m[kNH];
   __shared__ float s_alpha[kNH], s_inv[kNH];
@@ -121,6 +121,7 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
   if (tid == 0) {
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
+    mbar_init(smem_u32(&s_bar[2]), 1);
     fence_mbar_init();
   }
   tc::fence_before_sync();
@@ -434,8 +435,12 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
     __syncthreads();
   }
 
-  // leave no copy in flight and give the tensor memory back
+  // leave no copy or MMA in flight and give the tensor memory back
   cp_async_wait<0>();
+  if (tid == 0) {  // thread 0 issued every MMA: their completion, also after an abort
+    tc::mma_commit(smem_u32(&s_bar[2]));
+    mbar_wait_bounded(smem_u32(&s_bar[2]), 0, status);
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();

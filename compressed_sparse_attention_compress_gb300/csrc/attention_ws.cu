@@ -126,6 +126,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[2][2], s_empty[2][2];
+  __shared__ __align__(8) uint64_t s_drain[2];  // each MMA thread's last commit, before tensor memory is freed
   __shared__ __align__(8) uint64_t s_qfull[2], s_qempty[2], s_sfull[2], s_sfree[2], s_pfull[2], s_odone[2],
       s_ofree[2];
   __shared__ Meta s_meta[2][2];
@@ -167,6 +168,8 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       mbar_init(smem_u32(&s_odone[g]), 1);
       mbar_init(smem_u32(&s_ofree[g]), kSoftWarps);
     }
+    mbar_init(smem_u32(&s_drain[0]), 1);
+    mbar_init(smem_u32(&s_drain[1]), 1);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -398,6 +401,9 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
           }
         }
       }
+      // every MMA this thread issued has completed before tensor memory is freed (also after an abort)
+      tc::mma_commit(smem_u32(&s_drain[g]));
+      mbar_wait_bounded(smem_u32(&s_drain[g]), 0, status);
     }
   } else {
     // =================== softmax: group g, warp sw = (head half, lane quadrant) ===================

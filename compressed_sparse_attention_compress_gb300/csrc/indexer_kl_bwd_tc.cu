@@ -122,6 +122,7 @@ indexer_kl_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid
   __shared__ __align__(8) uint64_t s_kfull[kKStages], s_kempty[kKStages], s_ifull[kIStages], s_iempty[kIStages];
   __shared__ __align__(8) uint64_t s_sfull, s_sfree, s_cfull, s_cfree, s_kvfull[2], s_kvfree[2];
   __shared__ __align__(8) uint64_t s_qfull, s_qempty, s_dqdone, s_dqfree;
+  __shared__ __align__(8) uint64_t s_drain;  // the MMA thread's last commit, before tensor memory is freed
   __shared__ __align__(16) float s_L[kQB][kNH];  // per (query, head): minus the teacher lse, log2 units
   __shared__ float s_w[kQB][kHI];
   __shared__ float s_lseI[kQB];
@@ -163,6 +164,7 @@ indexer_kl_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid
     mbar_init(bar_qempty, 1);
     mbar_init(bar_dqdone, 1);
     mbar_init(bar_dqfree, 2);  // the two warps that read dqI^T
+    mbar_init(smem_u32(&s_drain), 1);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -284,6 +286,9 @@ indexer_kl_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid
         ++nblk;
       }
       if (!ok) *abort_flag = 1;
+      // every MMA this thread issued has completed before tensor memory is freed (also after an abort)
+      tc::mma_commit(smem_u32(&s_drain));
+      mbar_wait_bounded(smem_u32(&s_drain), 0, status);
     }
   } else {
     // ---------------- compute: warpgroup q = query, thread = entry of the tile ----------------

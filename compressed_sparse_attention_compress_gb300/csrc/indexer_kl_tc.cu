@@ -106,6 +106,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
   __shared__ __align__(8) uint64_t s_sfull[2], s_sfree[2], s_qfull, s_qempty;
+  __shared__ __align__(8) uint64_t s_drain;  // the MMA thread's last commit, before tensor memory is freed
   __shared__ __align__(16) float s_L[kQB][kNH];  // per (query, head) minus the log2 normaliser over C_t
   __shared__ float s_w[kQB][kHI];
   __shared__ float s_red[kComputeWarps][4];  // per compute warp: A, B, mI, lI
@@ -140,6 +141,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
     }
     mbar_init(bar_qfull, 1);
     mbar_init(bar_qempty, 1);
+    mbar_init(smem_u32(&s_drain), 1);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -249,6 +251,9 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         }
         tc::mma_commit(bar_qempty);  // Q / qI free once this block's MMAs are done
       }
+      // every MMA this thread issued has completed before tensor memory is freed (also after an abort)
+      tc::mma_commit(smem_u32(&s_drain));
+      mbar_wait_bounded(smem_u32(&s_drain), 0, status);
     }
   } else {
     // ---------------- compute warpgroups ----------------

@@ -139,6 +139,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_dfull[2], s_dfree[2];
   __shared__ __align__(8) uint64_t s_qfull, s_qempty;
+  __shared__ __align__(8) uint64_t s_drain;  // the MMA thread's last commit, before tensor memory is freed
   __shared__ float s_w[G][kHI];
   __shared__ uint32_t s_hist[kBins];
   __shared__ int s_scan[kComputeWarps];
@@ -170,6 +171,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
     }
     mbar_init(bar_qfull, 1);
     mbar_init(bar_qempty, 1);
+    mbar_init(smem_u32(&s_drain), 1);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -239,6 +241,9 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
         }
         tc::mma_commit(bar_qempty);
       }
+      // every MMA this thread issued has completed before tensor memory is freed (also after an abort)
+      tc::mma_commit(smem_u32(&s_drain));
+      mbar_wait_bounded(smem_u32(&s_drain), 0, status);
     }
   } else {
     // ---------------- compute warps: scores, then selection ----------------
