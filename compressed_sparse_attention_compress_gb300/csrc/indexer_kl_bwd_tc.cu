@@ -92,16 +92,6 @@ __device__ __forceinline__ void red_add_v2(float* p, uint32_t a, uint32_t b) {
                : "memory");
 }
 
-// 16 lanes x 16 columns of tensor memory: thread t gets lanes t/4 and 8 + t/4,
-// columns 2 (t % 4) + {0, 1} and 8 + 2 (t % 4) + {0, 1} (the mma.sync
-// accumulator arrangement, two 8-column repetitions): four threads hold 32
-// contiguous bytes of a row, so each reduction below fills whole sectors.
-__device__ __forceinline__ void tmem_ld16x256_x2(uint32_t taddr, uint32_t (&r)[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-}
-
 __device__ __forceinline__ int rotated_tile(int ii, int rot, int ntiles) {
   const int ti = ii + rot;
   return ti >= ntiles ? ti - ntiles : ti;
@@ -306,10 +296,8 @@ indexer_kl_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid
       if (__any_sync(0xffffffffu, !okw)) return false;
       tc::fence_after_sync();
       uint32_t v[2][8];
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-        tmem_ld16x256_x2(tmem + ((uint32_t)(quad * 32 + hf * 16) << 16) + kColKI + buf * kDI + q * 16, v[hf]);
-      tc::tmem_wait_ld();
+      tc::tmem_ld16x256_pair_sync(tmem + ((uint32_t)(quad * 32) << 16) + kColKI + buf * kDI + q * 16,
+                                  tmem + ((uint32_t)(quad * 32 + 16) << 16) + kColKI + buf * kDI + q * 16, v[0], v[1]);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_kvfree + 8 * buf);

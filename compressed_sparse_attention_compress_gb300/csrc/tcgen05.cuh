@@ -168,6 +168,22 @@ __device__ __forceinline__ void tmem_ld8_sync(uint32_t taddr, uint32_t (&r)[8]) 
       : "r"(taddr)
       : "memory");
 }
+// Two blocks of 16 lanes x 16 columns (lane addresses taddr0, taddr1), in the
+// 16x256b shape: thread t gets lanes t/4 and 8 + t/4 of each block, columns
+// 2 (t % 4) + {0, 1} (registers 0-3) and 8 + 2 (t % 4) + {0, 1} (registers
+// 4-7): the mma.sync accumulator arrangement, so four threads hold 32
+// contiguous bytes of a row.  Waited for in the same asm statement.
+__device__ __forceinline__ void tmem_ld16x256_pair_sync(uint32_t taddr0, uint32_t taddr1, uint32_t (&r0)[8],
+                                                        uint32_t (&r1)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n"
+      "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]), "=r"(r0[6]), "=r"(r0[7]),
+        "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]), "=r"(r1[7])
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
