@@ -416,36 +416,25 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
         TK_T0(tk_w);
         int gt_before = 0, eq_before = 0;
         for (int ww = 0; ww < warp; ++ww) { gt_before += s_cnt[0][ww]; eq_before += s_cnt[1][ww]; }
-        // write pass, 128 consecutive entries per step (4 per lane, lane-major): one ballot per
-        // slot and flag gives every lane the count of selected entries ahead of its own four
+        // write pass, 128 consecutive entries per step as four rounds of 32 (entry jb + 32 e + lane):
+        // one ballot per round and flag gives every lane the count of selected entries ahead of its
+        // own, and the selected entries of a round go to consecutive slots (coalesced stores)
         const uint32_t lt = (1u << lane) - 1u;
         for (int jb = j_lo; jb < j_hi; jb += 128) {
-          const int j0 = jb + 4 * lane;
-          uint32_t kk[4];
-          int cgt, ceq;
-          flags_of(j0, kk, cgt, ceq);
-          bool fgt[4], feq[4];
-          int my_gt = gt_before, my_eq = eq_before, tot_gt = 0, tot_eq = 0;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const bool in = j0 + e < j_hi;
-            fgt[e] = in && (all || kk[e] > thr);
-            feq[e] = in && !all && kk[e] == thr;
-            const uint32_t bg = __ballot_sync(0xffffffffu, fgt[e]);
-            const uint32_t be = __ballot_sync(0xffffffffu, feq[e]);
-            my_gt += __popc(bg & lt);
-            my_eq += __popc(be & lt);
-            tot_gt += __popc(bg);
-            tot_eq += __popc(be);
+            const int j = jb + 32 * e + lane;
+            const bool in = j < j_hi;
+            const uint32_t kv = (!all && in) ? keys[j] : 0u;
+            const bool fg = in && (all || kv > thr);
+            const bool fe = in && !all && kv == thr;
+            const uint32_t bg = __ballot_sync(0xffffffffu, fg);
+            const uint32_t be = __ballot_sync(0xffffffffu, fe);
+            const int my_gt = gt_before + __popc(bg & lt), my_eq = eq_before + __popc(be & lt);
+            if (fg || (fe && my_eq < need_eq)) idx[orow + my_gt + min(my_eq, need_eq)] = bk.cmp0 + j;
+            gt_before += __popc(bg);
+            eq_before += __popc(be);
           }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (fgt[e] || (feq[e] && my_eq < need_eq)) idx[orow + my_gt + min(my_eq, need_eq)] = bk.cmp0 + j0 + e;
-            my_gt += fgt[e] ? 1 : 0;
-            my_eq += feq[e] ? 1 : 0;
-          }
-          gt_before += tot_gt;
-          eq_before += tot_eq;
         }
         for (int i = m + tid; i < k_pad; i += kComputeThreads) idx[orow + i] = -1;
         named_sync(1, kComputeThreads);
