@@ -384,7 +384,10 @@ csa_status_t csa_indexer_kl_static_scratch(csa_handle_t handle, const void* q, c
  * teacher's per-head log normaliser over C_t -- csa_sparse_attn_fwd's lse_cmp
  * in sparse mode, or the teacher_lse of csa_indexer_kl_ex in either mode;
  * student_lse (may be NULL): the student's, from csa_indexer_kl_ex.  With both
- * the call takes one pass over C_t instead of two.  Same limits. */
+ * the call takes one pass over C_t instead of two (for the dense teacher at 64
+ * heads x 128 and an 8 x 64 indexer in bf16, on the tensor cores).  dqI and dw
+ * are deterministic; dkI's float32 sums follow the order of the atomic
+ * additions and may differ in the last bits between runs.  Same limits. */
 csa_status_t csa_indexer_kl_bwd(csa_handle_t handle, const void* q, const void* kv_cmp,
                                 const void* qI, const void* w, const void* kI, const int32_t* idx,
                                 int k_pad, const float* lse_cmp, const float* student_lse,
