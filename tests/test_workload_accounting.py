@@ -29,3 +29,16 @@ def test_headline_counts():
 def test_thd_lengths_and_capacity():
     wl = WORKLOADS["thd128k"]
     assert wl.T == 140343 and wl.T_cap % 128 == 0 and wl.n_cmp == 35081
+
+
+def test_backward_counts():
+    # attention backward: S recompute, dP, dQ, dK, dV at 2 H d FLOPs each per (query, candidate key);
+    # indexer backward: the teacher once plus the indexer dots, dqI and dkI at 2 H_I d_I each
+    wl = WORKLOADS["warmup32k"]
+    c = workload.counts(wl)
+    assert c["attn_bwd_flops"] == 5 * 2 * 64 * 128 * c["attn_pairs"]
+    assert c["teacher_pairs"] == c["visible_pairs"]          # dense teacher: every visible entry
+    assert c["indexer_bwd_flops"] == (2 * 64 * 128 + 3 * 2 * 8 * 64) * c["teacher_pairs"]
+    # the selected teacher counts the selected entries instead
+    s = workload.counts(WORKLOADS["csa8k"])
+    assert s["teacher_pairs"] == sum(min(512, (t + 1) // 4) for t in range(8192))
