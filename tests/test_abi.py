@@ -51,3 +51,39 @@ def test_null_handle_is_rejected_before_any_launch(lib):
     assert lib.csa_compress(None, *([None] * 5), 0, 0, 0, 0, 0, 0, 0, None, None) == -1
     lib.csa_create.restype = ctypes.c_int
     assert lib.csa_create(0, None) == -1
+
+
+def _params(name):
+    text = open(HEADER).read()
+    m = re.search(r"^(?:csa_status_t)\s+" + name + r"\s*\((.*?)\);", text, flags=re.M | re.S)
+    return [p.strip() for p in m.group(1).replace("\n", " ").split(",")]
+
+
+def _null_args(params):
+    out = []
+    for p in params:
+        if "*" in p or p.startswith(("csa_handle_t", "cudaStream_t")):
+            out.append(ctypes.c_void_p(None))
+        elif p.startswith("float"):
+            out.append(ctypes.c_float(0.0))
+        elif p.startswith("int64_t"):
+            out.append(ctypes.c_int64(0))
+        elif p.startswith("size_t"):
+            out.append(ctypes.c_size_t(0))
+        else:  # int, csa_dtype_t
+            out.append(ctypes.c_int(0))
+    return out
+
+
+def test_every_call_rejects_a_null_handle_on_the_host(lib):
+    # the header's error rule: host-visible argument errors return CSA_ERR_INVALID_ARG
+    # before any launch -- checked for every call that takes a handle, with all
+    # other arguments zero or null, so nothing here touches a device
+    text = open(HEADER).read()
+    names = re.findall(r"^csa_status_t\s+(\w+)\s*\(\s*csa_handle_t", text, flags=re.M)
+    names = [n for n in names if n != "csa_destroy"]
+    assert len(names) >= 18, names
+    for n in names:
+        fn = getattr(lib, n)
+        fn.restype = ctypes.c_int
+        assert fn(*_null_args(_params(n))) == -1, n
