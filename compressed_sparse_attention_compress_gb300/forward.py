@@ -313,7 +313,8 @@ def attention_chunk_plan(cu: list, T_cap: int, W: int, n: int) -> list:
     ``lo``, ``hi`` (the rows its call sees), ``own`` (the rows whose outputs it
     leaves in place), ``copy`` (the query rows copied for
     it), ``cu`` (its own packing, one segment per sequence), ``pos0`` (each
-    segment's first position in its sequence) and ``max_len``.  Chunk starts
+    segment's first position in its sequence) and ``max_len`` (a bound on the
+    positions in the view, the calls' max_seqlen).  Chunk starts
     are multiples of 16 rows; fewer than 8 W rows per chunk: no chunks."""
     T = cu[-1]
     B = len(cu) - 1
@@ -331,9 +332,9 @@ def attention_chunk_plan(cu: list, T_cap: int, W: int, n: int) -> list:
         cu_l = [0]
         for L in seg:
             cu_l.append(cu_l[-1] + L)
+        pos0 = [max(lo, cu[b]) - cu[b] if seg[b] > 0 else 0 for b in range(B)]
         plan.append(dict(lo=lo, hi=hi, own=(a[k], hi), copy=(los[k], los[k + 1] if k + 1 < n else T_cap), cu=cu_l,
-                         pos0=[max(lo, cu[b]) - cu[b] if seg[b] > 0 else 0 for b in range(B)],
-                         max_len=max(seg + [1])))
+                         pos0=pos0, max_len=max([p + L for p, L in zip(pos0, seg)] + [1])))
     return plan
 
 

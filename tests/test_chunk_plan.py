@@ -57,6 +57,9 @@ def test_plan_invariants(n, W):
                 if L:
                     assert c["cu"][s] == s0 - lo and c["pos0"][s] == s0 - cu[s]
             assert c["cu"][-1] == min(hi, T) - lo
+            # max_seqlen bounds every position the view holds, and no more than the longest sequence
+            assert all(p + (c["cu"][s + 1] - c["cu"][s]) <= c["max_len"] for s, p in enumerate(c["pos0"]))
+            assert c["max_len"] <= max(lengths + [1])
             # owned queries see their whole window inside the view
             for t in range(a, min(b, T)):
                 s = seq_of[t]

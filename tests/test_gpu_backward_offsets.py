@@ -68,7 +68,7 @@ def test_backward_on_offset_ranges(L, a):
         delta = torch.empty(n, wl.H, dtype=torch.float32, device="cuda")
         h.set_position_offsets(torch.tensor([lo], dtype=torch.int32, device="cuda"), n_cap)
         try:
-            api.csa_sparse_attn_bwd(h, x["q"][lo:hi], f.kv_cmp, x["x_kv"][lo:hi], f.idx[lo:hi], cu_l, f.cu_cmp, n,
+            api.csa_sparse_attn_bwd(h, x["q"][lo:hi], f.kv_cmp, x["x_kv"][lo:hi], f.idx[lo:hi], cu_l, f.cu_cmp, L,
                                     r, W, f.scale, f.out[lo:hi], f.lse[lo:hi], d_l, dq_l, dc_l, dr_l, delta)
         finally:
             h.set_position_offsets(None)
@@ -94,7 +94,7 @@ def test_backward_on_offset_ranges(L, a):
         h.set_position_offsets(torch.tensor([lo], dtype=torch.int32, device="cuda"), n_cap)
         try:
             api.csa_indexer_kl_bwd(h, x["q"][lo:hi], f.kv_cmp, x["qI"][lo:hi], x["w"][lo:hi], f.kI, cu_l, f.cu_cmp,
-                                   n, r, f.scale, dqI_l, dw_l, dkI_l, lse_cmp=f.teacher_lse[lo:hi],
+                                   L, r, f.scale, dqI_l, dw_l, dkI_l, lse_cmp=f.teacher_lse[lo:hi],
                                    student_lse=f.student_lse[lo:hi], grad_scale=1.0)
         finally:
             h.set_position_offsets(None)
