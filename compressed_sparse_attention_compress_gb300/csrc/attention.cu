@@ -16,6 +16,9 @@
 // (mma.sync m16n8k16 bf16, fp32 accumulate) with an online softmax in the
 // exp2 domain; the compressed-only normaliser (lse_cmp) is taken when the
 // compressed part ends.
+// Precision: the normalisers are sums of the bf16-rounded weights that enter
+// the P V products (the output is a convex combination of the value rows with
+// the weights used); the reference is the exact running maximum.
 #include <math.h>
 
 #include "common.cuh"
@@ -177,10 +180,11 @@ attention_kernel(int kind, const TIn* __restrict__ q, const TIn* __restrict__ k_
     for (int n = 0; n < 8; ++n) {
       const float p0 = exp2f(s[n][0] - muse[0]), p1 = exp2f(s[n][1] - muse[0]);
       const float p2 = exp2f(s[n][2] - muse[1]), p3 = exp2f(s[n][3] - muse[1]);
-      l_run[0] += p0 + p1;
-      l_run[1] += p2 + p3;
-      pa[n >> 1][(n & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-      pa[n >> 1][(n & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+      const uint32_t a01 = pack_bf16x2(p0, p1), a23 = pack_bf16x2(p2, p3);
+      pa[n >> 1][(n & 1) * 2 + 0] = a01;
+      pa[n >> 1][(n & 1) * 2 + 1] = a23;
+      l_run[0] += bf16_lo(a01) + bf16_hi(a01);  // the sums are of the weights as written
+      l_run[1] += bf16_lo(a23) + bf16_hi(a23);
     }
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) {

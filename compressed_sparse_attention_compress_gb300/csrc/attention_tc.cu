@@ -27,6 +27,9 @@
 // Pipelining: the gather of tile i+1 (cp.async, zero-filled for missing keys)
 // runs during the softmax of tile i; PV(i) and QK(i+1) are issued together;
 // two CTAs share an SM.  Compressed tiles with no valid entry are skipped.
+// Precision: as in the warp-specialised kernel, the normalisers are sums of
+// the bf16-rounded weights that enter P^T, and the reference is the exact
+// maximum while a query has seen fewer than kExactKeys keys.
 #include <math.h>
 
 #include "common.cuh"
@@ -42,6 +45,7 @@ constexpr int kNH = 64;        // heads (N of both MMAs)
 constexpr int kDim = 128;      // head dim
 constexpr int kThr = 128;      // one thread per tensor-memory lane
 constexpr float kTau = 8.f;    // lazy-max slack, log2 units
+constexpr int kExactKeys = 32;  // exact maximum until this many keys were seen
 
 constexpr uint32_t kQRegion = kNH * 128;      // 8 KB: 64 rows x 64 dims
 constexpr uint32_t kTileRegion = kTK * 128;   // 16 KB: 128 rows x 64 dims
@@ -274,6 +278,7 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
 #pragma unroll
     for (int h = 0; h < kNH; ++h) l_part[h] = 0.f;
     bool have_o = false, snap = false;
+    int seen = 0;  // keys of this query in the tiles before this one
 
     bool aborted = false;
     while (cur < ntiles) {
@@ -331,7 +336,11 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       load_t();
       float excess = -INFINITY;
       if (valid) excess = to_log2_weights();  // m = -inf (first tile) gives +inf
-      if (__syncthreads_or(excess > kTau)) {
+      // the reference is the exact running maximum while the query has seen fewer
+      // than kExactKeys keys (with few candidates one key can carry most of the
+      // weight: its P^T weight is then exactly 1, free of bf16 rounding), and lags by
+      // up to kTau after that
+      if (__syncthreads_or(excess > (seen < kExactKeys ? 0.f : kTau))) {
         // new reference: the tile's per-head column maxima (warp max-reductions)
         load_t();
 #pragma unroll
@@ -375,10 +384,9 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int h = c * 8 + 2 * j;
-              const float p0 = ex2(t[h]), p1 = ex2(t[h + 1]);
-              l_part[h] += p0;
-              l_part[h + 1] += p1;
-              pk[j] = pack_bf16x2(p0, p1);
+              pk[j] = pack_bf16x2(ex2(t[h]), ex2(t[h + 1]));
+              l_part[h] += bf16_lo(pk[j]);  // the sums are of the weights as written
+              l_part[h + 1] += bf16_hi(pk[j]);
             }
           }
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + tc::sw128_offset(tid, c)),
@@ -390,7 +398,7 @@ attention_tc_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       tc::fence_proxy_async_smem();
       cp_async_wait<0>();           // next tile's gather has landed
       tc::fence_proxy_async_smem();
-      __syncthreads();
+      seen += __syncthreads_count(valid);
       if (tid == 0) {
         tc::fence_after_sync();
         issue_pv(buf, !have_o);

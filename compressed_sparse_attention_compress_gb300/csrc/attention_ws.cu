@@ -29,6 +29,12 @@
 //   an MMA warp per group: issues QK of the next tile as soon as S^T has been
 //     read and the tile gathered, then PV of the current tile once its P^T is
 //     written (shared-memory descriptors precomputed, waits that sleep).
+// Precision: the weights enter P^T as bf16 (relative error up to 2^-9), and
+// every normaliser (the output's, lse, lse_cmp) is the sum of those rounded
+// weights, so the output is a convex combination of the value rows with the
+// weights the tensor cores used.  The running reference is the exact maximum
+// while a query has seen fewer than kExactKeys keys: one key can then carry
+// most of the weight, and at the exact maximum its weight is exactly 1.
 #include <math.h>
 
 #include "common.cuh"
@@ -70,6 +76,7 @@ constexpr int kMmaWarp = kProdWarp0 + 2 * kProdWarps;      // warps 18, 19: one 
 constexpr int kRowsPerProd = kTK / kProdThreads;           // 4
 constexpr int kThreads = 32 * (kMmaWarp + 2);
 constexpr float kTau = 8.f;                                // lazy-max slack, log2 units
+constexpr int kExactKeys = 32;                             // exact maximum until this many keys were seen
 
 constexpr uint32_t kQRegion = kNH * 128;                   // 8 KB: 64 rows x 64 dims
 constexpr uint32_t kQBytes = 2 * kQRegion;                 // 16 KB per group
@@ -85,6 +92,7 @@ enum : int { kFirst = 1, kLast = 2, kWinStart = 4, kDone = 8, kCmp = 16 };
 struct Meta {
   int row;
   int flags;
+  int nvalid;  // keys of the tile that take part
 };
 
 __device__ __forceinline__ int ord_of(float f) {
@@ -275,6 +283,9 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
         }
         const bool cmpt = it < nct;
         const __nv_bfloat16* ks = cmpt ? k_cmp : k_raw;
+        int nval = 0;
+#pragma unroll
+        for (int i = 0; i < kRowsPerProd; ++i) nval += __popc(__ballot_sync(0xffffffffu, rr[i] >= 0));
         const uint32_t kb = base + kStageOff + (g * 2 + st) * kTileBytes;
 #pragma unroll
         for (int i = 0; i < kRowsPerProd; ++i) s_rows[g][st][pt + 32 * i] = rr[i];
@@ -293,7 +304,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
         if (pt == 0) {
           const int flags = (first ? kFirst : 0) | (cmpt ? kCmp : 0) | (it == nct ? kWinStart : 0) |
                             (it == ntl - 1 ? kLast : 0);
-          s_meta[g][st] = Meta{row, flags};
+          s_meta[g][st] = Meta{row, flags, nval};
         }
         arrive_cp_async(full_bar(g, st));
         __syncwarp();
@@ -310,7 +321,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       if (__any_sync(0xffffffffu, !ok)) {
         *abort_flag = 1;
       } else {
-        if (pt == 0) s_meta[g][st] = Meta{-1, kDone};
+        if (pt == 0) s_meta[g][st] = Meta{-1, kDone, 0};
         mbar_arrive(full_bar(g, st));
         __syncwarp();
         if (lane == 0) arrive_warp(full_bar(g, st));
@@ -416,6 +427,9 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
     const uint32_t t_o = tmem + lane_off + g * 128 + kNH + hh * 32;
     // this thread's running per-head sums of p over its key (32 heads) live in
     // tensor memory next to the accumulators, which keeps registers for the scores
+    // The sums are of the bf16-rounded weights that enter P^T, so the output is a
+    // convex combination of the value rows with exactly the weights the tensor
+    // cores used, and the LSEs are those of the same weights.
     const uint32_t t_l = tmem + lane_off + 256 + g * kNH + hh * 32;
     const int gbar = 1 + g;
     float* m_g = s_m[g];
@@ -423,11 +437,12 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
     uint32_t k = 0;
     int row = -1;
     bool have_o = false;
-    auto load_l = [&](float (&v)[32]) {
+    int seen = 0;  // keys of the current query in the tiles before this one
+    auto load_l = [&](float (&v)[32], uint32_t at) {
 #pragma unroll
       for (int c0 = 0; c0 < 32; c0 += 16) {
         uint32_t rv[16];
-        tc::tmem_ld16_sync(t_l + c0, rv);
+        tc::tmem_ld16_sync(at + c0, rv);
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[c0 + j] = __uint_as_float(rv[j]);
       }
@@ -447,6 +462,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       if (fresh) {
         row = mt.row;
         have_o = false;
+        seen = 0;
       }
       if ((mt.flags & kWinStart) && lse_cmp != nullptr) {  // compressed candidates done: their normaliser
         float tmp[32];
@@ -454,7 +470,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
 #pragma unroll
           for (int j = 0; j < 32; ++j) tmp[j] = 0.f;
         } else {
-          load_l(tmp);
+          load_l(tmp, t_l);
         }
         s_lsum[g][quad][hh * 32 + lane] = warp_sum32(tmp, lane);
         bar_sync(gbar, kSoftThreads);
@@ -509,7 +525,12 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
       // PV keeps running meanwhile: it is waited for only where P^T / O^T are touched.
       const bool bad = !ok || *abort_flag != 0;
       bool pv_done = k == 0;
-      if (bar_or(gbar, kSoftThreads, excess > kTau || bad)) {
+      // the reference is the exact running maximum while a query has seen fewer than
+      // kExactKeys keys (with few candidates one key can carry most of the weight:
+      // its weight is then exactly 1 in P^T, free of bf16 rounding), and lags by up
+      // to kTau after that
+      const float tau = seen < kExactKeys ? 0.f : kTau;
+      if (bar_or(gbar, kSoftThreads, excess > tau || bad)) {
         // new reference: the tile's per-head column maxima (t + m is the scaled score)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -575,9 +596,9 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int h = c * 8 + 2 * j;
-          t[h] = valid ? ex2(t[h]) : 0.f;  // t now holds p
-          t[h + 1] = valid ? ex2(t[h + 1]) : 0.f;
-          pk[j] = pack_bf16x2(t[h], t[h + 1]);
+          pk[j] = valid ? pack_bf16x2(ex2(t[h]), ex2(t[h + 1])) : 0u;
+          t[h] = bf16_lo(pk[j]);  // t now holds the weight as written
+          t[h + 1] = bf16_hi(pk[j]);
         }
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + tc::sw128_offset(key, hh * 4 + c)),
                      "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]));
@@ -607,6 +628,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
         tc::tmem_st16(t_l + c2 * 16, lv);
       }
       tc::tmem_wait_st();
+      seen += mt.nvalid;
       WS_ADD(5, s_p);
       WS_CNT(7);
       have_o = true;
@@ -622,7 +644,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
         tc::fence_after_sync();
         {
           float lt[32];
-          load_l(lt);
+          load_l(lt, t_l);
           s_lsum[g][quad][hh * 32 + lane] = warp_sum32(lt, lane);
         }
         bar_sync(gbar, kSoftThreads);
@@ -630,7 +652,7 @@ attention_ws_kernel(int kind, const __nv_bfloat16* __restrict__ q, const __nv_bf
           float l = s_lsum[g][0][tig] + s_lsum[g][1][tig] + s_lsum[g][2][tig] + s_lsum[g][3][tig];
           float m = m_g[tig];
           float corr = 1.f;
-          if (sink != nullptr) {
+          if (sink != nullptr) {  // the sink enters the normaliser only (it has no value row)
             const float s2 = __ldg(sink + tig) * 1.4426950408889634f;
             const float mf = fmaxf(m, s2);
             corr = (m == -INFINITY) ? 0.f : ex2(m - mf);

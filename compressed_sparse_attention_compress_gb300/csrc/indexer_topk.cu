@@ -90,7 +90,9 @@ indexer_topk_kernel(const TIn* __restrict__ qI, const TIn* __restrict__ w, const
     for (int bb = 0; bb < B; ++bb) {
       L = __ldg(cu + bb + 1) - __ldg(cu + bb);
       if (L < 0) { raise_status(status, CSA_ERR_DEVICE_BOUNDS); L = 0; }
-      if (L / r > max_vis) { raise_status(status, CSA_ERR_DEVICE_BOUNDS); L = 0; }
+      // the last query of the sequence sees (L + p0) / r entries (p0: position of its first row)
+      const int pp = pos0 ? __ldg(pos0 + bb) : 0;
+      if ((L + pp) / r > max_vis) { raise_status(status, CSA_ERR_DEVICE_BOUNDS); L = 0; }
       const int nch = (L + G - 1) / G;
       if (c < nch) { b = bb; break; }
       c -= nch;
@@ -109,7 +111,7 @@ indexer_topk_kernel(const TIn* __restrict__ qI, const TIn* __restrict__ w, const
   const int n_b = (__ldg(cu + b + 1) - seq0 + p0) / r;
   const int rows = G * H_I;
   const int mtiles = (rows + 15) / 16;
-  const int vis_last = (q0 + nq + p0) / r;  // visible entries of the chunk's last query
+  const int vis_last = min((q0 + nq + p0) / r, max_vis);  // visible entries of the chunk's last query
   const int ntiles = (vis_last + kTileN - 1) / kTileN;
 
   // A operand: indexer query rows (g, h) -> row g*H_I + h; zero past nq.
@@ -195,7 +197,7 @@ indexer_topk_kernel(const TIn* __restrict__ qI, const TIn* __restrict__ w, const
   for (int g = 0; g < nq; ++g) {
     const int t = q0 + g;
     const int64_t orow = (int64_t)(seq0 + t) * k_pad;
-    const int n = (t + p0 + 1) / r;
+    const int n = min((t + p0 + 1) / r, max_vis);
     const int m = min(topk, n);
     const uint32_t* keys = sKey + (size_t)g * vstride;
     uint32_t thr = 0;

@@ -12,7 +12,10 @@
 // that loads this library holds it (2 MiB) until the process exits.  Its
 // device address is looked up once per device, with that device current,
 // the first time the entry point runs on it; make that first call before any
-// stream capture.  Calls share the array: two calls that overlap on the GPU
+// stream capture.  The address is cached for the life of the process, so it is
+// stale after cudaDeviceReset or any other teardown of that device's primary
+// context: do not call this entry point on the device again after one.  Calls
+// share the array: two calls that overlap on the GPU
 // (different streams, or different host threads) race on it and must be
 // serialised by the caller.  Every scratch element a call reads is written
 // earlier in the same call, so nothing in it has to start at zero and the

@@ -215,6 +215,13 @@ csa_status_t csa_indexer_topk_fp8(csa_handle_t handle, const uint8_t* qI, const 
  *   out[t,h,:] = sum_i softmax_i(s_i; sink_h) V_i,  lse[t,h] = log(sum_i e^{s_i} + e^{sink_h})
  *   lse_cmp[t,h] = logsumexp of s_i over the compressed candidates only (no
  *   window, no sink), -inf when there are none.
+ * The weights e^{s_i - m} enter the value products on the tensor cores
+ * rounded to bf16 (relative error up to 2^-9), and the normalisers in lse,
+ * lse_cmp and the output are the sums of those same rounded weights, so out
+ * is a convex combination of the value rows with exactly the weights used
+ * and out, lse combine consistently (merging partial results by their LSEs).
+ * lse and lse_cmp therefore differ from the float64 log-sum-exp by up to
+ * about 2e-3 when one key dominates (much less when the weight is spread).
  *   q [T_cap, H, d], kv_cmp [., d], kv_raw [T_cap, d]          (dtype)
  *   v_cmp / v_raw: separate value rows, or NULL for K = V
  *   sink [H] float32 or NULL; lse [T_cap, H], lse_cmp [T_cap, H] or NULL (float32)
@@ -325,9 +332,12 @@ csa_status_t window_attn_bwd(csa_handle_t handle, const void* q, const void* kv_
  *   kl_per_query[t] = sum_j p(j) (log p(j) - log q(j)), 0 when C_t is empty
  *   kl_sum[0]  = sum over rows of kl_per_query (float32, fixed summation order)
  *   n_valid[0] = number of rows with a non-empty C_t
- * lse_cmp (sparse mode only, may be NULL): the per-head log normaliser over
- * C_t from csa_sparse_attn_fwd; when given, the teacher takes one pass over
- * C_t instead of two.  kl_per_query and n_valid may be NULL.
+ * lse_cmp (sparse mode only, may be NULL): a per-head log normaliser over
+ * C_t to use for the teacher instead of computing it; the teacher then takes
+ * one pass over C_t instead of two.  csa_sparse_attn_fwd's lse_cmp is the
+ * normaliser of its bf16-rounded weights (see there), so a teacher normalised
+ * by it sums to 1 only within about 2e-3 when one key dominates; pass NULL
+ * for the exact teacher.  kl_per_query and n_valid may be NULL.
  * ws/ws_bytes: device scratch of at least csa_indexer_kl_workspace(T_cap)
  * bytes (per-query partial results); CSA_ERR_WORKSPACE otherwise.
  * Same layouts as csa_indexer_topk / csa_sparse_attn_fwd. */
@@ -353,6 +363,10 @@ size_t csa_indexer_kl_workspace(int T_cap);
  *   - T_cap must be <= 262144; larger returns CSA_ERR_WORKSPACE.
  *   - The first call on each device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
+ *     The address is kept for the life of the process: after a
+ *     cudaDeviceReset (or any other teardown of the device's primary
+ *     context) it is stale, and this entry point must not be called again on
+ *     that device in the same process.
  *   - Calls share the array: calls that overlap on the GPU race on it, so the
  *     caller serialises them.  Each call writes every scratch element it
  *     reads, so leftover contents from an earlier call are never used.

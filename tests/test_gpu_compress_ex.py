@@ -3,8 +3,10 @@
 The variant adds a separate previous-half stream, a post-compression RMSNorm
 and a rotary embedding on compressed coordinates to the softmax-gated
 compressor ("DeepSeek-V4 Attention Training Systems", §10, §12 invariants 2
-and 3).  Every case compares all entries with the fp64 oracle within max-abs
-1e-2 beyond the half-ulp of the output's own storage rounding; ragged lengths
+and 3).  Every case compares all entries with the fp64 oracle: float32
+outputs within max-abs 1e-2; bf16 outputs within max-abs 1e-2 where |x| < 4,
+and at |x| >= 4 (bf16 spacing 1/32, after the RMSNorm) one of the two bf16
+values bracketing the exact one; ragged lengths
 cover empty sequences, sequences shorter than one block, a tail of L mod r
 tokens and runs that end mid-CTA.
 """
@@ -57,9 +59,11 @@ def _run(lengths, D, ratio, overlap, two, norm, rope_dim, fp32=False, stride=1, 
                              gamma=arrs["gamma"] if norm else None, eps=eps, rope_dim=rope_dim, theta=theta,
                              pos_stride=stride, pos_offset=offset)
     got = ph.np32(out[:n_c]).astype(np.float64)
-    quant = ph.bf16_half_ulp(ref) if not fp32 else 0.0
-    err = (np.abs(got - ref) - quant).max() if ref.size else 0.0
-    assert err <= ph.ATOL, f"compress_ex max-abs {err}"
+    if fp32:
+        err = ph.record("compress_ex_fp32", np.abs(got - ref).max() if ref.size else 0.0)
+        assert err <= ph.ATOL, f"compress_ex max-abs {err}"
+    elif ref.size:
+        ph.check_stored_bf16(got, ref, "compress_ex")
     return out[:n_c], (h, x, z, P, cu, cu_cmp)
 
 
@@ -67,6 +71,13 @@ def _run(lengths, D, ratio, overlap, two, norm, rope_dim, fp32=False, stride=1, 
 @pytest.mark.parametrize("two", [True, False])
 def test_csa_overlap_norm_rope(D, two):
     _run(RAGGED, D, 4, True, two, norm=True, rope_dim=min(64, D // 2))
+
+
+@pytest.mark.parametrize("D", [256, 512])
+def test_fp32_output_of_the_widest_norm_rope_cases(D):
+    """The unrounded (float32-output) values of the cases whose RMSNorm outputs
+    reach |x| >= 4: the arithmetic itself within the plain max-abs 1e-2."""
+    _run(RAGGED, D, 4, True, True, norm=True, rope_dim=64, fp32=True)
 
 
 @pytest.mark.parametrize("fp32", [False, True])

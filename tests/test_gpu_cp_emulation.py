@@ -8,12 +8,17 @@ keeps the entries it owns, the owned entries are gathered by local copies, and
 each rank's top-k, attention and KL run on its local rows with the handle's
 position offsets.  Every owned query must reproduce the one-GPU forward bit
 for bit: the per-query arithmetic is the same, only the rows around it moved.
+The emulated ranks' results are also compared with the oracle on every row
+(gathered compressed rows, index sets, outputs and LSEs, per-query KL and its
+sum), within the same tolerances as the one-GPU parity tests.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from compressed_sparse_attention_compress_gb300 import inputs as I
+from tests import parity_helpers as ph
 
 pytestmark = pytest.mark.gpu
 
@@ -54,3 +59,27 @@ def test_cp_ranks_reproduce_the_single_gpu_forward(wl, P):
     assert torch.equal(res["lse_cmp"], f.lse_cmp[:T])
     if wl.kl_mode != "none":
         assert torch.equal(res["kl_rows"], f.kl_rows[:T])
+
+
+@pytest.mark.parametrize("wl,P", CASES, ids=[c[0].name for c in CASES])
+def test_cp_ranks_match_the_oracle(wl, P):
+    arrs = I.generate(wl, 11)
+    dev = to_device(arrs, wl.io_fp32)
+    res = cp.emulate(wl, dev, P)
+    assert res["status"] == 0
+    cu = arrs["cu_seqlens"]
+    T, n_c = wl.T, wl.n_cmp
+    rows = np.arange(T)
+    # gathered compressed rows (each rank compressed its own rows plus the boundary)
+    ph.check_compress(res["kv_cmp"], arrs["x_kv"], arrs["z_kv"], arrs["P_kv"], cu, wl.ratio, wl.overlap, n_c)
+    ph.check_compress(res["kI"], arrs["x_I"], arrs["z_I"], arrs["P_I"], cu, wl.ratio, wl.overlap, n_c)
+    kv_cmp, kI = ph.operand(res["kv_cmp"]), ph.operand(res["kI"])
+    idx = res["idx"].cpu().numpy()
+    ph.check_topk(idx, arrs["qI"], arrs["w"], kI, cu, wl.ratio, wl.topk, rows)
+    scale = 1.0 / float(np.sqrt(wl.d))
+    ph.check_attention(oracle.KIND_CSA, res["out"], res["lse"], res["lse_cmp"], arrs["q"], kv_cmp, None,
+                       arrs["x_kv"], None, cu, wl.ratio, wl.window, scale, idx, rows)
+    kl_rows = ph.np32(res["kl_rows"])
+    kl_idx = idx if wl.kl_mode == "sparse" else None
+    ph.check_kl(float(kl_rows.astype(np.float64).sum()), kl_rows, arrs["q"], kv_cmp, arrs["qI"], arrs["w"], kI,
+                cu, wl.ratio, scale, kl_idx, rows, full=True)

@@ -102,6 +102,9 @@ RAGGED = [
     I.custom("window_small", lengths=[333, 129, 64], ratio=0, overlap=False, H=32, d=128, window=100),
     I.custom("csa_sepv_h8", lengths=[517], ratio=4, overlap=True, H=8, d=128, window=64, H_I=1, d_I=64,
              topk=200, k_pad=256, separate_v=True, kl_mode="sparse"),
+    # a separate value stream at 64 heads x 128 (the tcgen05 kernel that stages K and V)
+    I.custom("csa_sepv_h64", lengths=[517, 0, 130], ratio=4, overlap=True, H=64, d=128, window=128, H_I=8,
+             d_I=64, topk=96, k_pad=128, separate_v=True, kl_mode="sparse", cap_align=64),
 ]
 
 
@@ -147,6 +150,32 @@ def test_full_size_workloads_sampled(name):
     f, arrs = _run(wl, seed=0)
     rows = _sample_rows(wl)
     _check_all(f, arrs, wl, rows=rows, kl_full=False)
+
+
+def test_csa8k_kl_sum_over_every_query_against_the_oracle():
+    """Sparse mode at full size: the KL sum of all 8192 queries (the selected-set
+    teacher over the GPU's own index lists) within 1e-3 relative of the oracle's,
+    and every per-query value."""
+    wl = I.WORKLOADS["csa8k"]
+    f, arrs = _run(wl, seed=0)
+    cu = arrs["cu_seqlens"]
+    n_c = int(f.cu_cmp[-1].item())
+    kv_cmp, kI = ph.operand(f.kv_cmp[:n_c]), ph.operand(f.kI[:n_c])
+    idx = f.idx.cpu().numpy()
+    ph.check_kl(float(f.kl_sum.item()), ph.np32(f.kl_rows), arrs["q"], kv_cmp, arrs["qI"], arrs["w"], kI, cu,
+                wl.ratio, f.scale, idx, np.arange(wl.T_cap), full=True)
+    assert int(f.n_valid.item()) == wl.T - (wl.ratio - 1)   # queries t >= r - 1 see an entry
+
+
+def test_warmup32k_kl_sum_is_the_fixed_order_sum_of_its_rows():
+    """The dense-teacher step at full size: the loss the finalising reduction
+    returns equals the float64 sum of the per-query values it was given."""
+    wl = I.WORKLOADS["warmup32k"]
+    f, _ = _run(wl, seed=0)
+    rows = ph.np32(f.kl_rows).astype(np.float64)
+    want = rows.sum()
+    rel = ph.record("kl_sum_vs_rows_rel", abs(float(f.kl_sum.item()) - want) / abs(want))
+    assert rel <= 1e-6, (float(f.kl_sum.item()), want)
 
 
 V4 = [
