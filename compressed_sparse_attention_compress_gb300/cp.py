@@ -187,7 +187,7 @@ def emulate(wl, dev: dict, P: int, boundary: int | None = None):
             kl_rows = torch.zeros(T_l, device=dvc)
             ws = torch.empty(api.csa_indexer_kl_workspace(T_l), dtype=torch.uint8, device=dvc)
             api.csa_indexer_kl(h, q, kv_cmp, qI, w, kI, cu_l, cu_cmp, max_pos, r, scale, kl_sum, ws,
-                               idx=idx if sparse else None, kl_per_query=kl_rows)
+                               idx=idx if sparse else None, lse_cmp=lse_c if sparse else None, kl_per_query=kl_rows)
             res["kl_rows"].append(kl_rows)
         own = torch.from_numpy(lay.own_local_rows()).to(dvc)
         grow = np.concatenate([np.arange(cu_g[b] + s, cu_g[b] + e) for b, (s, e) in enumerate(zip(lay.start, lay.end))])

@@ -8,8 +8,7 @@
 //
 // Teacher: p(j) = (1/H) sum_h softmax_{C_t}(scale q_h . K_j); student: softmax of
 // the indexer logits over C_t.  Per query row one CTA; warps split the heads as
-// in the attention kernel.  Pass 1 (skipped when the per-head normaliser over
-// C_t is given) runs the per-head online log-sum-exp; pass 2 recomputes the
+// in the attention kernel.  Pass 1 runs the per-head online log-sum-exp; pass 2 recomputes the
 // scores, forms p(j) by summing exp2(s - lse) over heads (shuffles within a
 // warp, shared memory across warps), computes the indexer logit of each key
 // and accumulates sum p log p, sum p i and the student's log-sum-exp, so that
@@ -37,7 +36,6 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
   constexpr int kRows = NW * 16;
   constexpr int kThreads = NW * 32;
   constexpr float kLn2 = 0.6931471805599453f;
-  constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ __align__(128) uint8_t smem[];
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem);
   __nv_bfloat16* sK = sQ + kRows * kStride;                       // [2][kKeys][kStride]
@@ -121,16 +119,11 @@ indexer_kl_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k_cmp, cons
     }
   };
 
-  // per-head log2 normaliser over C_t for the two rows this thread holds
+  // per-head log2 normaliser over C_t for the two rows this thread holds (the
+  // exact one: a given lse_cmp only serves the tensor-core kernel as a reference)
   float lse2[2] = {-INFINITY, -INFINITY};
-  const bool have_lse = (!dense) && lse_cmp != nullptr;
-  if (have_lse) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int h = warp * 16 + (lane >> 2) + i * 8;
-      lse2[i] = h < H ? __ldg(lse_cmp + (int64_t)row * H + h) * kLog2e : -INFINITY;
-    }
-  } else {
+  (void)lse_cmp;
+  {
     // ---- pass 1: per-head online log-sum-exp over C_t ----
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     if (ntiles > 0) { resolve(0, 0, false); __syncthreads(); issue(0, false); }
@@ -347,6 +340,13 @@ cudaError_t launch_indexer_kl(const KLArgs& a, bool fp32, cudaStream_t stream) {
   // the dense teacher at 64 x 128 heads / 8 x 64 indexer (bf16) runs on tcgen05 with TMA-fed tiles
   if (indexer_kl_dense_tc_supported(a, fp32)) {
     cudaError_t err = launch_indexer_kl_dense_tc(a, stream);
+    if (err != cudaSuccess) return err;
+    kl_finalize_kernel<<<1, 1024, 0, stream>>>(a.kl_rows, a.csize, a.T_cap, a.kl_sum, a.n_valid);
+    return cudaGetLastError();
+  }
+  // the selected-set teacher at the same shapes, with a reference normaliser from the attention
+  if (indexer_kl_sparse_tc_supported(a, fp32)) {
+    cudaError_t err = launch_indexer_kl_sparse_tc(a, stream);
     if (err != cudaSuccess) return err;
     kl_finalize_kernel<<<1, 1024, 0, stream>>>(a.kl_rows, a.csize, a.T_cap, a.kl_sum, a.n_valid);
     return cudaGetLastError();

@@ -501,6 +501,12 @@ __global__ void kl_zero_rows_kernel(float* __restrict__ kl_rows, int32_t* __rest
       teacher_lse[i] = -INFINITY;
 }
 
+cudaError_t launch_kl_zero_rows(float* kl_rows, int32_t* csize, int T_cap, float* teacher_lse, int H,
+                                float* student_lse, cudaStream_t stream) {
+  kl_zero_rows_kernel<<<152, 256, 0, stream>>>(kl_rows, csize, T_cap, teacher_lse, H, student_lse);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream) {
   if (a.T_cap <= 0) return cudaSuccess;
   CUtensorMap mq, mk, mqi, mki;

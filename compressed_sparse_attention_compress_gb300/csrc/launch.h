@@ -134,6 +134,13 @@ struct KLArgs {
 cudaError_t launch_indexer_kl(const KLArgs& a, bool fp32, cudaStream_t stream);
 bool indexer_kl_dense_tc_supported(const KLArgs& a, bool fp32);
 cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream);
+// tcgen05 selected-set teacher (64 x 128 heads, indexer 8 x 64, bf16, with a
+// reference normaliser lse_cmp); launch_indexer_kl dispatches to it.
+bool indexer_kl_sparse_tc_supported(const KLArgs& a, bool fp32);
+cudaError_t launch_indexer_kl_sparse_tc(const KLArgs& a, cudaStream_t stream);
+// Every row as an empty C_t (KL 0, |C_t| 0, normalisers -inf).
+cudaError_t launch_kl_zero_rows(float* kl_rows, int32_t* csize, int T_cap, float* teacher_lse, int H,
+                                float* student_lse, cudaStream_t stream);
 
 // Indexer KL backward: dqI, dw (I/O dtype) and float32 dkI (zeroed by the
 // launcher) for upstream gradient grad_scale; the teacher is detached.

@@ -114,10 +114,10 @@ class Forward:
         wl, x = self.wl, self.x
         save_stats = self.keep_stats if save_stats is None else save_stats
         sparse = wl.kl_mode == "sparse"
-        # the teacher computes its own exact normaliser (the attention's lse_cmp is
-        # that of its bf16-rounded weights)
-        kw = dict(idx=self.idx if sparse else None, kl_per_query=self.kl_rows, n_valid=self.n_valid,
-                  stream=stream)
+        # the teacher computes its own exact normaliser; the attention's lse_cmp (that of
+        # its bf16-rounded weights) serves as the reference of that computation
+        kw = dict(idx=self.idx if sparse else None, lse_cmp=self.lse_cmp if sparse else None,
+                  kl_per_query=self.kl_rows, n_valid=self.n_valid, stream=stream)
         if not save_stats:
             api.csa_indexer_kl(self.h, x["q"], self.kv_cmp, x["qI"], x["w"], self.kI, self.cu, self.cu_cmp,
                                self.max_seqlen, wl.ratio, self.scale, self.kl_sum, self.ws, **kw)

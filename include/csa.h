@@ -332,12 +332,14 @@ csa_status_t window_attn_bwd(csa_handle_t handle, const void* q, const void* kv_
  *   kl_per_query[t] = sum_j p(j) (log p(j) - log q(j)), 0 when C_t is empty
  *   kl_sum[0]  = sum over rows of kl_per_query (float32, fixed summation order)
  *   n_valid[0] = number of rows with a non-empty C_t
- * lse_cmp (sparse mode only, may be NULL): a per-head log normaliser over
- * C_t to use for the teacher instead of computing it; the teacher then takes
- * one pass over C_t instead of two.  csa_sparse_attn_fwd's lse_cmp is the
- * normaliser of its bf16-rounded weights (see there), so a teacher normalised
- * by it sums to 1 only within about 2e-3 when one key dominates; pass NULL
- * for the exact teacher.  kl_per_query and n_valid may be NULL.
+ * lse_cmp (sparse mode only, may be NULL): a reference for the teacher's
+ * per-head log normaliser over C_t, within a few units of it --
+ * csa_sparse_attn_fwd's lse_cmp is one.  The teacher's exact normaliser is
+ * computed either way (a first pass over C_t); with the reference, 64 heads x
+ * 128 and an 8 x 64 indexer in bf16 run on the tensor cores, the first pass
+ * summing exp(s - reference) per head.  A reference more than about 22 below
+ * the true value raises CSA_ERR_DEVICE_BOUNDS.  kl_per_query and n_valid may
+ * be NULL.
  * ws/ws_bytes: device scratch of at least csa_indexer_kl_workspace(T_cap)
  * bytes (per-query partial results); CSA_ERR_WORKSPACE otherwise.
  * Same layouts as csa_indexer_topk / csa_sparse_attn_fwd. */
@@ -395,8 +397,9 @@ csa_status_t csa_indexer_kl_static_scratch(csa_handle_t handle, const void* q, c
  * (dtype) are written (0 for capacity rows and rows with an empty C_t); dkI
  * [floor(T_cap/ratio), d_I] float32 is zeroed and accumulated with float32
  * atomic additions.  idx as in csa_indexer_kl.  lse_cmp (may be NULL): the
- * teacher's per-head log normaliser over C_t -- csa_sparse_attn_fwd's lse_cmp
- * in sparse mode, or the teacher_lse of csa_indexer_kl_ex in either mode;
+ * teacher's per-head log normaliser over C_t -- the teacher_lse of
+ * csa_indexer_kl_ex (csa_sparse_attn_fwd's lse_cmp is that of its
+ * bf16-rounded weights, within about 2e-3 of it);
  * student_lse (may be NULL): the student's, from csa_indexer_kl_ex.  With both
  * the call takes one pass over C_t instead of two (for the dense teacher at 64
  * heads x 128 and an 8 x 64 indexer in bf16, on the tensor cores).  dqI and dw
