@@ -412,7 +412,11 @@ def f_launches(wl) -> int:
     """Kernels of ours launched per step (mirrors the dispatch in csrc/)."""
     n = 0
     if wl.ratio > 0:
-        n += 1 + 1 + (1 if wl.separate_v else 0) + (1 if wl.H_I > 0 else 0)   # offsets + compress calls
+        if (wl.compressor != "v4" and not wl.separate_v and wl.H_I > 0
+                and (wl.d, wl.d_I) in ((128, 64), (64, 32))):
+            n += 1                                                              # both compressors + offsets
+        else:
+            n += 1 + 1 + (1 if wl.separate_v else 0) + (1 if wl.H_I > 0 else 0)   # offsets + compress calls
         if wl.H_I > 0:
             n += 2                                                              # top-k + capacity fill
             if wl.indexer == "fp8":

@@ -49,6 +49,7 @@ def _load():
         "csa_set_position_offsets": [P, P, I],
         "csa_compressed_offsets": [P, P, I, I, P, P],
         "csa_compress": [P, P, P, P, P, P, I, I, I, I, I, I, I, P, P],
+        "csa_compress_pair": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P],
         "csa_compress_ex": [P, P, P, P, P, P, P, F, I, F, I, I, P, P, I, I, I, I, I, I, I, P, P],
         "csa_indexer_topk": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P],
         "csa_sparse_attn_fwd": [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P],
@@ -153,6 +154,17 @@ def csa_compress(h: Handle, x, z, pos_bias, cu_seqlens, cu_cmp, max_seqlen: int,
     return _check("csa_compress", LIB.csa_compress(
         h.ptr, _p(x), _p(z), _p(pos_bias), _p(cu_seqlens), _p(cu_cmp), cu_seqlens.numel() - 1, T_cap,
         int(max_seqlen), D, int(ratio), int(bool(overlap)), _dtype(x), _p(out), _stream(stream)))
+
+
+def csa_compress_pair(h: Handle, x_kv, z_kv, pos_bias_kv, x_I, z_I, pos_bias_I, cu_seqlens, max_seqlen: int,
+                      ratio: int, overlap: bool, cu_cmp, kv_cmp, kI_cmp, stream=None):
+    """Both compressors of a layer and the compressed offsets in one launch."""
+    T_cap, D = x_kv.shape
+    d_I = x_I.shape[1]
+    return _check("csa_compress_pair", LIB.csa_compress_pair(
+        h.ptr, _p(x_kv), _p(z_kv), _p(pos_bias_kv), _p(x_I), _p(z_I), _p(pos_bias_I), _p(cu_seqlens),
+        cu_seqlens.numel() - 1, T_cap, int(max_seqlen), D, d_I, int(ratio), int(bool(overlap)), _dtype(x_kv),
+        _p(cu_cmp), _p(kv_cmp), _p(kI_cmp), _stream(stream)))
 
 
 def csa_compress_ex(h: Handle, x, z, pos_bias, cu_seqlens, cu_cmp, max_seqlen: int, ratio: int, overlap: bool,

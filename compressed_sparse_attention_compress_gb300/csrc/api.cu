@@ -135,6 +135,28 @@ csa_status_t csa_compress(csa_handle_t h, const void* x, const void* z, const fl
                                         T_cap, D, ratio, S, fp32, out, h->status, stream));
 }
 
+csa_status_t csa_compress_pair(csa_handle_t h, const void* x_kv, const void* z_kv, const float* pos_bias_kv,
+                               const void* x_I, const void* z_I, const float* pos_bias_I, const int32_t* cu,
+                               int B, int T_cap, int max_seqlen, int D, int d_I, int ratio, int overlap,
+                               csa_dtype_t dtype, int32_t* cu_cmp, void* kv_cmp, void* kI_cmp, cudaStream_t stream) {
+  if (!h || !x_kv || !z_kv || !pos_bias_kv || !x_I || !z_I || !pos_bias_I || !cu_cmp || !kv_cmp || !kI_cmp ||
+      !packing_ok(cu, B, T_cap, max_seqlen))
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(x_kv) || !aligned16(z_kv) || !aligned16(pos_bias_kv) || !aligned16(x_I) || !aligned16(z_I) ||
+      !aligned16(pos_bias_I) || !aligned16(kv_cmp) || !aligned16(kI_cmp))
+    return CSA_ERR_INVALID_ARG;
+  if ((dtype != CSA_BF16 && dtype != CSA_FP32) || (overlap != 0 && overlap != 1) || ratio < 1)
+    return CSA_ERR_INVALID_ARG;
+  const int S = overlap ? 2 * ratio : ratio;
+  const bool fp32 = dtype == CSA_FP32;
+  if (ratio > 128 || S > 256 || !csa::compress_pair_supported(D, d_I, ratio, S, fp32 ? 4 : 2))
+    return CSA_ERR_UNSUPPORTED;
+  DeviceGuard g(h->device);
+  if (!g.ok) return CSA_ERR_CUDA;
+  return from_cuda(csa::launch_compress_pair(x_kv, z_kv, pos_bias_kv, kv_cmp, D, x_I, z_I, pos_bias_I, kI_cmp, d_I,
+                                             cu, B, T_cap, ratio, S, fp32, cu_cmp, h->status, stream));
+}
+
 csa_status_t csa_compress_ex(csa_handle_t h, const void* x, const void* z, const void* x_prev,
                              const void* z_prev, const float* pos_bias, const float* norm_weight, float norm_eps,
                              int rope_dim, float rope_theta, int rope_pos_stride, int rope_pos_offset,

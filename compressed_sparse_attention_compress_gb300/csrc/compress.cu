@@ -44,6 +44,9 @@ namespace csa {
 
 namespace {
 
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
 __device__ __forceinline__ float ex2f(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -61,41 +64,55 @@ __device__ __forceinline__ void store_pair(float* p, float a, float b) {
   *reinterpret_cast<float2*>(p) = make_float2(a, b);
 }
 
-// Warp 0 finds the run of blockIdx.x: blockIdx.x counts chunks of E entries
-// over the sequences in order, 32 sequences at a time (one load round trip
-// each).  Writes the owning sequence (-1: past the last run) and the run's
-// entry range [j0, j1).
-__device__ __forceinline__ void locate_run(const int32_t* __restrict__ cu, int B, int r, int E, int* status,
-                                           int* s_b, int* s_j0, int* s_j1) {
-  const int lane = threadIdx.x;
-  int c = blockIdx.x, b = -1, n = 0;
+constexpr int kCuCache = 256;  // sequences whose offsets a CTA keeps in shared memory
+constexpr int kThreads = 256;  // 8 warps
+
+// Warp 0: the run with index c (runs of E entries over the sequences in order,
+// 32 sequences per load round trip) as (owning sequence or -1 past the last
+// run, first entry j0, end entry j1, the sequence's first compressed row).
+__device__ __forceinline__ int4 locate_run(const int32_t* cu, int B, int r, int E, int c, int* status) {
+  const int lane = (int)threadIdx.x & 31;
+  int b = -1, n = 0, ecarry = 0, cmp0 = 0;
   for (int base = 0; base < B && b < 0; base += 32) {
     const int bb = base + lane;
-    int L = bb < B ? __ldg(cu + bb + 1) - __ldg(cu + bb) : 0;
+    int L = bb < B ? cu[bb + 1] - cu[bb] : 0;
     if (L < 0) { raise_status(status, CSA_ERR_DEVICE_BOUNDS); L = 0; }
     const int nb = L / r;
     const int nch = (nb + E - 1) / E;
-    int incl = nch;
+    int incl = nch, ie = nb;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+      const int ve = __shfl_up_sync(0xffffffffu, ie, o);
+      if (lane >= o) { incl += v; ie += ve; }
     }
     const uint32_t hit = __ballot_sync(0xffffffffu, bb < B && c < incl);
     if (hit != 0u) {
-      const int w = __ffs(hit) - 1;  // first sequence whose chunks reach c
+      const int w = __ffs(hit) - 1;  // first sequence whose runs reach c
       b = base + w;
       c -= __shfl_sync(0xffffffffu, incl - nch, w);
       n = __shfl_sync(0xffffffffu, nb, w);
+      cmp0 = ecarry + __shfl_sync(0xffffffffu, ie - nb, w);
     } else {
       c -= __shfl_sync(0xffffffffu, incl, 31);
+      ecarry += __shfl_sync(0xffffffffu, ie, 31);
     }
   }
-  if (lane == 0) {
-    *s_b = b;
-    *s_j0 = c * E;
-    *s_j1 = b >= 0 ? min(c * E + E, n) : 0;
+  return make_int4(b, c * E, b >= 0 ? min(c * E + E, n) : 0, cmp0);
+}
+
+// Warp 0: the number of runs of E entries over all sequences.
+__device__ __forceinline__ int count_runs(const int32_t* cu, int B, int r, int E) {
+  const int lane = (int)threadIdx.x & 31;
+  int total = 0;
+  for (int base = 0; base < B; base += 32) {
+    const int bb = base + lane;
+    const int L = bb < B ? max(0, cu[bb + 1] - cu[bb]) : 0;
+    total += (L / r + E - 1) / E;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+  return total;
 }
 
 }  // namespace
@@ -120,70 +137,182 @@ struct CompressExArgs {
   int* status;
 };
 
+// The raw rows run `ri` reads, one contiguous span of each packed input stream:
+// x and z from the current-half rows on, x_prev and z_prev (when given) from
+// the run's first token on.  Staging layout: [x | z | x_prev | z_prev], each
+// rows_max x D.
+struct RunRows {
+  int tok0, cur0, Rc, Rp;
+};
+__device__ __forceinline__ RunRows run_rows(const CompressExArgs& a, int r, int S, int4 ri) {
+  const bool two = a.xp != nullptr;
+  const int tok0 = max(0, r * ri.y + r - S);  // first local token the run reads
+  const int tok1 = r * ri.z;                  // one past the last
+  const int cur0 = two ? r * ri.y : tok0;     // first token of the current-half rows
+  return RunRows{tok0, cur0, tok1 - cur0, two ? tok1 - r - tok0 : 0};
+}
+
+// Thread 0: bulk copies of the run's rows into `buf`, completing on `bar`.
+template <typename TIn, int D>
+__device__ __forceinline__ void stage_run(const CompressExArgs& a, int r, int S, int4 ri, int64_t seq0, uint32_t buf,
+                                          uint32_t bar) {
+  const RunRows rr = run_rows(a, r, S, ri);
+  const bool two = a.xp != nullptr;
+  const uint32_t region = (uint32_t)a.rows_max * D * sizeof(TIn);
+  const uint32_t bc = (uint32_t)rr.Rc * D * sizeof(TIn), bp = (uint32_t)rr.Rp * D * sizeof(TIn);
+  mbar_arrive_expect_tx(bar, 2u * (bc + bp));
+  constexpr uint32_t kPiece = 32768;
+  const TIn* src[4] = {static_cast<const TIn*>(a.x) + (seq0 + rr.cur0) * D,
+                       static_cast<const TIn*>(a.z) + (seq0 + rr.cur0) * D,
+                       two ? static_cast<const TIn*>(a.xp) + (seq0 + rr.tok0) * D : nullptr,
+                       two ? static_cast<const TIn*>(a.zp) + (seq0 + rr.tok0) * D : nullptr};
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t bytes = k < 2 ? bc : bp;
+    const char* g = reinterpret_cast<const char*>(src[k]);
+    for (uint32_t off = 0; off < bytes; off += kPiece)
+      bulk_g2s(buf + k * region + off, g + off, min(kPiece, bytes - off), bar);
+  }
+}
+
+// All threads: the entries of run `ri` from its rows staged in `smem_buf`.
 // kR, kS: the ratio and span when fixed at compile time (0: taken from a).
 template <typename TIn, typename TOut, int D, int kR, int kS>
-__global__ void __launch_bounds__(256) compress_ex_kernel(const __grid_constant__ CompressExArgs a) {
+__device__ __forceinline__ void compress_run(const CompressExArgs& a, int4 ri, const uint8_t* smem_buf) {
   constexpr int kPairs = D / 2;
   constexpr int kLanes = kPairs < 32 ? kPairs : 32;  // lanes per entry
   constexpr int kPerWarp = 32 / kLanes;              // entries per warp
   constexpr int kQ = kPairs / kLanes;                // channel pairs per lane
   constexpr float kLog2e = 1.4426950408889634f;
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ int s_b, s_j0, s_j1;
-
   const int r = kR ? kR : a.r, S = kS ? kS : a.S;
-  if (threadIdx.x < 32) locate_run(a.cu, a.B, r, a.E, a.status, &s_b, &s_j0, &s_j1);
-  __syncthreads();
-  const int b = s_b;
-  if (b < 0) return;
-  const int j0 = s_j0, j1 = s_j1;
   const bool two = a.xp != nullptr;
-  const int tok0 = max(0, r * j0 + r - S);   // first local token the run reads
-  const int tok1 = r * j1;                   // one past the last
-  const int cur0 = two ? r * j0 : tok0;      // first token of the current-half rows
-  const int Rc = tok1 - cur0;                // rows of x / z
-  const int Rp = two ? tok1 - r - tok0 : 0;  // rows of x_prev / z_prev
-  const int64_t seq0 = (int64_t)__ldg(a.cu + b);
+  const RunRows rr = run_rows(a, r, S, ri);
+  const int tok0 = rr.tok0, cur0 = rr.cur0;
+  const int j0 = ri.y, j1 = ri.z;
   const int region = a.rows_max * D;
-  TIn* sx = reinterpret_cast<TIn*>(smem);
-  TIn* sz = sx + region;
-  TIn* sxp = sz + region;
-  TIn* szp = sxp + region;
-  const uint32_t bar_a = smem_u32(&bar);
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar_a, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t bc = (uint32_t)Rc * D * sizeof(TIn), bp = (uint32_t)Rp * D * sizeof(TIn);
-    mbar_arrive_expect_tx(bar_a, 2u * (bc + bp));
-    constexpr uint32_t kPiece = 32768;
-    const TIn* src[4] = {static_cast<const TIn*>(a.x) + (seq0 + cur0) * D,
-                         static_cast<const TIn*>(a.z) + (seq0 + cur0) * D,
-                         two ? static_cast<const TIn*>(a.xp) + (seq0 + tok0) * D : nullptr,
-                         two ? static_cast<const TIn*>(a.zp) + (seq0 + tok0) * D : nullptr};
-    TIn* dst[4] = {sx, sz, sxp, szp};
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t bytes = k < 2 ? bc : bp;
-      const char* g = reinterpret_cast<const char*>(src[k]);
-      for (uint32_t off = 0; off < bytes; off += kPiece)
-        bulk_g2s(smem_u32(dst[k]) + off, g + off, min(kPiece, bytes - off), bar_a);
-    }
-  }
-  const bool ok = mbar_wait_bounded(bar_a, 0, a.status);
-  if (__syncthreads_or(!ok)) return;
-
+  const TIn* sx = reinterpret_cast<const TIn*>(smem_buf);
+  const TIn* sz = sx + region;
+  const TIn* sxp = sz + region;
+  const TIn* szp = sxp + region;
   const int lane = (int)threadIdx.x & 31, warp = (int)threadIdx.x >> 5;
   const int le = lane % kLanes, sub = lane / kLanes;
   const bool norm = a.gamma != nullptr;
   const int rope_lo = D - a.rope_dim;              // first rotated channel (D: none)
   const int usplit = two ? r : 0;                  // positions u < usplit read the previous half
-  TOut* out = static_cast<TOut*>(a.out) + (int64_t)__ldg(a.cu_cmp + b) * D;
+  TOut* out = static_cast<TOut*>(a.out) + (int64_t)ri.w * D;
   const int n = j1 - j0;
-  constexpr int kWarps = 256 / 32;
+  constexpr int kWarps = kThreads / 32;
+  if (S >= 64 && n == 1 && a.E == 1) {
+    // one long span per run (ratio 128): warp w reduces the span positions
+    // [w S/8, (w+1) S/8) of the entry, then warp 0 merges the eight partial
+    // softmax sums (max, sum of weights, weighted sum) and finishes the entry
+    const int j = j0;
+    const int first = r * j + r - S;
+    const int per = S / kWarps;
+    const int ulo = max(warp * per, max(0, -first)), uhi = (warp + 1) * per;
+    const TIn* xcur = sx + (first - cur0) * D;
+    const TIn* zcur = sz + (first - cur0) * D;
+    const TIn* xprv = two ? sxp + (first - tok0) * D : xcur;
+    const TIn* zprv = two ? szp + (first - tok0) * D : zcur;
+    float pm[2 * kQ], pd[2 * kQ], pn[2 * kQ];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const int c = 2 * (le + q * kLanes);
+      const float2* pcol = reinterpret_cast<const float2*>(a.P + c);
+      float m0 = -INFINITY, m1 = -INFINITY, d0 = 0.f, d1 = 0.f, n0 = 0.f, n1 = 0.f;
+      for (int u = ulo; u < uhi; ++u) {
+        const bool pv = u < usplit;
+        const float2 zz = load_pair((pv ? zprv : zcur) + u * D + c);
+        const float2 xx = load_pair((pv ? xprv : xcur) + u * D + c);
+        const float2 pp = __ldg(pcol + u * (D / 2));
+        const float l0 = zz.x + pp.x, l1 = zz.y + pp.y;
+        if (l0 > m0) {  // a new maximum: rescale the sums (m0 = -inf: they are 0)
+          const float sc = ex2f((m0 - l0) * kLog2e);
+          d0 *= sc;
+          n0 *= sc;
+          m0 = l0;
+        }
+        if (l1 > m1) {
+          const float sc = ex2f((m1 - l1) * kLog2e);
+          d1 *= sc;
+          n1 *= sc;
+          m1 = l1;
+        }
+        const float w0 = ex2f((l0 - m0) * kLog2e), w1 = ex2f((l1 - m1) * kLog2e);
+        d0 += w0;
+        d1 += w1;
+        n0 = fmaf(w0, xx.x, n0);
+        n1 = fmaf(w1, xx.y, n1);
+      }
+      pm[2 * q] = m0; pm[2 * q + 1] = m1;
+      pd[2 * q] = d0; pd[2 * q + 1] = d1;
+      pn[2 * q] = n0; pn[2 * q + 1] = n1;
+    }
+    __syncthreads();  // every warp has read the staged rows: the partials go over them
+    float* part = reinterpret_cast<float*>(const_cast<uint8_t*>(smem_buf));  // [warp][channel][3]
+    if (lane < kLanes) {
+#pragma unroll
+      for (int q = 0; q < kQ; ++q)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float* pp = part + ((size_t)warp * D + 2 * (le + q * kLanes) + h) * 3;
+          pp[0] = pm[2 * q + h];
+          pp[1] = pd[2 * q + h];
+          pp[2] = pn[2 * q + h];
+        }
+    }
+    __syncthreads();
+    if (warp != 0 || lane >= kLanes) return;
+    float y[2 * kQ];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = 2 * (le + q * kLanes) + h;
+        float m = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) m = fmaxf(m, part[((size_t)w * D + c) * 3]);
+        float den = 0.f, num = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+          const float* pp = part + ((size_t)w * D + c) * 3;
+          if (pp[0] == -INFINITY) continue;  // a warp whose positions were all left out
+          const float sc = ex2f((pp[0] - m) * kLog2e);
+          den = fmaf(pp[1], sc, den);
+          num = fmaf(pp[2], sc, num);
+        }
+        y[2 * q + h] = __fdividef(num, den);  // den >= 1: the maximum's own weight
+      }
+    if (norm) {
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < 2 * kQ; ++k) ss = fmaf(y[k], y[k], ss);
+      const uint32_t mask = kLanes == 32 ? 0xffffffffu : ((1u << kLanes) - 1u);
+#pragma unroll
+      for (int o = kLanes / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
+      const float inv = rsqrtf(ss * (1.0f / D) + a.eps);
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const float2 g = __ldg(reinterpret_cast<const float2*>(a.gamma + 2 * (le + q * kLanes)));
+        y[2 * q] *= inv * g.x;
+        y[2 * q + 1] *= inv * g.y;
+      }
+    }
+    const int64_t p = (int64_t)j * a.pos_stride + a.pos_offset;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const int c = 2 * (le + q * kLanes);
+      float y0 = y[2 * q], y1 = y[2 * q + 1];
+      if (c >= rope_lo) {
+        const uint64_t ph = (uint64_t)p * a.rope_turn[(c - rope_lo) >> 1];
+        const float ang = (float)(int32_t)(uint32_t)(ph >> 32) * 1.4629180792671596e-09f;  // 2 pi / 2^32
+        float sn, cs;
+        __sincosf(ang, &sn, &cs);
+        const float t0 = y0 * cs - y1 * sn;
+        y1 = y0 * sn + y1 * cs;
+        y0 = t0;
+      }
+      store_pair(out + (int64_t)j * D + c, y0, y1);
+    }
+    return;
+  }
   for (int e0 = warp * kPerWarp; e0 < n; e0 += kWarps * kPerWarp) {  // uniform within a warp
     const int e = e0 + sub;
     const bool active = e < n;
@@ -285,14 +414,126 @@ __global__ void __launch_bounds__(256) compress_ex_kernel(const __grid_constant_
   }
 }
 
-// Staging rows and entries per CTA: about 64 span rows per run, fewer when
-// `streams` staging buffers of that size would hold more than 40 KB (five
-// CTAs per SM keep copies in flight while others reduce), but at least one
-// entry per warp where the span allows.
+// One CTA processes runs g = blockIdx.x + i * gridDim.x of a combined list --
+// the runs of stream a0, then (D1 > 0) those of stream a1.  With two staging
+// buffers (nbuf = 2) the next run's rows are copied in while the current run
+// is reduced; when two do not fit (long spans of wide rows) one buffer is
+// refilled after each run.  Block 0 also writes the compressed offsets (when
+// cu_cmp_out is given).
+template <typename TIn, typename TOut, int D0, int D1, int kR, int kS>
+__global__ void __launch_bounds__(kThreads) compress_kernel(const __grid_constant__ CompressExArgs a0,
+                                                       const __grid_constant__ CompressExArgs a1, uint32_t buf_bytes,
+                                                       int nbuf, int32_t* __restrict__ cu_cmp_out) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t s_bar[2];
+  __shared__ int4 s_run[2];
+  __shared__ int s_which[2];
+  __shared__ int s_n0;
+  __shared__ int32_t s_cu[kCuCache + 1];  // the packing's offsets, on chip when B is small
+  const int tid = (int)threadIdx.x;
+  const int r = kR ? kR : a0.r, S = kS ? kS : a0.S;
+  const bool cached = a0.B <= kCuCache;
+  if (cached)
+    for (int i = tid; i <= a0.B; i += kThreads) s_cu[i] = __ldg(a0.cu + i);
+  const int32_t* cu = cached ? s_cu : a0.cu;  // both streams share the packing
+  if (tid == 0) {
+    mbar_init(smem_u32(&s_bar[0]), 1);
+    mbar_init(smem_u32(&s_bar[1]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int n0 = D1 > 0 ? count_runs(cu, a0.B, r, a0.E) : 0x7fffffff;
+    if (tid == 0) s_n0 = n0;
+    if (blockIdx.x == 0 && cu_cmp_out != nullptr) {  // cu_cmp[b] = sum_{b' < b} floor(L_b' / r)
+      int carry = 0;
+      if (tid == 0) {
+        cu_cmp_out[0] = 0;
+        if (cu[0] != 0) raise_status(a0.status, CSA_ERR_DEVICE_BOUNDS);
+      }
+      for (int base = 0; base < a0.B; base += 32) {
+        const int bb = base + tid;
+        const int n = bb < a0.B ? max(0, cu[bb + 1] - cu[bb]) / r : 0;
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (tid >= o) incl += v;
+        }
+        if (bb < a0.B) cu_cmp_out[bb + 1] = carry + incl;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+  }
+  __syncthreads();
+  const int n0 = s_n0;
+  // warp 0: run g of the combined list into slot `slot`
+  auto locate = [&](int g, int slot) {
+    int4 ri;
+    int which = 0;
+    if (g < n0) {
+      ri = locate_run(cu, a0.B, r, a0.E, g, a0.status);
+    } else {
+      ri = locate_run(cu, a1.B, r, a1.E, g - n0, a1.status);
+      which = 1;
+    }
+    if (tid == 0) {
+      s_run[slot] = ri;
+      s_which[slot] = which;
+    }
+  };
+  auto stage = [&](int slot, int bi) {  // thread 0: the run of meta slot `slot` into buffer bi
+    const uint32_t buf = smem_u32(smem) + (uint32_t)bi * buf_bytes, bar = smem_u32(&s_bar[bi]);
+    const int64_t seq0 = cu[s_run[slot].x];
+    if (s_which[slot] == 0) stage_run<TIn, D0>(a0, r, S, s_run[slot], seq0, buf, bar);
+    if constexpr (D1 > 0) {
+      if (s_which[slot] == 1) stage_run<TIn, D1>(a1, r, S, s_run[slot], seq0, buf, bar);
+    }
+  };
+  if (tid < 32) locate(blockIdx.x, 0);
+  __syncthreads();
+  if (tid == 0 && s_run[0].x >= 0) stage(0, 0);
+  for (int i = 0;; ++i) {
+    const int slot = i & 1;                          // metadata slot of run i
+    const int bi = nbuf == 2 ? slot : 0;             // its staging buffer
+    const uint32_t ph = nbuf == 2 ? (i >> 1) & 1u : i & 1u;
+    const int4 ri = s_run[slot];
+    const int which = s_which[slot];
+    if (ri.x < 0) break;  // uniform: every thread read the same slot after a barrier
+    if (tid < 32) locate(blockIdx.x + (i + 1) * gridDim.x, slot ^ 1);
+    __syncthreads();      // the next run is known; the other buffer was released at the end of run i - 1
+    const bool next = s_run[slot ^ 1].x >= 0;
+    if (nbuf == 2 && tid == 0 && next) {
+      fence_proxy_async_shared();
+      stage(slot ^ 1, bi ^ 1);
+    }
+    const bool ok = mbar_wait_bounded(smem_u32(&s_bar[bi]), ph, a0.status);
+    if (__syncthreads_or(!ok)) {
+      // leave no copy in flight into this CTA's shared memory
+      if (nbuf == 2 && tid == 0 && next) mbar_wait_bounded(smem_u32(&s_bar[bi ^ 1]), ((i + 1) >> 1) & 1u, a0.status);
+      return;
+    }
+    const uint8_t* buf = smem + (size_t)bi * buf_bytes;
+    if (which == 0) compress_run<TIn, TOut, D0, kR, kS>(a0, ri, buf);
+    if constexpr (D1 > 0) {
+      if (which == 1) compress_run<TIn, TOut, D1, kR, kS>(a1, ri, buf);
+    }
+    __syncthreads();      // this buffer and slot are free again
+    if (nbuf == 1 && tid == 0 && next) {  // one buffer: refill it now
+      fence_proxy_async_shared();
+      stage(slot ^ 1, 0);
+    }
+  }
+}
+
+// Staging rows and entries per run: about 64 span rows, fewer when `streams`
+// staging buffers of that size would hold more than 32 KB (each CTA holds two
+// runs' rows, and three CTAs per SM keep copies in flight while others
+// reduce), but at least one entry per warp where the span allows.
 static void compress_plan(int D, int r, int S, int in_bytes, int streams, int* rows_max, int* E, size_t* smem) {
   const size_t row_bytes = (size_t)streams * D * in_bytes;
   int e = S > 64 ? 1 : 64 / r;
-  const long long fit = ((long long)(40 * 1024 / row_bytes) - (S - r)) / r;
+  const long long fit = ((long long)(32 * 1024 / row_bytes) - (S - r)) / r;
   if (e > fit) e = (int)(fit < 1 ? 1 : fit);
   const int floor_e = S > 64 ? 1 : (64 / r < 8 ? 64 / r : 8);
   if (e < floor_e && row_bytes * (size_t)((S - r) + r * floor_e) <= 200 * 1024) e = floor_e;
@@ -308,15 +549,30 @@ bool compress_supported(int D, int r, int S, int in_bytes, bool two) {
   return smem <= 200 * 1024 && (D == 32 || D == 64 || D == 128 || D == 256 || D == 512);
 }
 
+// Grid of the persistent kernel: CTAs per SM by shared memory (two staging
+// buffers each), at most one per run.
+static int compress_nbuf(size_t buf_bytes) { return 2 * buf_bytes <= 200 * 1024 ? 2 : 1; }
+static unsigned compress_grid(size_t buf_bytes, long long runs) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long per_sm = (long long)(200 * 1024) / (long long)(compress_nbuf(buf_bytes) * buf_bytes + 1024);
+  if (per_sm > 2048 / kThreads) per_sm = 2048 / kThreads;
+  if (per_sm < 1) per_sm = 1;
+  const long long slots = per_sm * sms;
+  return (unsigned)(runs < slots ? (runs > 0 ? runs : 1) : slots);
+}
+
 template <typename TIn, typename TOut, int D, int kR, int kS>
 static cudaError_t launch_d(CompressExArgs& a, int T_cap, cudaStream_t stream) {
   size_t smem;
   compress_plan(D, a.r, a.S, (int)sizeof(TIn), a.xp ? 4 : 2, &a.rows_max, &a.E, &smem);
-  auto kern = compress_ex_kernel<TIn, TOut, D, kR, kS>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = compress_kernel<TIn, TOut, D, 0, kR, kS>;
+  const int nbuf = compress_nbuf(smem);
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(nbuf * smem));
   if (err != cudaSuccess) return err;
-  const long long chunks = (long long)T_cap / ((long long)a.r * a.E) + a.B + 1;
-  kern<<<(unsigned)chunks, 256, smem, stream>>>(a);
+  const long long runs = (long long)T_cap / ((long long)a.r * a.E) + a.B + 1;  // an upper bound
+  kern<<<compress_grid(smem, runs), kThreads, nbuf * smem, stream>>>(a, a, (uint32_t)smem, nbuf, nullptr);
   return cudaGetLastError();
 }
 
@@ -352,6 +608,51 @@ cudaError_t launch_compress(const void* x, const void* z, const void* x_prev, co
   }
   if (fp32) return launch_t<float, float>(a, D, T_cap, stream);
   return launch_t<__nv_bfloat16, __nv_bfloat16>(a, D, T_cap, stream);
+}
+
+template <typename TIn, typename TOut, int D0, int D1, int kR, int kS>
+static cudaError_t launch_pair_d(CompressExArgs& a0, CompressExArgs& a1, int T_cap, int32_t* cu_cmp,
+                                 cudaStream_t stream) {
+  size_t s0, s1;
+  compress_plan(D0, a0.r, a0.S, (int)sizeof(TIn), 2, &a0.rows_max, &a0.E, &s0);
+  compress_plan(D1, a1.r, a1.S, (int)sizeof(TIn), 2, &a1.rows_max, &a1.E, &s1);
+  const size_t smem = s0 > s1 ? s0 : s1;
+  auto kern = compress_kernel<TIn, TOut, D0, D1, kR, kS>;
+  const int nbuf = compress_nbuf(smem);
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(nbuf * smem));
+  if (err != cudaSuccess) return err;
+  const long long runs = (long long)T_cap / ((long long)a0.r * a0.E) + (long long)T_cap / ((long long)a1.r * a1.E) +
+                         2 * (long long)a0.B + 2;  // an upper bound
+  kern<<<compress_grid(smem, runs), kThreads, nbuf * smem, stream>>>(a0, a1, (uint32_t)smem, nbuf, cu_cmp);
+  return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut, int D0, int D1>
+static cudaError_t launch_pair_span(CompressExArgs& a0, CompressExArgs& a1, int T_cap, int32_t* cu_cmp,
+                                    cudaStream_t stream) {
+  if (a0.r == 4 && a0.S == 8) return launch_pair_d<TIn, TOut, D0, D1, 4, 8>(a0, a1, T_cap, cu_cmp, stream);
+  return launch_pair_d<TIn, TOut, D0, D1, 0, 0>(a0, a1, T_cap, cu_cmp, stream);
+}
+
+bool compress_pair_supported(int D, int D_I, int r, int S, int in_bytes) {
+  return ((D == 128 && D_I == 64) || (D == 64 && D_I == 32)) && compress_supported(D, r, S, in_bytes, false) &&
+         compress_supported(D_I, r, S, in_bytes, false);
+}
+
+cudaError_t launch_compress_pair(const void* x, const void* z, const float* P, void* out, int D, const void* x_i,
+                                 const void* z_i, const float* P_i, void* out_i, int D_I, const int32_t* cu, int B,
+                                 int T_cap, int r, int S, bool fp32, int32_t* cu_cmp, int* status,
+                                 cudaStream_t stream) {
+  CompressExArgs a0{x, z, nullptr, nullptr, P, nullptr, 0.f, 0, 0, 0, {}, cu, cu_cmp, B, r, S, 0, 0, out, status};
+  CompressExArgs a1{x_i, z_i, nullptr, nullptr, P_i, nullptr, 0.f, 0, 0, 0, {}, cu, cu_cmp, B, r, S, 0, 0, out_i,
+                    status};
+  if (D == 128 && D_I == 64)
+    return fp32 ? launch_pair_span<float, float, 128, 64>(a0, a1, T_cap, cu_cmp, stream)
+                : launch_pair_span<__nv_bfloat16, __nv_bfloat16, 128, 64>(a0, a1, T_cap, cu_cmp, stream);
+  if (D == 64 && D_I == 32)
+    return fp32 ? launch_pair_span<float, float, 64, 32>(a0, a1, T_cap, cu_cmp, stream)
+                : launch_pair_span<__nv_bfloat16, __nv_bfloat16, 64, 32>(a0, a1, T_cap, cu_cmp, stream);
+  return cudaErrorInvalidValue;
 }
 
 // cu_cmp[b] = sum_{b'<b} floor(L_b' / r); also checks cu_seqlens.

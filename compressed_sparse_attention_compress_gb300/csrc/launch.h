@@ -14,6 +14,13 @@ cudaError_t launch_compress(const void* x, const void* z, const void* x_prev, co
                             const float* gamma, float eps, int rope_dim, float theta, int pos_stride,
                             int pos_offset, const int32_t* cu, const int32_t* cu_cmp, int B, int T_cap, int D,
                             int r, int S, bool fp32, void* out, int* status, cudaStream_t stream);
+// The main KV (D) and indexer K (D_I) compressors of a layer in one launch,
+// plus the compressed offsets: (D, D_I) in {(128, 64), (64, 32)}.
+bool compress_pair_supported(int D, int D_I, int r, int S, int in_bytes);
+cudaError_t launch_compress_pair(const void* x, const void* z, const float* P, void* out, int D, const void* x_i,
+                                 const void* z_i, const float* P_i, void* out_i, int D_I, const int32_t* cu, int B,
+                                 int T_cap, int r, int S, bool fp32, int32_t* cu_cmp, int* status,
+                                 cudaStream_t stream);
 cudaError_t launch_compressed_offsets(const int32_t* cu, int B, int r, int32_t* cu_cmp, int* status,
                                       cudaStream_t stream);
 

@@ -52,6 +52,12 @@ class Forward:
     # individual stages -----------------------------------------------------
     def compress(self, stream=None):
         wl, x = self.wl, self.x
+        if (wl.compressor != "v4" and self.v_cmp is None and wl.H_I > 0
+                and (wl.d, wl.d_I) in ((128, 64), (64, 32))):
+            # both compressors and the compressed offsets in one launch
+            api.csa_compress_pair(self.h, x["x_kv"], x["z_kv"], x["P_kv"], x["x_I"], x["z_I"], x["P_I"], self.cu,
+                                  self.max_seqlen, wl.ratio, wl.overlap, self.cu_cmp, self.kv_cmp, self.kI, stream)
+            return
         api.csa_compressed_offsets(self.h, self.cu, wl.ratio, self.cu_cmp, stream)
         if wl.compressor == "v4":
             # previous-half stream (overlapping spans), RMSNorm and RoPE fused in

@@ -128,6 +128,24 @@ csa_status_t csa_compress(csa_handle_t handle, const void* x, const void* z,
                           int ratio, int overlap, csa_dtype_t dtype, void* out,
                           cudaStream_t stream);
 
+/* The two compressors of a CSA layer -- main KV and indexer K (§3: the
+ * indexer has its own compressor; §4: both reset at packed-sample
+ * boundaries) -- and their compressed offsets in one launch: the same results
+ * as csa_compressed_offsets followed by csa_compress for each stream, with
+ * one set of cu_seqlens, ratio and overlap.
+ *   x_kv, z_kv [T_cap, D], pos_bias_kv [S, D] -> kv_cmp [cu_cmp[B], D]
+ *   x_I,  z_I  [T_cap, d_I], pos_bias_I [S, d_I] -> kI_cmp [cu_cmp[B], d_I]
+ *   cu_cmp [B + 1] int32, written
+ * (D, d_I) must be (128, 64) or (64, 32) (CSA_ERR_UNSUPPORTED otherwise);
+ * other arguments and errors as csa_compress.  No counterpart call is named
+ * by the page: it fuses three of the calls above into one launch. */
+csa_status_t csa_compress_pair(csa_handle_t handle, const void* x_kv, const void* z_kv,
+                               const float* pos_bias_kv, const void* x_I, const void* z_I,
+                               const float* pos_bias_I, const int32_t* cu_seqlens, int B, int T_cap,
+                               int max_seqlen, int D, int d_I, int ratio, int overlap,
+                               csa_dtype_t dtype, int32_t* cu_cmp, void* kv_cmp, void* kI_cmp,
+                               cudaStream_t stream);
+
 /* Compressor variant: csa_compress with the extras that sit around the
  * compressor in a DeepSeek-V4 layer, fused before the single rounding of the
  * output (§10 "compressor softmax and normalization intermediates"; §12

@@ -60,8 +60,11 @@ def test_no_sample_in_a_region_reads_unsampled(bench):
 def test_launch_counts_follow_the_dispatch(bench):
     from compressed_sparse_attention_compress_gb300.inputs import WORKLOADS
     wl = WORKLOADS["warmup32k"]
-    # offsets, two compress calls, top-k + capacity fill, attention + capacity rows, KL zero + KL + finalize
-    assert bench.f_launches(wl) == 1 + 2 + 2 + 2 + 3
+    # both compressors with the offsets, top-k + capacity fill, attention + capacity rows, KL zero + KL + finalize
+    assert bench.f_launches(wl) == 1 + 2 + 2 + 3
+    # the v4 compressor: offsets and one call per stream
+    import dataclasses
+    assert bench.f_launches(dataclasses.replace(wl, compressor="v4")) == 1 + 2 + 2 + 2 + 3
     # attention backward: delta, capacity rows, kernel; indexer backward: one kernel
     assert bench.b_launches(wl) == 3 + 1
     assert bench.f_launches(WORKLOADS["hca64k"]) == 1 + 1 + 2
