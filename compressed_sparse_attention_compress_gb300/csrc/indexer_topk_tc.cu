@@ -11,15 +11,24 @@
 // One CTA takes a block of G consecutive queries of one sequence (G = 4, or 2
 // for very long sequences).  Their visible entries are a prefix of the
 // sequence's compressed rows, so the key tiles (128 entries x 64 dims) are
-// shared: a TMA warp streams them through a 4-stage pipeline, an MMA warp
-// computes I^T = kI qI^T (M = 128 entries, N = G x 8 query-heads) into a
-// double-buffered tensor-memory tile, and 8 compute warps turn each entry's
-// head scores into sum_h w ReLU(.) for their queries and store it in shared
-// memory as an order-preserving 32-bit key.  No score reaches global memory.
-// Then, per query, an exact radix select (11/11/10-bit digits, warp-aggregated
-// shared-memory histograms) finds the k-th largest key, and an ordered
-// compaction writes the selected entries in ascending index order (ties at
-// the threshold: smaller index first) as global compressed rows, -1 padded.
+// shared: a TMA warp streams them through a 2- or 4-stage pipeline, an MMA
+// warp computes I^T = kI qI^T (M = 128 entries, N = G x 8 query-heads) into a
+// double-buffered tensor-memory tile, and the compute warps turn each entry's
+// head scores into sum_h w ReLU(.) for their queries, store it in shared
+// memory (float) and track each query's score range.  No score reaches global
+// memory.  Then each warpgroup selects one query at a time, exactly:
+//   * a histogram of value-linear buckets over the query's [min, max] score
+//     (monotone in the score, so every entry in a bucket above the one that
+//     holds the k-th largest is selected, and only that bucket needs the
+//     exact order);
+//   * one pass counts, per warp segment, the entries above that bucket and
+//     lists the bucket's entries (order-preserving 32-bit key, index);
+//   * one warp finds the exact k-th largest key among them bit by bit and the
+//     number of entries equal to it still selected (ties: smaller index first);
+//     when the bucket holds more entries than the list, an exact 8-bit radix
+//     select over all the keys takes its place;
+//   * an ordered compaction writes the selected entries in ascending index
+//     order as global compressed rows, -1 padded.
 // Blocks whose queries all see at most k entries select everything without
 // scoring.
 #include <math.h>
@@ -53,7 +62,12 @@ namespace {
 
 constexpr int kHI = 8, kDI = 64;
 constexpr int kTK = 128;                 // entries per tile
-constexpr int kBins = 2048;
+// selection: value-linear buckets of one query's score range, then the list of
+// the entries in the threshold's bucket (key, index), in one 4 KB region per
+// selecting warpgroup
+constexpr int kSelBins = 1024;
+constexpr int kSelBytes = 4096;
+constexpr int kCand = kSelBytes / 8;
 constexpr uint32_t kTileBytes = kTK * 128;  // 16 KB
 constexpr uint32_t kQIOff = 0;              // up to 32 rows x 128 B
 constexpr uint32_t kStageOff = 4096;
@@ -63,7 +77,6 @@ constexpr uint32_t kStageOff = 4096;
 // scores).
 template <int CW>
 struct TopkCfg {
-  static constexpr int kWarps = CW;
   static constexpr int kStages = CW == 8 ? 2 : 4;
   static constexpr int kCtasPerSm = CW == 8 ? 2 : 1;
   static constexpr int kThreads = 32 * CW + 64;
@@ -74,6 +87,67 @@ __device__ __forceinline__ uint32_t order_key(float v) {
   if (v == 0.f) v = 0.f;  // -0 and +0 are the same score
   const uint32_t u = __float_as_uint(v);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The float of an order-preserving key (the inverse of order_key).
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// One warp: the need-th largest order key among the c candidates (key, entry
+// index) of `cand`, searched bit by bit below the bits every candidate shares;
+// then, per warp segment u (entry index / seg, four segments), the candidates
+// above it (g[u]) and equal to it (e[u]).  thr: that key; need_eq: how many of
+// the equal ones are still selected.  Every lane gets every result.
+__device__ __forceinline__ void resolve_candidates(const uint2* cand, int c, int need, int seg, int lane,
+                                                   uint32_t& thr, int& need_eq, int (&g)[4], int (&e)[4]) {
+  const bool regs = c <= 64;  // the common case: the keys stay in registers
+  const uint32_t r0 = (regs && lane < c) ? cand[lane].x : 0u;
+  const uint32_t r1 = (regs && lane + 32 < c) ? cand[lane + 32].x : 0u;
+  uint32_t kand = 0xFFFFFFFFu, kor = 0u;
+  for (int i = lane; i < c; i += 32) {
+    const uint32_t k = cand[i].x;
+    kand &= k;
+    kor |= k;
+  }
+  kand = __reduce_and_sync(0xffffffffu, kand);
+  kor = __reduce_or_sync(0xffffffffu, kor);
+  const uint32_t diff = kand ^ kor;
+  uint32_t pre = kand;
+  if (diff != 0u) {
+    const int top = 31 - __clz(diff);
+    pre = kand & ~((2u << top) - 1u);  // the shared leading bits (top = 31: none)
+    for (int bit = top; bit >= 0; --bit) {
+      const uint32_t trial = pre | (1u << bit);
+      int cnt = 0;
+      if (regs) {
+        cnt = (r0 >= trial ? 1 : 0) + (r1 >= trial ? 1 : 0);  // empty slots hold 0 < trial
+      } else {
+        for (int i = lane; i < c; i += 32) cnt += cand[i].x >= trial ? 1 : 0;
+      }
+      if (__reduce_add_sync(0xffffffffu, cnt) >= need) pre = trial;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) g[u] = e[u] = 0;
+  for (int i = lane; i < c; i += 32) {
+    const uint2 cd = cand[i];
+    const int w = (int)cd.y / seg;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      g[u] += (w == u && cd.x > pre) ? 1 : 0;
+      e[u] += (w == u && cd.x == pre) ? 1 : 0;
+    }
+  }
+  int gsum = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    g[u] = __reduce_add_sync(0xffffffffu, g[u]);
+    e[u] = __reduce_add_sync(0xffffffffu, e[u]);
+    gsum += g[u];
+  }
+  thr = pre;
+  need_eq = need - gsum;
 }
 
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -141,17 +215,19 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   __shared__ __align__(8) uint64_t s_qfull, s_qempty;
   __shared__ __align__(8) uint64_t s_drain;  // the MMA thread's last commit, before tensor memory is freed
   __shared__ float s_w[G][kHI];
-  __shared__ uint32_t s_hist[kBins];
-  __shared__ int s_scan[kComputeWarps];
-  __shared__ int s_cnt[2][kComputeWarps];
-  __shared__ uint32_t s_digit;
-  __shared__ int s_need, s_bincount;
+  constexpr int kSelWG = CW / 4;  // selecting warpgroups: one query each at a time
+  __shared__ uint32_t s_kmin[G], s_kmax[G];  // order keys: each query's visible score range
+  __shared__ int s_scan[kSelWG][4];
+  __shared__ int s_cnt[kSelWG][2][4];
+  __shared__ int s_bin[kSelWG], s_binneed[kSelWG], s_bincnt[kSelWG], s_ncand[kSelWG];
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  uint32_t* sKey = reinterpret_cast<uint32_t*>(smem_raw + (base - smem_u32(smem_raw)) + kKeysOff);
   const int vstride = (max_vis + 3) & ~3;
+  // scores (float, -0 stored as +0) of query q at [q * vstride, ...), then the selection regions
+  float* sScore = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)) + kKeysOff);
+  uint32_t* sSel = reinterpret_cast<uint32_t*>(sScore + (size_t)G * vstride);
   const uint32_t bar_full = smem_u32(&s_full[0]), bar_empty = smem_u32(&s_empty[0]);
   const uint32_t bar_dfull = smem_u32(&s_dfull[0]), bar_dfree = smem_u32(&s_dfree[0]);
   const uint32_t bar_qfull = smem_u32(&s_qfull), bar_qempty = smem_u32(&s_qempty);
@@ -264,8 +340,25 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
           if constexpr (kFp8) wv = q < bk.nq ? wv * __ldg(qs + wr) : 0.f;
           s_w[q][h] = wv;
         }
+        if (tid < G) {
+          s_kmin[tid] = 0xFFFFFFFFu;
+          s_kmax[tid] = 0u;
+        }
         named_sync(1, kComputeThreads);
         const bool active = g * kQPW < G;  // this warpgroup's queries exist in the tile
+        // the range of each of its queries' visible scores (order keys), for the selection's buckets
+        uint32_t kmn[kQPW], kmx[kQPW];
+        int nvq[kQPW];
+        float wq[kQPW][kHI];  // this warpgroup's head weights, in registers for the whole block
+#pragma unroll
+        for (int qq = 0; qq < kQPW; ++qq) {
+          const int q = g * kQPW + qq;
+          kmn[qq] = 0xFFFFFFFFu;
+          kmx[qq] = 0u;
+          nvq[qq] = q < bk.nq ? min((bk.q0 + q + bk.p0 + 1) / r, max_vis) : 0;
+#pragma unroll
+          for (int h = 0; h < kHI; ++h) wq[qq][h] = q < G ? s_w[q][h] : 0.f;
+        }
         for (int i = 0; i < bk.ntiles; ++i, ++it) {
           const uint32_t d = it & 1u;
           if (!mbar_wait_bounded(bar_dfull + 8 * d, (it >> 1) & 1u, status)) { s_abort = 1; break; }
@@ -287,9 +380,26 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
               const int q = g * kQPW + qq;
               float sc = 0.f;
 #pragma unroll
-              for (int h = 0; h < kHI; ++h) sc = fmaf(s_w[q][h], fmaxf(__uint_as_float(rv[qq * kHI + h]), 0.f), sc);
+              for (int h = 0; h < kHI; ++h) sc = fmaf(wq[qq][h], fmaxf(__uint_as_float(rv[qq * kHI + h]), 0.f), sc);
               if constexpr (kFp8) sc *= kscale;
-              sKey[(size_t)q * vstride + j] = order_key(sc);
+              if (sc == 0.f) sc = 0.f;  // -0 and +0 are the same score
+              sScore[(size_t)q * vstride + j] = sc;
+              if (j < nvq[qq]) {
+                const uint32_t key = order_key(sc);
+                kmn[qq] = min(kmn[qq], key);
+                kmx[qq] = max(kmx[qq], key);
+              }
+            }
+          }
+        }
+        if (active) {
+#pragma unroll
+          for (int qq = 0; qq < kQPW; ++qq) {
+            const uint32_t lo = __reduce_min_sync(0xffffffffu, kmn[qq]);
+            const uint32_t hi = __reduce_max_sync(0xffffffffu, kmx[qq]);
+            if (lane == 0 && nvq[qq] > 0) {
+              atomicMin(&s_kmin[g * kQPW + qq], lo);
+              atomicMax(&s_kmax[g * kQPW + qq], hi);
             }
           }
         }
@@ -297,149 +407,234 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
         if (*(volatile int*)&s_abort) break;
       }
       TK_ADD(5, tk_sc);
-      // ---- per query: select and write (each lane takes 4 consecutive entries) ----
-      for (int q = 0; q < bk.nq; ++q) {
-        const int t = bk.q0 + q;
-        const int64_t orow = (int64_t)(bk.seq0 + t) * k_pad;
-        const int n = min((t + bk.p0 + 1) / r, max_vis);
-        const int m = min(topk, n);
-        const uint32_t* keys = sKey + (size_t)q * vstride;
-        const bool all = n <= topk;
-        // selected: key > thr, plus the first need_eq entries with key == thr
-        uint32_t thr = 0;
-        int need_eq = 0;
-        if (!all) {
-          uint32_t prefix = 0, pmask = 0;
-          int need = m;
-          bool whole_bin = false;
-          for (int round = 0; round < 3 && !whole_bin; ++round) {
-            const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
-            const uint32_t dmask = round == 2 ? 0x3FFu : 0x7FFu;
-            const int nb = (int)dmask + 1;
-            TK_T0(tk_clr);
-            for (int b = tid; b < nb; b += kComputeThreads) s_hist[b] = 0;
-            named_sync(1, kComputeThreads);
-            TK_ADD(4, tk_clr);
-            TK_CNT(6);
-            TK_T0(tk_h);
-            for (int jb = warp * 128; jb < n; jb += kComputeWarps * 128) {
-              const int j0 = jb + 4 * lane;
-              uint4 k4 = make_uint4(0u, 0u, 0u, 0u);
-              if (j0 < n) k4 = *reinterpret_cast<const uint4*>(keys + j0);
-              const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+      // ---- selection: warpgroup sg selects queries sg, sg + kSelWG, ... one at a time ----
+      {
+        const int sg = warp >> 2, sw = warp & 3, st = tid & 127;
+        const int wg_bar = 2 + sg;
+        uint32_t* hist = sSel + sg * (kSelBytes / 4);
+        uint2* cand = reinterpret_cast<uint2*>(hist);
+        // The bin of this warpgroup's histogram of nb bins holding the need-th largest
+        // entry (thread st sums nb / 128 bins counted from the top): s_bin, the entries
+        // still needed inside it (s_binneed) and its count (s_bincnt).
+        auto find_bin = [&](int nb, int need) {
+          const int bpt = nb / 128;
+          const int hi_bin = nb - 1 - st * bpt;
+          int local = 0;
+          for (int kb = 0; kb < bpt; ++kb) local += (int)hist[hi_bin - kb];
+          int incl = local;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {  // plain shared atomics: cheaper here than warp-aggregating them
-                const bool ok = j0 + e < n && (kk[e] & pmask) == prefix;
-                if (ok) atomicAdd(&s_hist[(kk[e] >> shift) & dmask], 1u);
+          for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+          }
+          if (lane == 31) s_scan[sg][sw] = incl;
+          named_sync(wg_bar, 128);
+          int cum = incl - local;
+          for (int ww = 0; ww < sw; ++ww) cum += s_scan[sg][ww];
+          if (cum < need && need <= cum + local) {
+            for (int kb = 0; kb < bpt; ++kb) {
+              const int bin = hi_bin - kb;
+              const int hc = (int)hist[bin];
+              if (need <= cum + hc) {
+                s_bin[sg] = bin;
+                s_binneed[sg] = need - cum;
+                s_bincnt[sg] = hc;
+                break;
               }
+              cum += hc;
             }
-            named_sync(1, kComputeThreads);
-            TK_ADD(0, tk_h);
-            TK_T0(tk_s);
-            // thread tid owns bpt bins counted from the top
-            const int bpt = nb / kComputeThreads;
-            const int hi_bin = nb - 1 - tid * bpt;
-            int local = 0;
-            for (int kb = 0; kb < bpt; ++kb) local += (int)s_hist[hi_bin - kb];
-            int incl = local;
+          }
+          named_sync(wg_bar, 128);
+        };
+        for (int q = sg; q < bk.nq; q += kSelWG) {
+          const int t = bk.q0 + q;
+          const int64_t orow = (int64_t)(bk.seq0 + t) * k_pad;
+          const int n = min((t + bk.p0 + 1) / r, max_vis);
+          const int m = min(topk, n);
+          const float* sc = sScore + (size_t)q * vstride;
+          const bool all = n <= topk;
+          // warp sw of the warpgroup owns entries [j_lo, j_hi) (seg a multiple of 128)
+          const int seg = ((n + 4 * 128 - 1) / (4 * 128)) * 128;
+          const int j_lo = sw * seg, j_hi = min(n, j_lo + seg);
+          // selected: score > thr, then the first need_eq entries (by index) with score == thr;
+          // s_cnt[sg][0 / 1][w]: the entries of warp w's segment above / equal to thr
+          float thr = 0.f;
+          int need_eq = 0;
+          // selected entries of the earlier warps' segments: above thr / equal to it
+          int gt_before = 0, eq_before = 0;
+          bool from_cnt = true;  // from s_cnt (else already counted)
+          if (all) {
+            if (lane == 0) {
+              s_cnt[sg][0][sw] = max(0, j_hi - j_lo);
+              s_cnt[sg][1][sw] = 0;
+            }
+            named_sync(wg_bar, 128);
+          } else if (s_kmax[q] == s_kmin[q]) {
+            // every visible score equal: the first m by index
+            thr = key_float(s_kmax[q]);
+            need_eq = m;
+            if (lane == 0) {
+              s_cnt[sg][0][sw] = 0;
+              s_cnt[sg][1][sw] = max(0, j_hi - j_lo);
+            }
+            named_sync(wg_bar, 128);
+          } else {
+            // value-linear buckets over [vmin, vmax]: monotone in the score, so every entry of
+            // a bucket above the threshold's is selected and only that bucket needs the exact order
+            const float vmin = key_float(s_kmin[q]), vmax = key_float(s_kmax[q]);
+            const float span = vmax - vmin;
+            const float bscale = span < INFINITY ? (float)(kSelBins - 1) / span : 0.f;
+            auto bucket = [&](float v) { return min((int)((v - vmin) * bscale), kSelBins - 1); };
+            for (int b = st; b < kSelBins; b += 128) hist[b] = 0u;
+            if (st == 0) s_ncand[sg] = 0;
+            named_sync(wg_bar, 128);
+            for (int j0 = 4 * st; j0 < n; j0 += 512) {
+              const float4 v4 = *reinterpret_cast<const float4*>(sc + j0);
+              const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (j0 + e < n) atomicAdd(&hist[bucket(vv[e])], 1u);
+            }
+            named_sync(wg_bar, 128);
+            find_bin(kSelBins, m);
+            const int b0 = s_bin[sg], need = s_binneed[sg], c = s_bincnt[sg];
+            if (c <= kCand) {
+              // above bucket b0: selected; bucket b0: to the candidate list.  Lane l takes
+              // entries jb + 4 l .. jb + 4 l + 3 of each 128 (one 16-byte read)
+              int gt0 = 0;
+              for (int jb = j_lo; jb < j_hi; jb += 128) {
+                const int j0 = jb + 4 * lane;
+                const float4 v4 = j0 < j_hi ? *reinterpret_cast<const float4*>(sc + j0) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+                int bb[4], nc = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  bb[e] = j0 + e < j_hi ? bucket(vv[e]) : -1;
+                  gt0 += bb[e] > b0 ? 1 : 0;
+                  nc += bb[e] == b0 ? 1 : 0;
+                }
+                if (__any_sync(0xffffffffu, nc > 0)) {
+                  int incl = nc;
+#pragma unroll
+                  for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                  }
+                  int slot = 0;
+                  if (lane == 31) slot = atomicAdd(&s_ncand[sg], incl);
+                  slot = __shfl_sync(0xffffffffu, slot, 31) + incl - nc;
+#pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    if (bb[e] == b0) {
+                      if (slot < kCand) cand[slot] = make_uint2(order_key(vv[e]), (uint32_t)(j0 + e));
+                      ++slot;
+                    }
+                }
+              }
+              gt0 = __reduce_add_sync(0xffffffffu, gt0);
+              if (lane == 0) s_cnt[sg][0][sw] = gt0;
+              named_sync(wg_bar, 128);
+              // every warp resolves the threshold itself (no second barrier)
+              uint32_t tk;
+              int gc[4], ec[4];
+              resolve_candidates(cand, c, need, seg, lane, tk, need_eq, gc, ec);
+              thr = key_float(tk);
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if (u < sw) {
+                  gt_before += s_cnt[sg][0][u] + gc[u];
+                  eq_before += ec[u];
+                }
+              from_cnt = false;
+            } else {
+              // more entries share the threshold bucket than the list holds (heavy ties):
+              // exact radix select over the order keys, 8 bits a round
+              uint32_t prefix = 0u, pmask = 0u;
+              int needf = m;
+              for (int round = 0; round < 4; ++round) {
+                const int shift = 24 - 8 * round;
+                for (int b = st; b < 256; b += 128) hist[b] = 0u;
+                named_sync(wg_bar, 128);
+                for (int j0 = 4 * st; j0 < n; j0 += 512) {
+                  const float4 v4 = *reinterpret_cast<const float4*>(sc + j0);
+                  const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const uint32_t k = order_key(vv[e]);
+                    if (j0 + e < n && (k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 0xFFu], 1u);
+                  }
+                }
+                named_sync(wg_bar, 128);
+                find_bin(256, needf);
+                prefix |= (uint32_t)s_bin[sg] << shift;
+                pmask |= 0xFFu << shift;
+                needf = s_binneed[sg];
+              }
+              thr = key_float(prefix);
+              need_eq = needf;
+              int gt = 0, eq = 0;
+              for (int j = j_lo + lane; j < j_hi; j += 32) {
+                const float v = sc[j];
+                gt += v > thr ? 1 : 0;
+                eq += v == thr ? 1 : 0;
+              }
+              gt = __reduce_add_sync(0xffffffffu, gt);
+              eq = __reduce_add_sync(0xffffffffu, eq);
+              if (lane == 0) {
+                s_cnt[sg][0][sw] = gt;
+                s_cnt[sg][1][sw] = eq;
+              }
+              named_sync(wg_bar, 128);
+            }
+          }
+          if (from_cnt)
+            for (int ww = 0; ww < sw; ++ww) {
+              gt_before += s_cnt[sg][0][ww];
+              eq_before += s_cnt[sg][1][ww];
+            }
+          // write pass: lane l takes entries jb + 4 l .. jb + 4 l + 3 of each 128 (one 16-byte
+          // read); a warp scan of the per-lane counts places the selected entries in index order
+          for (int jb = j_lo; jb < j_hi; jb += 128) {
+            const int j0 = jb + 4 * lane;
+            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!all && j0 < j_hi) v4 = *reinterpret_cast<const float4*>(sc + j0);
+            const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+            bool fg[4], fe[4];
+            int ng = 0, ne = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const bool in = j0 + e < j_hi;
+              fg[e] = in && (all || vv[e] > thr);
+              fe[e] = in && !all && vv[e] == thr;
+              ng += fg[e] ? 1 : 0;
+              ne += fe[e] ? 1 : 0;
+            }
+            int ig = ng, ie = ne;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-              const int v = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += v;
-            }
-            if (lane == 31) s_scan[warp] = incl;
-            named_sync(1, kComputeThreads);
-            int above = incl - local;
-            for (int ww = 0; ww < warp; ++ww) above += s_scan[ww];
-            if (above < need && need <= above + local) {
-              int cum = above;
-              for (int kb = 0; kb < bpt; ++kb) {
-                const int bin = hi_bin - kb;
-                const int hc = (int)s_hist[bin];
-                if (need <= cum + hc) {
-                  s_digit = (uint32_t)bin;
-                  s_need = need - cum;
-                  s_bincount = hc;
-                  break;
-                }
-                cum += hc;
+              const int a = __shfl_up_sync(0xffffffffu, ig, o);
+              const int b = __shfl_up_sync(0xffffffffu, ie, o);
+              if (lane >= o) {
+                ig += a;
+                ie += b;
               }
             }
-            named_sync(1, kComputeThreads);
-            prefix |= s_digit << shift;
-            pmask |= dmask << shift;
-            need = s_need;
-            // the bin holds exactly the entries still needed: all of it is selected
-            whole_bin = s_bincount == need && prefix != 0u;
-            named_sync(1, kComputeThreads);
-            TK_ADD(1, tk_s);
-          }
-          if (whole_bin) {
-            thr = prefix - 1u;  // every key >= prefix (lower digits free) is selected
-            need_eq = 0;
-          } else {
-            thr = prefix;
-            need_eq = need;
-          }
-        }
-        // ordered compaction: warp w scans [w*seg, (w+1)*seg), seg a multiple of 128
-        const int seg = ((n + kComputeWarps * 128 - 1) / (kComputeWarps * 128)) * 128;
-        const int j_lo = warp * seg, j_hi = min(n, j_lo + seg);
-        auto flags_of = [&](int j0, uint32_t (&kk)[4], int& cgt, int& ceq) {
-          uint4 k4 = make_uint4(0u, 0u, 0u, 0u);
-          if (!all && j0 < j_hi) k4 = *reinterpret_cast<const uint4*>(keys + j0);
-          kk[0] = k4.x; kk[1] = k4.y; kk[2] = k4.z; kk[3] = k4.w;
-          cgt = 0;
-          ceq = 0;
+            int pg = gt_before + ig - ng, pe = eq_before + ie - ne;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const bool in = j0 + e < j_hi;
-            cgt += (in && (all || kk[e] > thr)) ? 1 : 0;
-            ceq += (in && !all && kk[e] == thr) ? 1 : 0;
+            for (int e = 0; e < 4; ++e) {
+              if (fg[e]) idx[orow + pg + min(pe, need_eq)] = bk.cmp0 + j0 + e;
+              if (fe[e] && pe < need_eq) idx[orow + pg + pe] = bk.cmp0 + j0 + e;
+              pg += fg[e] ? 1 : 0;
+              pe += fe[e] ? 1 : 0;
+            }
+            gt_before += __shfl_sync(0xffffffffu, ig, 31);
+            eq_before += __shfl_sync(0xffffffffu, ie, 31);
           }
-        };
-        TK_T0(tk_c);
-        TK_CNT(7);
-        int gt = 0, eq = 0;
-        for (int jb = j_lo; jb < j_hi; jb += 128) {
-          uint32_t kk[4];
-          int cgt, ceq;
-          flags_of(jb + 4 * lane, kk, cgt, ceq);
-          gt += cgt;
-          eq += ceq;
+          for (int i = m + st; i < k_pad; i += 128) idx[orow + i] = -1;
+          named_sync(wg_bar, 128);  // s_cnt and the histogram are reused by this warpgroup's next query
         }
-        gt = __reduce_add_sync(0xffffffffu, gt);
-        eq = __reduce_add_sync(0xffffffffu, eq);
-        if (lane == 0) { s_cnt[0][warp] = gt; s_cnt[1][warp] = eq; }
-        named_sync(1, kComputeThreads);
-        TK_ADD(2, tk_c);
-        TK_T0(tk_w);
-        int gt_before = 0, eq_before = 0;
-        for (int ww = 0; ww < warp; ++ww) { gt_before += s_cnt[0][ww]; eq_before += s_cnt[1][ww]; }
-        // write pass, 128 consecutive entries per step as four rounds of 32 (entry jb + 32 e + lane):
-        // one ballot per round and flag gives every lane the count of selected entries ahead of its
-        // own, and the selected entries of a round go to consecutive slots (coalesced stores)
-        const uint32_t lt = (1u << lane) - 1u;
-        for (int jb = j_lo; jb < j_hi; jb += 128) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = jb + 32 * e + lane;
-            const bool in = j < j_hi;
-            const uint32_t kv = (!all && in) ? keys[j] : 0u;
-            const bool fg = in && (all || kv > thr);
-            const bool fe = in && !all && kv == thr;
-            const uint32_t bg = __ballot_sync(0xffffffffu, fg);
-            const uint32_t be = __ballot_sync(0xffffffffu, fe);
-            const int my_gt = gt_before + __popc(bg & lt), my_eq = eq_before + __popc(be & lt);
-            if (fg || (fe && my_eq < need_eq)) idx[orow + my_gt + min(my_eq, need_eq)] = bk.cmp0 + j;
-            gt_before += __popc(bg);
-            eq_before += __popc(be);
-          }
-        }
-        for (int i = m + tid; i < k_pad; i += kComputeThreads) idx[orow + i] = -1;
-        named_sync(1, kComputeThreads);
-        TK_ADD(3, tk_w);
       }
+      named_sync(1, kComputeThreads);  // every query of the block is written: its scores may be overwritten
     }
   }
 
@@ -458,12 +653,12 @@ extern "C" int csa_topk_profile(unsigned long long* out16) {
 #endif
 
 // Shared memory a CTA may use for scores: per-SM capacity split over the CTAs
-// resident on it, less static arrays (about 10 KB), the 1 KB every block
-// reserves, alignment slack and the fixed front part.
+// resident on it, less static arrays (under 2 KB), the 1 KB every block
+// reserves, alignment slack, the fixed front part and the selection regions.
 template <int CW>
 static size_t topk_key_budget() {
   const size_t per_cta = 233472 / TopkCfg<CW>::kCtasPerSm;
-  return per_cta - 10 * 1024 - 1024 - 1024 - TopkCfg<CW>::kKeysOff;
+  return per_cta - 2 * 1024 - 1024 - 1024 - TopkCfg<CW>::kKeysOff - (size_t)(CW / 4) * kSelBytes;
 }
 
 struct TopkShape {
@@ -473,8 +668,8 @@ struct TopkShape {
 static TopkShape topk_tc_shape(int max_vis) {
   const size_t per_query = (size_t)((max_vis + 3) & ~3) * 4;
   if (4 * per_query <= topk_key_budget<8>()) return {4, 8};
-  if (2 * per_query <= topk_key_budget<8>()) return {2, 8};
   if (4 * per_query <= topk_key_budget<16>()) return {4, 16};
+  if (2 * per_query <= topk_key_budget<8>()) return {2, 8};
   if (2 * per_query <= topk_key_budget<16>()) return {2, 16};
   return {0, 0};
 }
@@ -499,7 +694,8 @@ static cudaError_t launch_topk_tc_t(const void* qI, const float* qs, const void*
              !make_tmap_bf16_sw128(&mki, kI, n_cmp_rows, kDI, kTK)) {
     return cudaErrorInvalidValue;
   }
-  const size_t smem = 1024 + TopkCfg<CW>::kKeysOff + (size_t)G * ((max_vis + 3) & ~3) * 4;
+  const size_t smem =
+      1024 + TopkCfg<CW>::kKeysOff + (size_t)G * ((max_vis + 3) & ~3) * 4 + (size_t)(CW / 4) * kSelBytes;
   auto kern = indexer_topk_tc_kernel<G, CW, kFp8>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
