@@ -13,7 +13,7 @@
 // sequence's compressed rows, so the key tiles (128 entries x 64 dims) are
 // shared: a TMA warp streams them through a 2- or 4-stage pipeline, an MMA
 // warp computes I^T = kI qI^T (M = 128 entries, N = G x 8 query-heads) into a
-// double-buffered tensor-memory tile, and the compute warps turn each entry's
+// four-deep ring of tensor-memory tiles, and the compute warps turn each entry's
 // head scores into sum_h w ReLU(.) for their queries, store it in shared
 // memory (float) and track each query's score range.  No score reaches global
 // memory.  Then each warpgroup selects one query at a time, exactly:
@@ -69,6 +69,7 @@ constexpr int kSelBins = 1024;
 constexpr int kSelBytes = 4096;
 constexpr int kCand = kSelBytes / 8;
 constexpr uint32_t kTileBytes = kTK * 128;  // 16 KB
+constexpr int kDBufs = 4;                   // score tiles in tensor memory (32 columns each)
 constexpr uint32_t kQIOff = 0;              // up to 32 rows x 128 B
 constexpr uint32_t kStageOff = 4096;
 
@@ -211,7 +212,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   constexpr int kQPW = G * 4 / CW > 1 ? G * 4 / CW : 1;  // queries scored per warpgroup
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_dfull[2], s_dfree[2];
+  __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_dfull[kDBufs], s_dfree[kDBufs];
   __shared__ __align__(8) uint64_t s_qfull, s_qempty;
   __shared__ __align__(8) uint64_t s_drain;  // the MMA thread's last commit, before tensor memory is freed
   __shared__ float s_w[G][kHI];
@@ -233,7 +234,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   const uint32_t bar_qfull = smem_u32(&s_qfull), bar_qempty = smem_u32(&s_qempty);
 
   if (warp == kComputeWarps + 1) {
-    tc::tmem_alloc(smem_u32(&s_tmem), 64);
+    tc::tmem_alloc(smem_u32(&s_tmem), 32 * kDBufs);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
@@ -241,7 +242,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kDBufs; ++i) {
       mbar_init(bar_dfull + 8 * i, 1);
       mbar_init(bar_dfree + 8 * i, kComputeWarps);
     }
@@ -289,9 +290,9 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
         if (!mbar_wait_bounded(bar_qfull, nblk & 1u, status)) { s_abort = 1; break; }
         ++nblk;
         for (int i = 0; i < bk.ntiles; ++i, ++it) {
-          const uint32_t s = it % kStages, d = it & 1u;
+          const uint32_t s = it % kStages, d = it % kDBufs;
           if (!mbar_wait_bounded(bar_full + 8 * s, (it / kStages) & 1u, status) ||
-              !mbar_wait_bounded(bar_dfree + 8 * d, ((it >> 1) & 1u) ^ 1u, status)) {
+              !mbar_wait_bounded(bar_dfree + 8 * d, ((it / kDBufs) & 1u) ^ 1u, status)) {
             s_abort = 1;
             break;
           }
@@ -360,8 +361,8 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
           for (int h = 0; h < kHI; ++h) wq[qq][h] = q < G ? s_w[q][h] : 0.f;
         }
         for (int i = 0; i < bk.ntiles; ++i, ++it) {
-          const uint32_t d = it & 1u;
-          if (!mbar_wait_bounded(bar_dfull + 8 * d, (it >> 1) & 1u, status)) { s_abort = 1; break; }
+          const uint32_t d = it % kDBufs;
+          if (!mbar_wait_bounded(bar_dfull + 8 * d, (it / kDBufs) & 1u, status)) { s_abort = 1; break; }
           tc::fence_after_sync();
           uint32_t rv[8 * kQPW];
           if (active) {
@@ -463,6 +464,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
           // selected entries of the earlier warps' segments: above thr / equal to it
           int gt_before = 0, eq_before = 0;
           bool from_cnt = true;  // from s_cnt (else already counted)
+          int eq_total = 0;      // entries equal to thr over the whole query
           if (all) {
             if (lane == 0) {
               s_cnt[sg][0][sw] = max(0, j_hi - j_lo);
@@ -540,11 +542,13 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
               resolve_candidates(cand, c, need, seg, lane, tk, need_eq, gc, ec);
               thr = key_float(tk);
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
+              for (int u = 0; u < 4; ++u) {
                 if (u < sw) {
                   gt_before += s_cnt[sg][0][u] + gc[u];
                   eq_before += ec[u];
                 }
+                eq_total += ec[u];
+              }
               from_cnt = false;
             } else {
               // more entries share the threshold bucket than the list holds (heavy ties):
@@ -588,47 +592,74 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
             }
           }
           if (from_cnt)
-            for (int ww = 0; ww < sw; ++ww) {
-              gt_before += s_cnt[sg][0][ww];
-              eq_before += s_cnt[sg][1][ww];
+            for (int ww = 0; ww < 4; ++ww) {
+              if (ww < sw) {
+                gt_before += s_cnt[sg][0][ww];
+                eq_before += s_cnt[sg][1][ww];
+              }
+              eq_total += s_cnt[sg][1][ww];
             }
-          // write pass: lane l takes entries jb + 4 l .. jb + 4 l + 3 of each 128 (one 16-byte
-          // read); a warp scan of the per-lane counts places the selected entries in index order
-          for (int jb = j_lo; jb < j_hi; jb += 128) {
-            const int j0 = jb + 4 * lane;
-            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (!all && j0 < j_hi) v4 = *reinterpret_cast<const float4*>(sc + j0);
-            const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-            bool fg[4], fe[4];
-            int ng = 0, ne = 0;
+          if (all || eq_total == need_eq) {
+            // every entry equal to thr is selected: the selected set is score >= thr (all: every
+            // entry).  Entry jb + 32 e + lane per round: one ballot places a round's entries in
+            // index order, in consecutive slots (coalesced stores)
+            const uint32_t lt = (1u << lane) - 1u;
+            int at = gt_before + eq_before;
+            for (int jb = j_lo; jb < j_hi; jb += 128) {
+              float vv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const bool in = j0 + e < j_hi;
-              fg[e] = in && (all || vv[e] > thr);
-              fe[e] = in && !all && vv[e] == thr;
-              ng += fg[e] ? 1 : 0;
-              ne += fe[e] ? 1 : 0;
-            }
-            int ig = ng, ie = ne;
+              for (int e = 0; e < 4; ++e) {
+                const int j = jb + 32 * e + lane;
+                vv[e] = (!all && j < j_hi) ? sc[j] : 0.f;
+              }
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const int a = __shfl_up_sync(0xffffffffu, ig, o);
-              const int b = __shfl_up_sync(0xffffffffu, ie, o);
-              if (lane >= o) {
-                ig += a;
-                ie += b;
+              for (int e = 0; e < 4; ++e) {
+                const int j = jb + 32 * e + lane;
+                const bool f = j < j_hi && (all || vv[e] >= thr);
+                const uint32_t bm = __ballot_sync(0xffffffffu, f);
+                if (f) idx[orow + at + __popc(bm & lt)] = bk.cmp0 + j;
+                at += __popc(bm);
               }
             }
-            int pg = gt_before + ig - ng, pe = eq_before + ie - ne;
+          } else {
+            // write pass: lane l takes entries jb + 4 l .. jb + 4 l + 3 of each 128 (one 16-byte
+            // read); a warp scan of the per-lane counts places the selected entries in index order
+            for (int jb = j_lo; jb < j_hi; jb += 128) {
+              const int j0 = jb + 4 * lane;
+              float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (!all && j0 < j_hi) v4 = *reinterpret_cast<const float4*>(sc + j0);
+              const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+              bool fg[4], fe[4];
+              int ng = 0, ne = 0;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (fg[e]) idx[orow + pg + min(pe, need_eq)] = bk.cmp0 + j0 + e;
-              if (fe[e] && pe < need_eq) idx[orow + pg + pe] = bk.cmp0 + j0 + e;
-              pg += fg[e] ? 1 : 0;
-              pe += fe[e] ? 1 : 0;
+              for (int e = 0; e < 4; ++e) {
+                const bool in = j0 + e < j_hi;
+                fg[e] = in && (all || vv[e] > thr);
+                fe[e] = in && !all && vv[e] == thr;
+                ng += fg[e] ? 1 : 0;
+                ne += fe[e] ? 1 : 0;
+              }
+              int ig = ng, ie = ne;
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1) {
+                const int a = __shfl_up_sync(0xffffffffu, ig, o);
+                const int b = __shfl_up_sync(0xffffffffu, ie, o);
+                if (lane >= o) {
+                  ig += a;
+                  ie += b;
+                }
+              }
+              int pg = gt_before + ig - ng, pe = eq_before + ie - ne;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if (fg[e]) idx[orow + pg + min(pe, need_eq)] = bk.cmp0 + j0 + e;
+                if (fe[e] && pe < need_eq) idx[orow + pg + pe] = bk.cmp0 + j0 + e;
+                pg += fg[e] ? 1 : 0;
+                pe += fe[e] ? 1 : 0;
+              }
+              gt_before += __shfl_sync(0xffffffffu, ig, 31);
+              eq_before += __shfl_sync(0xffffffffu, ie, 31);
             }
-            gt_before += __shfl_sync(0xffffffffu, ig, 31);
-            eq_before += __shfl_sync(0xffffffffu, ie, 31);
           }
           for (int i = m + st; i < k_pad; i += 128) idx[orow + i] = -1;
           named_sync(wg_bar, 128);  // s_cnt and the histogram are reused by this warpgroup's next query
@@ -641,7 +672,7 @@ indexer_topk_tc_kernel(const __grid_constant__ CUtensorMap map_qi, const __grid_
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == kComputeWarps + 1) tc::tmem_dealloc(tmem, 64);
+  if (warp == kComputeWarps + 1) tc::tmem_dealloc(tmem, 32 * kDBufs);
 }
 
 #ifdef CSA_TOPK_PROFILE
