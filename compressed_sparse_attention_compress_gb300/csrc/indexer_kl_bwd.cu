@@ -419,6 +419,7 @@ static cudaError_t kl_bwd_dims(const KLBwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_indexer_kl_bwd(const KLBwdArgs& a, bool fp32, cudaStream_t stream) {
   if (a.T_cap <= 0) return cudaSuccess;
   if (indexer_kl_bwd_tc_supported(a, fp32)) return launch_indexer_kl_bwd_tc(a, stream);
+  if (indexer_kl_bwd_sparse_tc_supported(a, fp32)) return launch_indexer_kl_bwd_sparse_tc(a, stream);
   cudaError_t err = cudaMemsetAsync(a.dkI, 0, (size_t)a.n_cmp_cap * a.d_I * 4, stream);
   if (err != cudaSuccess) return err;
   return fp32 ? kl_bwd_dims<float>(a, stream) : kl_bwd_dims<__nv_bfloat16>(a, stream);

@@ -177,5 +177,9 @@ cudaError_t launch_indexer_kl_bwd(const KLBwdArgs& a, bool fp32, cudaStream_t st
 // bf16, both normalisers given); launch_indexer_kl_bwd dispatches to it.
 bool indexer_kl_bwd_tc_supported(const KLBwdArgs& a, bool fp32);
 cudaError_t launch_indexer_kl_bwd_tc(const KLBwdArgs& a, cudaStream_t stream);
+// tcgen05 one-pass backward of the selected-set teacher (same shapes, both
+// normalisers given, gathered 128-entry tiles); launch_indexer_kl_bwd dispatches to it.
+bool indexer_kl_bwd_sparse_tc_supported(const KLBwdArgs& a, bool fp32);
+cudaError_t launch_indexer_kl_bwd_sparse_tc(const KLBwdArgs& a, cudaStream_t stream);
 
 }  // namespace csa

@@ -154,6 +154,30 @@ def test_one_pass_dense_tensor_core_path_ragged(grad_scale):
     _run([1029, 3, 0, 517, 130, 4600], "dense", stats=True, seed=6, grad_scale=grad_scale)
 
 
+@pytest.mark.parametrize("grad_scale", [1.0, -3.0])
+def test_one_pass_sparse_tensor_core_path_several_tiles(grad_scale):
+    # the selected teacher with both forward normalisers at 64 x 128 heads and an
+    # 8 x 64 indexer runs the tcgen05 kernel: gathered 128-entry tiles, one to
+    # three per query (holes where a slot is -1), an empty sequence and
+    # sequences shorter than one compressed block; every row against the oracle
+    _run([900, 3, 0, 517, 1300], "sparse", topk=300, k_pad=384, stats=True, seed=7, grad_scale=grad_scale)
+
+
+def test_full_size_sparse_layer_sampled():
+    # the selected teacher at L = 8192, k = 512 (the CSA sparse-mode layer, one
+    # pass on the tensor cores): dqI and dw on sampled rows against the oracle;
+    # dkI through the homogeneity identity sum kI.dkI = sum w.dw
+    L = 8192
+    rng = np.random.default_rng(2)
+    rows = np.sort(np.concatenate([rng.choice(L, 24, replace=False), [3, 4, 2047, L - 1]]))
+    res = _run([L], "sparse", topk=512, k_pad=512, rows=rows, check_kI=False, cap_align=128, stats=True,
+               check_stats=False, seed=8)
+    f64 = lambda t: t.double()  # noqa: E731
+    lhs = (f64(res["dkI"][:res["n_c"]]) * f64(res["kI"][:res["n_c"]])).sum()
+    rhs = (f64(res["dw"]) * f64(res["w"])).sum()
+    assert abs(float(lhs - rhs)) <= 2e-2 * max(1e-3, float((f64(res["dw"]).abs() * f64(res["w"]).abs()).sum()))
+
+
 @pytest.mark.parametrize("stats", [False, True])
 def test_full_size_dense_warmup_layer_sampled(stats):
     # the dense teacher at L = 32768 (with the forward's normalisers: the
