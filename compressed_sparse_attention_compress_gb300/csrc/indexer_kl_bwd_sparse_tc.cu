@@ -24,7 +24,9 @@
 // threads write: the K-major A operand of dkI and the MN-major B operand of
 // dqI^T.  dqI^T accumulates in tensor memory over the query's tiles; each dkI
 // tile is added to the float32 gradient rows of the gathered entries with
-// red.global.add by the warpgroup that computed it.  The MMA warp issues a
+// red.global.add by the warpgroup that computed it, read in the 16x256b shape
+// so that every reduction instruction fills whole 32-byte sectors.  Three
+// gathered tiles are in flight when the index rows leave room, else two.  The MMA warp issues a
 // tile's gradient products after the next tile's scores, so the compute
 // warpgroups never wait on their own products.
 // Warp roles: six producer warps (warp 8 resolves the index slots; all six
@@ -46,7 +48,6 @@ using namespace ws;
 
 constexpr int kNH = 64, kDim = 128, kHI = 8, kDI = 64;
 constexpr int kTK = 128;                               // entries per tile
-constexpr int kStages = 2;
 constexpr int kComputeWarps = 8;                       // two warpgroups
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kProdWarps = 6;                          // warps 8-13
@@ -74,9 +75,7 @@ constexpr uint32_t kQOff = 0;                          // [2 slots]
 constexpr uint32_t kQIOff = 2 * kQBytes;               // [2 slots]
 constexpr uint32_t kAuxOff = kQIOff + 2 * kQIBytes;    // [2 slots]
 constexpr uint32_t kCOff = kAuxOff + 1024;             // [2 buffers], 1024-aligned
-constexpr uint32_t kStageOff = kCOff + 2 * kCBytes;    // [kStages]
-constexpr uint32_t kIdxOff = kStageOff + kStages * kStageBytes;  // [2 slots][k_pad] index rows
-constexpr uint32_t kSmem = kIdxOff;                                // + 8 k_pad bytes
+constexpr uint32_t kStageOff = kCOff + 2 * kCBytes;    // [stages], then [2 slots][k_pad] index rows
 static_assert(kCOff % 1024 == 0 && kStageOff % 1024 == 0, "swizzle atom alignment");
 
 // tensor memory: per buffer b (= tile parity, = the warpgroup that reads it)
@@ -102,14 +101,15 @@ __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(__uint_as_float(a)),
-               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+__device__ __forceinline__ void red_add_v2(float* p, uint32_t a, uint32_t b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};\n" ::"l"(p), "f"(__uint_as_float(a)), "f"(__uint_as_float(b))
                : "memory");
 }
 
 }  // namespace
 
+// kStages: gathered tiles in flight (3 when the index rows leave room, else 2).
+template <int kStages>
 __global__ void __launch_bounds__(kThreads, 1)
 indexer_kl_bwd_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_cmp,
                                 const __nv_bfloat16* __restrict__ qI, const __nv_bfloat16* __restrict__ w,
@@ -138,6 +138,7 @@ indexer_kl_bwd_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr uint32_t kIdxOff = kStageOff + kStages * kStageBytes;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (base - smem_u32(smem_raw));
   const uint32_t bar_full = smem_u32(&s_full[0]), bar_empty = smem_u32(&s_empty[0]);
@@ -463,22 +464,37 @@ indexer_kl_bwd_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_
     bool have_prev = false;
     uint32_t prev_n = 0;
     int prev_rk = -1;
-    // dkI of tile tn: this thread's entry (gathered row rk, -1: none), all 64 dims
+    // dkI of tile tn for this warp's 32 entries (rk: this lane's entry's gathered
+    // row, -1: none), read in the 16x256b shape so that four threads hold 32
+    // contiguous bytes of a row and each reduction instruction fills whole sectors
     auto epilogue = [&](uint32_t tn, int rk) {
       const uint32_t b = tn & 1u;
       const bool okw = mbar_wait_bounded(bar_kvfull + 8 * b, (tn >> 1) & 1u, status);
       if (__any_sync(0xffffffffu, !okw)) { failed = true; return; }
       tc::fence_after_sync();
-      uint32_t v[64];
-      tc::tmem_ld64_sync(tmem + lane_off + kColKI + b * kDI, v);
+      uint32_t v[4][2][8];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb)
+        tc::tmem_ld16x256_pair_sync(tmem + ((uint32_t)(quad * 32) << 16) + kColKI + b * kDI + cb * 16,
+                                    tmem + ((uint32_t)(quad * 32 + 16) << 16) + kColKI + b * kDI + cb * 16, v[cb][0],
+                                    v[cb][1]);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_kvfree + 8 * b);
-      if (rk >= 0) {
-        float* dst = dkI + (int64_t)rk * kDI;
 #pragma unroll
-        for (int c = 0; c < kDI / 4; ++c) red_add_v4(dst + 4 * c, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-      }
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int rr = __shfl_sync(0xffffffffu, rk, hf * 16 + e * 8 + (lane >> 2));  // entry of these registers
+          if (rr >= 0) {
+            float* dst = dkI + (int64_t)rr * kDI + 2 * (lane & 3);
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+              red_add_v2(dst + cb * 16, v[cb][hf][2 * e], v[cb][hf][2 * e + 1]);
+              red_add_v2(dst + cb * 16 + 8, v[cb][hf][4 + 2 * e], v[cb][hf][4 + 2 * e + 1]);
+            }
+          }
+        }
     };
     while (true) {
       const uint32_t qs = nq & 1u;
@@ -626,6 +642,25 @@ bool indexer_kl_bwd_sparse_tc_supported(const KLBwdArgs& a, bool fp32) {
          a.B <= kMaxB;
 }
 
+template <int kStages>
+static cudaError_t launch_kbs(const KLBwdArgs& a, size_t smem, cudaStream_t stream) {
+  auto kern = indexer_kl_bwd_sparse_tc_kernel<kStages>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = a.T_cap < sms ? a.T_cap : sms;
+  constexpr float kLog2e = 1.4426950408889634f;
+  kern<<<grid, kThreads, smem, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cmp),
+      static_cast<const __nv_bfloat16*>(a.qI), static_cast<const __nv_bfloat16*>(a.w),
+      static_cast<const __nv_bfloat16*>(a.kI), a.idx, a.k_pad, a.lse_cmp, a.student_lse, a.cu, a.cu_cmp, a.B,
+      a.T_cap, a.r, a.scale * kLog2e, a.grad_scale, static_cast<__nv_bfloat16*>(a.dqI),
+      static_cast<__nv_bfloat16*>(a.dw), a.dkI, a.status, a.pos0);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_indexer_kl_bwd_sparse_tc(const KLBwdArgs& a, cudaStream_t stream) {
   if (a.T_cap <= 0) return cudaSuccess;
   // rows without a selected entry (and capacity rows) keep zero gradients
@@ -633,21 +668,11 @@ cudaError_t launch_indexer_kl_bwd_sparse_tc(const KLBwdArgs& a, cudaStream_t str
   if (err == cudaSuccess) err = cudaMemsetAsync(a.dqI, 0, (size_t)a.T_cap * kHI * kDI * 2, stream);
   if (err == cudaSuccess) err = cudaMemsetAsync(a.dw, 0, (size_t)a.T_cap * kHI * 2, stream);
   if (err != cudaSuccess) return err;
-  const size_t smem = kSmem + (size_t)8 * a.k_pad + 1024;
-  err = cudaFuncSetAttribute(indexer_kl_bwd_sparse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = a.T_cap < sms ? a.T_cap : sms;
-  constexpr float kLog2e = 1.4426950408889634f;
-  indexer_kl_bwd_sparse_tc_kernel<<<grid, kThreads, smem, stream>>>(
-      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cmp),
-      static_cast<const __nv_bfloat16*>(a.qI), static_cast<const __nv_bfloat16*>(a.w),
-      static_cast<const __nv_bfloat16*>(a.kI), a.idx, a.k_pad, a.lse_cmp, a.student_lse, a.cu, a.cu_cmp, a.B,
-      a.T_cap, a.r, a.scale * kLog2e, a.grad_scale, static_cast<__nv_bfloat16*>(a.dqI),
-      static_cast<__nv_bfloat16*>(a.dw), a.dkI, a.status, a.pos0);
-  return cudaGetLastError();
+  // a third stage when it fits beside the index rows (227 KB a block, less 8 KB of static arrays)
+  const size_t idx_bytes = (size_t)8 * a.k_pad + 1024;
+  const size_t smem3 = kStageOff + 3 * (size_t)kStageBytes + idx_bytes;
+  if (smem3 + 8 * 1024 <= 232448) return launch_kbs<3>(a, smem3, stream);
+  return launch_kbs<2>(a, kStageOff + 2 * (size_t)kStageBytes + idx_bytes, stream);
 }
 
 }  // namespace csa
