@@ -26,9 +26,10 @@
 // tile is added to the float32 gradient rows of the gathered entries with
 // red.global.add by the warpgroup that computed it, read in the 16x256b shape
 // so that every reduction instruction fills whole 32-byte sectors.  Three
-// gathered tiles are in flight when the index rows leave room, else two.  The MMA warp issues a
-// tile's gradient products after the next tile's scores, so the compute
-// warpgroups never wait on their own products.
+// gathered tiles are in flight when the index rows leave room, else two.  The
+// MMA warp issues a tile's gradient products after the next tile's scores, so
+// the compute warpgroups never wait on their own products -- except for a
+// query's last tile, whose products (and the query's dqI^T) go out at once.
 // Warp roles: six producer warps (warp 8 resolves the index slots; all six
 // gather rows with coalesced 16-byte cp.async copies), one MMA warp (warp 14),
 // two compute warpgroups (warps 0-7) that take alternate tiles.  Every wait
@@ -406,6 +407,12 @@ indexer_kl_bwd_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_
       };
       while (true) {
         const uint32_t st = n % kStages, b = n & 1u;
+        // a query's last tile: its products (and the query's dqI^T) go out before the next
+        // tile is waited for, so the compute warps can close the query while it is gathered
+        if (pend && (pflags & kLast)) {
+          if (!grad()) { ok = false; break; }
+          pend = false;
+        }
         if (!mbar_wait_bounded(bar_full + 8 * st, (n / kStages) & 1u, status)) { ok = false; break; }
         const TileMeta mt = s_meta[st];
         if (mt.flags & kDone) break;
