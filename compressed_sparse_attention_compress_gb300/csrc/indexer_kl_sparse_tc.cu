@@ -303,8 +303,7 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
         for (int it = 0; it < ntl; ++it, ++n) {
           const uint32_t st = n % kStages;
           bool okw = mbar_wait_bounded(bar_empty + 8 * st, ((n / kStages) & 1u) ^ 1u, status);
-          if (bar_or(1, kProdThreads, !okw || *abort_flag != 0)) { *abort_flag = 1; alive = false; break; }
-          if (resolver) {
+          if (resolver && __all_sync(0xffffffffu, okw)) {  // uniform over the warp (the ballots below)
             uint32_t m4[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -323,7 +322,8 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
               s_meta[st] = TileMeta{flags, {m4[0], m4[1], m4[2], m4[3]}};
             }
           }
-          named_sync(1, kProdThreads);  // the resolved rows are visible to both producer warps
+          // one barrier: the joint abort decision, and the resolved rows are visible to every producer warp
+          if (bar_or(1, kProdThreads, !okw || *abort_flag != 0)) { *abort_flag = 1; alive = false; break; }
           // coalesced gather, eight lanes per row and four rows per step: this warp takes the
           // steps j with j % kProdWarps == pw
           const uint32_t kb = base + kStageOff + st * kStageBytes;
