@@ -23,6 +23,10 @@
 // number of issuing warps), one MMA warp (warp 14), and two compute warpgroups
 // (warps 0-7) that take alternate tiles through four tensor-memory score
 // buffers: thread = key of the tile, all 64 head scores of it.
+// When the selected set fits in four tiles (k_pad <= 512), pass 1 gathers the
+// kI rows with the keys and its S^T / I^T tiles stay in tensor memory (one
+// slot per tile) for pass 2, which then neither gathers nor multiplies again;
+// the next query's scores wait for both warpgroups to release the set.
 // Rows with an empty C_t are written by a fill kernel beforehand (KL 0).
 #include <math.h>
 
@@ -116,6 +120,12 @@ __device__ __forceinline__ void warp_sum64_t(float (&v)[64], int lane, float& s0
 
 }  // namespace
 
+// kKeep (a query's selected set fits in kBufs tiles): one gather and one S^T
+// per tile; the query's S^T tiles stay in tensor memory from pass 1 to pass 2
+// (slot = tile), so pass 2 reads them again instead of gathering and
+// multiplying the keys a second time; the next query's scores wait for the
+// compute warps to release the whole set.
+template <bool kKeep>
 __global__ void __launch_bounds__(kThreads, 1)
 indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_cmp,
                             const __nv_bfloat16* __restrict__ qI, const __nv_bfloat16* __restrict__ w,
@@ -130,6 +140,7 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
   __shared__ __align__(8) uint64_t s_sfull[kBufs], s_sfree[kBufs], s_qfull[2], s_qempty[2], s_rfull[2], s_rempty[2];
   __shared__ __align__(8) uint64_t s_ifull[2];  // a query's index row landed in its slot
+  __shared__ __align__(8) uint64_t s_setfree;   // kKeep: a query's score set was read by the compute warps
   __shared__ __align__(8) uint64_t s_drain;
   __shared__ TileMeta s_meta[kStages];     // written by the resolver, per stage
   __shared__ TileMeta s_bmeta[kBufs];      // copied by the MMA thread, per score buffer
@@ -172,6 +183,7 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
       mbar_init(smem_u32(&s_ifull[i]), 2 * kProdThreads);  // the producer warps' copies
     }
     mbar_init(smem_u32(&s_drain), 1);
+    mbar_init(smem_u32(&s_setfree), kComputeWarps);
     fence_mbar_init();
     s_abort = 0;
     s_bad = 0;
@@ -299,7 +311,7 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
         if (lane == 0) arrive_warp(bar_qfull + 8 * qs);
       }
       ++nq;
-      for (int pass = 0; pass < 2 && alive; ++pass) {
+      for (int pass = 0; pass < (kKeep ? 1 : 2) && alive; ++pass) {
         for (int it = 0; it < ntl; ++it, ++n) {
           const uint32_t st = n % kStages;
           bool okw = mbar_wait_bounded(bar_empty + 8 * st, ((n / kStages) & 1u) ^ 1u, status);
@@ -317,8 +329,9 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
               m4[i] = __ballot_sync(0xffffffffu, rr >= 0);
             }
             if (lane == 0) {
-              const int flags = (it == 0 && pass == 0 ? kFirst : 0) | (pass == 1 ? kPass2 : 0) |
-                                (it == ntl - 1 && pass == 0 ? kLastP1 : 0) | (it == ntl - 1 && pass == 1 ? kLast : 0);
+              const bool p2 = kKeep || pass == 1;  // the tile carries kI (every tile with kKeep)
+              const int flags = (it == 0 && pass == 0 ? kFirst : 0) | (p2 ? kPass2 : 0) |
+                                (it == ntl - 1 && pass == 0 ? kLastP1 : 0) | (it == ntl - 1 && p2 ? kLast : 0);
               s_meta[st] = TileMeta{flags, {m4[0], m4[1], m4[2], m4[3]}};
             }
           }
@@ -336,7 +349,7 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
             const uint32_t dst = kb + tc::sw128_offset(key, c);
             cp_async_16_zfill(dst, ks, rk >= 0);
             cp_async_16_zfill(dst + kKRegion, ks + 64, rk >= 0);
-            if (pass == 1)
+            if (kKeep || pass == 1)
               cp_async_16_zfill(dst + 2 * kKRegion, kI + (int64_t)(rk < 0 ? 0 : rk) * kDI + c * 8, rk >= 0);
           }
           arrive_cp_async(bar_full + 8 * st);
@@ -369,8 +382,10 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
       constexpr uint32_t kIdS = tc::idesc_bf16(kTK, kNH, 0, 0);
       constexpr uint32_t kIdI = tc::idesc_bf16(kTK, 16, 0, 0);
       uint32_t n = 0, nq = 0;
+      uint32_t slot = 0;               // kKeep: the tile's slot in its query's score set
+      uint32_t uses[kBufs] = {0u, 0u, 0u, 0u};
       while (true) {
-        const uint32_t st = n % kStages, d = n % kBufs;
+        const uint32_t st = n % kStages;
         if (!mbar_wait_bounded(bar_full + 8 * st, (n / kStages) & 1u, status)) { *abort_flag = 1; break; }
         const TileMeta mt = s_meta[st];
         if (mt.flags & kDone) break;
@@ -380,10 +395,25 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
           *abort_flag = 1;
           break;
         }
-        // the score buffer was read by the warpgroup that took tile n - kBufs
-        if (n >= kBufs && !mbar_wait_bounded(bar_sfree + 8 * d, ((n / kBufs) - 1) & 1u, status)) {
-          *abort_flag = 1;
-          break;
+        uint32_t d;
+        if constexpr (kKeep) {
+          if (mt.flags & kFirst) {
+            slot = 0;
+            // the previous query's score set was read by both compute warpgroups
+            if (nq > 0 && !mbar_wait_bounded(smem_u32(&s_setfree), (nq - 1) & 1u, status)) {
+              *abort_flag = 1;
+              break;
+            }
+          }
+          d = slot++;
+          ++uses[d];
+        } else {
+          d = n % kBufs;
+          // the score buffer was read by the warpgroup that took tile n - kBufs
+          if (n >= kBufs && !mbar_wait_bounded(bar_sfree + 8 * d, ((n / kBufs) - 1) & 1u, status)) {
+            *abort_flag = 1;
+            break;
+          }
         }
         s_bmeta[d] = mt;                 // for the warpgroup that reads buffer d,
         mbar_arrive(bar_sfull + 8 * d);  // released by this arrival (the commit gives the other)
@@ -425,6 +455,7 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
     const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
     constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
     uint32_t n = 0, nq = 0;
+    uint32_t uses[kBufs] = {0u, 0u, 0u, 0u};  // kKeep: queries that used each slot before this one
     while (true) {
       const uint32_t qs = nq & 1u;
       const bool okr = mbar_wait_bounded(bar_rfull + 8 * qs, (nq >> 1) & 1u, status);
@@ -449,9 +480,10 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
       for (int h = 0; h < kNH; ++h) zp[h] = 0.f;
       float tmax = -INFINITY;
       for (int it = 0; it < ntl; ++it) {
-        const uint32_t nn = n + it, d = nn % kBufs;
+        const uint32_t nn = n + it, d = kKeep ? (uint32_t)it : nn % kBufs;
         if ((int)(d & 1u) != wg || failed) continue;
-        if (!mbar_wait_bounded(bar_sfull + 8 * d, (nn / kBufs) & 1u, status)) { failed = true; continue; }
+        const uint32_t par = kKeep ? (uses[d] & 1u) : ((nn / kBufs) & 1u);
+        if (!mbar_wait_bounded(bar_sfull + 8 * d, par, status)) { failed = true; continue; }
         tc::fence_after_sync();
         float x[kNH];
         {
@@ -461,9 +493,11 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
           for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(rs[j]);
         }
         const bool valid = (s_bmeta[d].mask[quad] >> lane) & 1u;
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfree + 8 * d);
+        if constexpr (!kKeep) {
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_sfree + 8 * d);
+        }
         if (valid) {
 #pragma unroll
           for (int h4 = 0; h4 < kNH / 4; ++h4) {
@@ -479,7 +513,7 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
           }
         }
       }
-      n += ntl;
+      if constexpr (!kKeep) n += ntl;
       if (tmax > 32.f) s_bad = 1;  // the reference lies far below the scores
       {
         float s0, s1;
@@ -501,10 +535,12 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
       // ---- pass 2: p(j), i_j and the KL sums ----
       float A = 0.f, Bs = 0.f, mI = -INFINITY, lI = 0.f;
       for (int it = 0; it < ntl; ++it) {
-        const uint32_t nn = n + it, d = nn % kBufs;
+        const uint32_t nn = n + it, d = kKeep ? (uint32_t)it : nn % kBufs;
         if ((int)(d & 1u) != wg || failed) continue;
-        if (!mbar_wait_bounded(bar_sfull + 8 * d, (nn / kBufs) & 1u, status)) { failed = true; continue; }
-        tc::fence_after_sync();
+        if constexpr (!kKeep) {  // kKeep: the tile's scores are still in its slot from pass 1
+          if (!mbar_wait_bounded(bar_sfull + 8 * d, (nn / kBufs) & 1u, status)) { failed = true; continue; }
+          tc::fence_after_sync();
+        }
         float x[kNH];
         uint32_t ri[8];
         {
@@ -514,9 +550,11 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
           for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(rs[j]);
         }
         const bool valid = (s_bmeta[d].mask[quad] >> lane) & 1u;
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfree + 8 * d);
+        if constexpr (!kKeep) {
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_sfree + 8 * d);
+        }
         if (valid) {
           uint64_t pa = f2_pack(0.f, 0.f), pb = pa;
 #pragma unroll
@@ -545,7 +583,14 @@ indexer_kl_sparse_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bflo
           }
         }
       }
-      n += ntl;
+      if constexpr (kKeep) {  // the query's score set is read: the next query's scores may overwrite it
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s_setfree));
+        for (int it = 0; it < ntl; ++it) ++uses[it];
+      } else {
+        n += ntl;
+      }
       {  // reduce the per-key partials over the warp, then the eight warps
         float a = A, bs = Bs, mm = mI, ll = lI;
 #pragma unroll
@@ -598,25 +643,33 @@ bool indexer_kl_sparse_tc_supported(const KLArgs& a, bool fp32) {
          a.d_I == kDI && a.r > 0 && a.k_pad % 4 == 0 && a.k_pad <= 4096 && a.B <= kMaxB;
 }
 
-cudaError_t launch_indexer_kl_sparse_tc(const KLArgs& a, cudaStream_t stream) {
-  if (a.T_cap <= 0) return cudaSuccess;
-  // every row first as an empty C_t; the kernel overwrites the rows it computes
-  cudaError_t err = launch_kl_zero_rows(a.kl_rows, a.csize, a.T_cap, a.teacher_lse, a.H, a.student_lse, stream);
-  if (err != cudaSuccess) return err;
+template <bool kKeep>
+static cudaError_t launch_kls(const KLArgs& a, cudaStream_t stream) {
   const size_t smem = kSmem + (size_t)8 * a.k_pad + 1024;
-  err = cudaFuncSetAttribute(indexer_kl_sparse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = indexer_kl_sparse_tc_kernel<kKeep>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = a.T_cap < sms ? a.T_cap : sms;
   constexpr float kLog2e = 1.4426950408889634f;
-  indexer_kl_sparse_tc_kernel<<<grid, kThreads, smem, stream>>>(
+  kern<<<grid, kThreads, smem, stream>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cmp),
       static_cast<const __nv_bfloat16*>(a.qI), static_cast<const __nv_bfloat16*>(a.w),
       static_cast<const __nv_bfloat16*>(a.kI), a.idx, a.k_pad, a.lse_cmp, a.cu, a.cu_cmp, a.B, a.T_cap, a.r,
       a.scale * kLog2e, a.kl_rows, a.csize, a.status, a.teacher_lse, a.student_lse, a.pos0);
   return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_kl_sparse_tc(const KLArgs& a, cudaStream_t stream) {
+  if (a.T_cap <= 0) return cudaSuccess;
+  // every row first as an empty C_t; the kernel overwrites the rows it computes
+  cudaError_t err = launch_kl_zero_rows(a.kl_rows, a.csize, a.T_cap, a.teacher_lse, a.H, a.student_lse, stream);
+  if (err != cudaSuccess) return err;
+  // a selected set of at most kBufs tiles keeps its scores in tensor memory between the passes
+  if (a.k_pad <= kBufs * kTK) return launch_kls<true>(a, stream);
+  return launch_kls<false>(a, stream);
 }
 
 }  // namespace csa

@@ -9,6 +9,8 @@ the middle), rows whose selected set is empty, sequences shorter than one
 block and several tiles per query, and compare every row with the oracle; the
 same call without the reference (the warp-level kernel) must agree with it,
 and a reference far below the true normaliser must raise the bounds status.
+A selected set of up to four tiles keeps its scores in tensor memory between
+the passes; a longer one is gathered and multiplied again: both are covered.
 """
 import numpy as np
 import pytest
@@ -28,11 +30,14 @@ from compressed_sparse_attention_compress_gb300.forward import Forward, to_devic
 
 WL = I.custom("kl_sparse", lengths=[1500, 3, 0, 777], ratio=4, overlap=True, H=64, d=128, window=128, H_I=8,
               d_I=64, topk=300, k_pad=384, kl_mode="sparse", cap_align=64)
+# more than four tiles per query: the scores are gathered and multiplied again in pass 2
+WL_LONG = I.custom("kl_sparse_long", lengths=[3100, 3, 0, 777], ratio=4, overlap=True, H=64, d=128, window=128,
+                   H_I=8, d_I=64, topk=600, k_pad=640, kl_mode="sparse", cap_align=64)
 
 
-def _setup(seed=2):
-    arrs = I.generate(WL, seed)
-    f = Forward(WL, to_device(arrs, False))
+def _setup(seed=2, wl=WL):
+    arrs = I.generate(wl, seed)
+    f = Forward(wl, to_device(arrs, False))
     f.run()
     torch.cuda.synchronize()
     assert f.h.device_status() == 0
@@ -52,27 +57,28 @@ def _kl(f, idx, lse_cmp, T_cap):
     kl_sum = torch.zeros(1, device="cuda")
     rows = torch.full((T_cap,), 7.0, device="cuda")
     n_valid = torch.zeros(1, dtype=torch.int32, device="cuda")
-    tl = torch.full((T_cap, WL.H), 7.0, device="cuda")
+    tl = torch.full((T_cap, f.wl.H), 7.0, device="cuda")
     sl = torch.full((T_cap,), 7.0, device="cuda")
     api.csa_indexer_kl_ex(f.h, f.x["q"], f.kv_cmp, f.x["qI"], f.x["w"], f.kI, f.cu, f.cu_cmp, f.max_seqlen,
-                          WL.ratio, f.scale, kl_sum, f.ws, teacher_lse=tl, student_lse=sl, idx=idx,
+                          f.wl.ratio, f.scale, kl_sum, f.ws, teacher_lse=tl, student_lse=sl, idx=idx,
                           lse_cmp=lse_cmp, kl_per_query=rows, n_valid=n_valid)
     torch.cuda.synchronize()
     return kl_sum, rows, n_valid, tl, sl
 
 
+@pytest.mark.parametrize("wl", [WL, WL_LONG], ids=["keep", "long"])
 @pytest.mark.parametrize("with_reference", [True, False])
-def test_selected_set_kl_with_holes_and_empty_rows(with_reference):
-    f, arrs = _setup()
+def test_selected_set_kl_with_holes_and_empty_rows(with_reference, wl):
+    f, arrs = _setup(wl=wl)
     idx = _holes(f)
-    kl_sum, rows, n_valid, tl, sl = _kl(f, idx, f.lse_cmp if with_reference else None, WL.T_cap)
+    kl_sum, rows, n_valid, tl, sl = _kl(f, idx, f.lse_cmp if with_reference else None, wl.T_cap)
     assert f.h.device_status() == 0
     cu = arrs["cu_seqlens"]
     n_c = int(f.cu_cmp[-1].item())
     kv_cmp, kI = ph.operand(f.kv_cmp[:n_c]), ph.operand(f.kI[:n_c])
     idx_np = idx.cpu().numpy()
-    every = np.arange(WL.T_cap)
-    ph.check_kl(float(kl_sum.item()), ph.np32(rows), arrs["q"], kv_cmp, arrs["qI"], arrs["w"], kI, cu, WL.ratio,
+    every = np.arange(wl.T_cap)
+    ph.check_kl(float(kl_sum.item()), ph.np32(rows), arrs["q"], kv_cmp, arrs["qI"], arrs["w"], kI, cu, wl.ratio,
                 f.scale, idx_np, every, full=True)
     sizes = (idx_np >= 0).sum(1)
     assert int(n_valid.item()) == int((sizes > 0).sum())
@@ -80,7 +86,7 @@ def test_selected_set_kl_with_holes_and_empty_rows(with_reference):
     q = arrs["q"].astype(np.float64)
     qI, w = arrs["qI"].astype(np.float64), arrs["w"].astype(np.float64)
     tl_np, sl_np = ph.np32(tl), ph.np32(sl)
-    for row in [0, 4, 5, 700, 1499, 1500, 1502, 2000, WL.T - 1, WL.T_cap - 1]:
+    for row in [0, 4, 5, 700, 1499, 1500, 1502, 2000, wl.T - 1, wl.T_cap - 1]:
         sel = idx_np[row][idx_np[row] >= 0]
         if sel.size == 0:
             assert np.all(np.isneginf(tl_np[row])) and np.isneginf(sl_np[row]) and ph.np32(rows)[row] == 0
