@@ -85,6 +85,11 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 using klb::Block;
 
@@ -308,28 +313,47 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
 #pragma unroll
             for (int c = 0; c < kTK / 2; ++c) x[c] = c < nv ? x[c] : -INFINITY;
           }
-          float tmax = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < kTK / 2; c += 4)
-            tmax = fmaxf(tmax, fmaxf(fmaxf(x[c], x[c + 1]), fmaxf(x[c + 2], x[c + 3])));
-          const float mn = fmaxf(m, tmax * scale_log2);  // scale > 0: max commutes with it
-          if (mn != -INFINITY) {
-            // packed pairs: one f32x2 FMA and one f32x2 add per two columns
-            const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-mn, -mn);
+          // sum over the tile of 2^(x scale - ref): packed pairs, one f32x2 FMA and one f32x2 add
+          // per two columns
+          auto tile_sum = [&](float ref) {
+            const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nr2 = f2_pack(-ref, -ref);
             uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
             for (int c = 0; c < kTK / 2; c += 4) {
               float a0, a1, a2, a3;
-              f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sc2, nm2), a0, a1);
-              f2_unpack(f2_fma(f2_pack(x[c + 2], x[c + 3]), sc2, nm2), a2, a3);
+              f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sc2, nr2), a0, a1);
+              f2_unpack(f2_fma(f2_pack(x[c + 2], x[c + 3]), sc2, nr2), a2, a3);
               acc0 = f2_add(acc0, f2_pack(ex2(a0), ex2(a1)));
               acc1 = f2_add(acc1, f2_pack(ex2(a2), ex2(a3)));
             }
             float s0, s1, s2, s3;
             f2_unpack(acc0, s0, s1);
             f2_unpack(acc1, s2, s3);
-            l = l * ex2(m - mn) + ((s0 + s1) + (s2 + s3));
-            m = mn;
+            return (s0 + s1) + (s2 + s3);
+          };
+          // After the row's first tile, its running reference m stays put: every term is taken
+          // against it, with no tile maximum, which holds while no score exceeds m by 64 or more
+          // (each term below 2^64, the sum far from the float range's end). A tile whose sum
+          // reaches 2^64 (or overflows) is redone against its own maximum, as the first is.
+          bool exact = m == -INFINITY;
+          if (!exact) {
+            const float ts = tile_sum(m);
+            if (ts < 1.8446744e19f) l += ts;  // 2^64; false for inf and NaN
+            else exact = true;
+          }
+          if (exact) {
+            float t0 = -INFINITY, t1 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTK / 2; c += 4) {
+              t0 = max3f(t0, x[c], x[c + 1]);
+              t1 = max3f(t1, x[c + 2], x[c + 3]);
+            }
+            const float mn = fmaxf(m, fmaxf(t0, t1) * scale_log2);  // scale > 0: max commutes with it
+            if (mn != -INFINITY) {
+              const float ts = tile_sum(mn);
+              l = l * ex2(m - mn) + ts;
+              m = mn;
+            }
           }
           KL_ADD(2, c_c1);
           KL_CNT(7);
@@ -522,7 +546,8 @@ cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream) {
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t smem = kSmemBytes + 1024;
-  err = cudaFuncSetAttribute(indexer_kl_dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = indexer_kl_dense_tc_kernel;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -530,7 +555,7 @@ cudaError_t launch_indexer_kl_dense_tc(const KLArgs& a, cudaStream_t stream) {
   const int blocks = (a.T_cap + kQB - 1) / kQB + a.B;  // upper bound on query blocks
   const int grid = blocks < sms ? blocks : sms;
   constexpr float kLog2e = 1.4426950408889634f;
-  indexer_kl_dense_tc_kernel<<<grid, kThreads, smem, stream>>>(
+  kern<<<grid, kThreads, smem, stream>>>(
       mq, mk, mqi, mki, static_cast<const __nv_bfloat16*>(a.w), a.cu, a.cu_cmp, a.B, a.r, a.scale * kLog2e,
       a.kl_rows, a.csize, a.status, a.teacher_lse, a.student_lse, a.pos0);
   return cudaGetLastError();
