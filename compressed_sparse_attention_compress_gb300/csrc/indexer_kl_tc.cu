@@ -14,8 +14,10 @@
 // swizzle), each tile feeding 256 rows of tensor-core work.
 //   pass 1  S = Q K^T   (two M=128 tiles of query-head rows, N=128 keys, two
 //           tensor-memory buffers so the next tile's MMAs run during this
-//           tile's arithmetic): each row's online log-sum-exp -> lse_h, every
-//           row split over two threads (64 key columns each), merged at the end.
+//           tile's arithmetic): each row's log-sum-exp -> lse_h. Two warpgroup
+//           pairs take alternate tiles (one buffer each), a thread a whole row
+//           of its tile; each pair keeps a partial (reference, sum) per row,
+//           merged at the end.
 //   pass 2  S^T = K Q^T (M=128 keys, N=256 query-heads) and the indexer tile
 //           I^T = kI qI^T (M=128 keys, N=32 = 4 queries x 8 heads): one thread
 //           per (key, query) forms p(j) = mean_h exp(s_h - lse_h), the indexer
@@ -24,7 +26,8 @@
 // Warp roles: warps 0-15 compute (four warpgroups, one tensor-memory lane per
 // thread; four warps per scheduler hide the exp2 and FMA latencies), warp 16
 // issues the TMA loads, warp 17 allocates tensor memory and issues the MMAs.
-// Threads copy each score tile to registers and release it at once.
+// Pass 2 threads copy each score tile to registers and release it at once;
+// pass 1 threads release theirs once both 64-column chunks are loaded.
 #include <math.h>
 
 #include "common.cuh"
@@ -281,80 +284,102 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         const int q = tid / kHI, h = tid % kHI;
         s_w[q][h] = q < bk.nq ? __bfloat162float(w[(int64_t)(bk.seq0 + bk.q0 + q) * kHI + h]) : 0.f;
       }
-      // ---- pass 1: row (query, head) online log-sum-exp; warpgroup = (M-tile, column half) ----
+      // ---- pass 1: row (query, head) online log-sum-exp ----
+      // Warpgroup pair wg >> 1 takes the tiles of score buffer wg >> 1 (every other tile): whole
+      // 128-column rows of M-tile wg & 1, in two 64-column chunks, so the two pairs work on
+      // consecutive tiles at once rather than all sixteen warps waiting on one.
       {
-        const int mt = wg >> 1, half = wg & 1;
+        const int mt = wg & 1;
+        const int half = wg >> 1;  // the pair: its buffer, and the slot of its partial (m, l) of the row
         const int q = 2 * mt + (rowl >> 6), h = rowl & 63;
         const int nvis = (bk.q0 + q + bk.p0 + 1) / r;
         float m = -INFINITY, l = 0.f;
         for (int i = 0; i < bk.ntiles; ++i) {
           const uint32_t d = p1++ & 1u;
+          if (d != (uint32_t)half) {  // the other pair's tile
+            if (d) ++nf1; else ++nf0;
+            continue;
+          }
           KL_T0(c_w1);
           if (!mbar_wait_bounded(bar_sfull + 8 * d, (d ? nf1 : nf0) & 1u, status)) { s_abort = 1; break; }
           KL_ADD(0, c_w1);
           KL_T0(c_l1);
           tc::fence_after_sync();
           float x[kTK / 2];
+          auto load = [&](int col) {
 #pragma unroll
-          for (int c0 = 0; c0 < kTK / 2; c0 += 32) {
-            uint32_t rs[32];
-            tc::tmem_ld32_sync(tmem + lane_off + d * kBufCols + mt * kTK + half * (kTK / 2) + c0, rs);
+            for (int c0 = 0; c0 < kTK / 2; c0 += 32) {
+              uint32_t rs[32];
+              tc::tmem_ld32_sync(tmem + lane_off + d * kBufCols + mt * kTK + col + c0, rs);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) x[c0 + jj] = __uint_as_float(rs[jj]);
-          }
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_sfree + 8 * d);
-          if (d) ++nf1; else ++nf0;
+              for (int jj = 0; jj < 32; ++jj) x[c0 + jj] = __uint_as_float(rs[jj]);
+            }
+          };
+          auto release = [&]() {
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {  // the barrier counts an arrival from each of the sixteen compute warps
+              mbar_arrive(bar_sfree + 8 * d);
+              mbar_arrive(bar_sfree + 8 * d);
+            }
+            if (d) ++nf1; else ++nf0;
+          };
+          // the 64 columns in x, of which the first nv are visible, folded into (m, l)
+          auto fold = [&](int nv) {
+            if (nv < kTK / 2) {  // only the last tile of a row is partial
+#pragma unroll
+              for (int c = 0; c < kTK / 2; ++c) x[c] = c < nv ? x[c] : -INFINITY;
+            }
+            // sum over the chunk of 2^(x scale - ref): packed pairs, one f32x2 FMA and one f32x2
+            // add per two columns
+            auto chunk_sum = [&](float ref) {
+              const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nr2 = f2_pack(-ref, -ref);
+              uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+              for (int c = 0; c < kTK / 2; c += 4) {
+                float a0, a1, a2, a3;
+                f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sc2, nr2), a0, a1);
+                f2_unpack(f2_fma(f2_pack(x[c + 2], x[c + 3]), sc2, nr2), a2, a3);
+                acc0 = f2_add(acc0, f2_pack(ex2(a0), ex2(a1)));
+                acc1 = f2_add(acc1, f2_pack(ex2(a2), ex2(a3)));
+              }
+              float s0, s1, s2, s3;
+              f2_unpack(acc0, s0, s1);
+              f2_unpack(acc1, s2, s3);
+              return (s0 + s1) + (s2 + s3);
+            };
+            // After the row's first chunk, its running reference m stays put: every term is taken
+            // against it, with no chunk maximum, which holds while no score exceeds m by 64 or more
+            // (each term below 2^64, the sum far from the float range's end). A chunk whose sum
+            // reaches 2^64 (or overflows) is redone against its own maximum, as the first is.
+            bool exact = m == -INFINITY;
+            if (!exact) {
+              const float ts = chunk_sum(m);
+              if (ts < 1.8446744e19f) l += ts;  // 2^64; false for inf and NaN
+              else exact = true;
+            }
+            if (exact) {
+              float t0 = -INFINITY, t1 = -INFINITY;
+#pragma unroll
+              for (int c = 0; c < kTK / 2; c += 4) {
+                t0 = max3f(t0, x[c], x[c + 1]);
+                t1 = max3f(t1, x[c + 2], x[c + 3]);
+              }
+              const float mn = fmaxf(m, fmaxf(t0, t1) * scale_log2);  // scale > 0: max commutes with it
+              if (mn != -INFINITY) {
+                const float ts = chunk_sum(mn);
+                l = l * ex2(m - mn) + ts;
+                m = mn;
+              }
+            }
+          };
+          load(0);
           KL_ADD(1, c_l1);
           KL_T0(c_c1);
-          const int nv = nvis - i * kTK - half * (kTK / 2);  // valid columns of this thread's half
-          if (nv < kTK / 2) {               // only the last tile of a row is partial
-#pragma unroll
-            for (int c = 0; c < kTK / 2; ++c) x[c] = c < nv ? x[c] : -INFINITY;
-          }
-          // sum over the tile of 2^(x scale - ref): packed pairs, one f32x2 FMA and one f32x2 add
-          // per two columns
-          auto tile_sum = [&](float ref) {
-            const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nr2 = f2_pack(-ref, -ref);
-            uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-#pragma unroll
-            for (int c = 0; c < kTK / 2; c += 4) {
-              float a0, a1, a2, a3;
-              f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sc2, nr2), a0, a1);
-              f2_unpack(f2_fma(f2_pack(x[c + 2], x[c + 3]), sc2, nr2), a2, a3);
-              acc0 = f2_add(acc0, f2_pack(ex2(a0), ex2(a1)));
-              acc1 = f2_add(acc1, f2_pack(ex2(a2), ex2(a3)));
-            }
-            float s0, s1, s2, s3;
-            f2_unpack(acc0, s0, s1);
-            f2_unpack(acc1, s2, s3);
-            return (s0 + s1) + (s2 + s3);
-          };
-          // After the row's first tile, its running reference m stays put: every term is taken
-          // against it, with no tile maximum, which holds while no score exceeds m by 64 or more
-          // (each term below 2^64, the sum far from the float range's end). A tile whose sum
-          // reaches 2^64 (or overflows) is redone against its own maximum, as the first is.
-          bool exact = m == -INFINITY;
-          if (!exact) {
-            const float ts = tile_sum(m);
-            if (ts < 1.8446744e19f) l += ts;  // 2^64; false for inf and NaN
-            else exact = true;
-          }
-          if (exact) {
-            float t0 = -INFINITY, t1 = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kTK / 2; c += 4) {
-              t0 = max3f(t0, x[c], x[c + 1]);
-              t1 = max3f(t1, x[c + 2], x[c + 3]);
-            }
-            const float mn = fmaxf(m, fmaxf(t0, t1) * scale_log2);  // scale > 0: max commutes with it
-            if (mn != -INFINITY) {
-              const float ts = tile_sum(mn);
-              l = l * ex2(m - mn) + ts;
-              m = mn;
-            }
-          }
+          fold(nvis - i * kTK);
+          load(kTK / 2);  // the buffer is released once both chunks are in registers
+          release();
+          fold(nvis - i * kTK - kTK / 2);
           KL_ADD(2, c_c1);
           KL_CNT(7);
         }
@@ -362,7 +387,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         s_ml[half][mt * kTK + rowl][0] = m;
         s_ml[half][mt * kTK + rowl][1] = l;
         named_sync(1, kComputeThreads);
-        if (half == 0 && q < kQB) {  // merge the two column halves of the row
+        if (half == 0 && q < kQB) {  // merge the row's two partials
           const float m2 = s_ml[1][mt * kTK + rowl][0], l2 = s_ml[1][mt * kTK + rowl][1];
           const float mx = fmaxf(m, m2);
           const float ls = (mx == -INFINITY) ? 0.f : l * ex2(m - mx) + l2 * ex2(m2 - mx);
