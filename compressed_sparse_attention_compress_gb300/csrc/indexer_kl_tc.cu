@@ -201,7 +201,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
       constexpr uint32_t kIdP1 = tc::idesc_bf16(128, kTK, 0, 0);
       constexpr uint32_t kIdP2 = tc::idesc_bf16(kTK, kQB * kNH, 0, 0);
       constexpr uint32_t kIdI = tc::idesc_bf16(kTK, kQB * kHI, 0, 0);
-      uint32_t it = 0, nblk = 0, p1 = 0, nf0 = 0, nf1 = 0;
+      uint32_t it = 0, nblk = 0, nf0 = 0, nf1 = 0;
       for (int k = blockIdx.x; k < total && !*(volatile int*)&s_abort; k += gridDim.x) {
         Block bk;
         if (!klb::block_of<kQB, kTK>(cu, cu_cmp, B, r, total, k, bk, pos0) || bk.ntiles == 0) continue;
@@ -210,8 +210,10 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         for (int pass = 0; pass < 2; ++pass) {
           for (int i = 0; i < bk.ntiles; ++i, ++it) {
             const uint32_t s = it % kStages;
-            // pass 1 alternates the two score buffers; a pass 2 tile takes both
-            const uint32_t d = p1 & 1u;
+            // pass 1 alternates the two score buffers (even tiles of a block: buffer 0, so every
+            // row's partial sums take the same tiles whatever the block's place in the grid);
+            // a pass 2 tile takes both
+            const uint32_t d = (uint32_t)i & 1u;
             const bool use0 = pass == 1 || d == 0, use1 = pass == 1 || d == 1;
             KL_T0(m_f);
             const bool okf = mbar_wait_bounded(bar_full + 8 * s, (it / kStages) & 1u, status);
@@ -236,7 +238,6 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
                   const uint64_t bd = tc::smem_desc_sw128(st + (ks >> 2) * kKRegion + (ks & 3) * 32, 16, 1024);
                   tc::mma_bf16(tmem + d * kBufCols + g * kTK, a, bd, kIdP1, ks > 0 ? 1u : 0u);
                 }
-              ++p1;
             } else {
 #pragma unroll
               for (int ks = 0; ks < kDim / 16; ++ks) {
@@ -269,7 +270,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
     const int quad = warp & 3;               // tensor-memory lane quadrant
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const int rowl = quad * 32 + lane;       // tensor-memory lane of this thread
-    uint32_t p1 = 0, nf0 = 0, nf1 = 0;       // score-buffer uses, as counted by the MMA warp
+    uint32_t nf0 = 0, nf1 = 0;               // score-buffer uses, as counted by the MMA warp
     for (int k = blockIdx.x; k < total; k += gridDim.x) {
       Block bk;
       if (!klb::block_of<kQB, kTK>(cu, cu_cmp, B, r, total, k, bk, pos0)) continue;
@@ -295,7 +296,7 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         const int nvis = (bk.q0 + q + bk.p0 + 1) / r;
         float m = -INFINITY, l = 0.f;
         for (int i = 0; i < bk.ntiles; ++i) {
-          const uint32_t d = p1++ & 1u;
+          const uint32_t d = (uint32_t)i & 1u;
           if (d != (uint32_t)half) {  // the other pair's tile
             if (d) ++nf1; else ++nf0;
             continue;
