@@ -308,13 +308,10 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
           tc::fence_after_sync();
           float x[kTK / 2];
           auto load = [&](int col) {
+            uint32_t rs[kTK / 2];
+            tc::tmem_ld64_sync(tmem + lane_off + d * kBufCols + mt * kTK + col, rs);
 #pragma unroll
-            for (int c0 = 0; c0 < kTK / 2; c0 += 32) {
-              uint32_t rs[32];
-              tc::tmem_ld32_sync(tmem + lane_off + d * kBufCols + mt * kTK + col + c0, rs);
-#pragma unroll
-              for (int jj = 0; jj < 32; ++jj) x[c0 + jj] = __uint_as_float(rs[jj]);
-            }
+            for (int jj = 0; jj < kTK / 2; ++jj) x[jj] = __uint_as_float(rs[jj]);
           };
           auto release = [&]() {
             tc::fence_before_sync();
@@ -417,14 +414,12 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
         tc::fence_after_sync();
         float x[kNH];
         uint32_t ri[8];
+        {
+          uint32_t rs[kNH];
+          tc::tmem_ld64_ld8_sync(tmem + lane_off + q * kNH, tmem + lane_off + kColI + q * kHI, rs, ri);
 #pragma unroll
-        for (int c0 = 0; c0 < kNH; c0 += 32) {
-          uint32_t rs[32];
-          tc::tmem_ld32_sync(tmem + lane_off + q * kNH + c0, rs);
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) x[c0 + jj] = __uint_as_float(rs[jj]);
+          for (int jj = 0; jj < kNH; ++jj) x[jj] = __uint_as_float(rs[jj]);
         }
-        tc::tmem_ld8_sync(tmem + lane_off + kColI + q * kHI, ri);
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) {
@@ -458,11 +453,14 @@ indexer_kl_dense_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __gr
           for (int hh = 0; hh < kHI; ++hh) iv = fmaf(s_w[q][hh], fmaxf(__uint_as_float(ri[hh]), 0.f), iv);
           if (p > 0.f) A = fmaf(p, __logf(p), A);
           Bs = fmaf(p, iv, Bs);
-          if (iv > mI) {
+          // the student's sum against a held reference: the thread's first key sets it, and a
+          // key whose term reaches 2^64 against it moves it
+          const float e = __expf(iv - mI);
+          if (e < 1.8446744e19f) {
+            lI += e;  // not taken while mI == -inf (e = inf)
+          } else {
             lI = lI * __expf(mI - iv) + 1.f;
             mI = iv;
-          } else {
-            lI += __expf(iv - mI);
           }
         }
         KL_ADD(5, c_c2);
