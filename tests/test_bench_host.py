@@ -68,3 +68,17 @@ def test_launch_counts_follow_the_dispatch(bench):
     # attention backward: delta, capacity rows, kernel; indexer backward: one kernel
     assert bench.b_launches(wl) == 3 + 1
     assert bench.f_launches(WORKLOADS["hca64k"]) == 1 + 1 + 2
+
+
+def test_dense_kl_traffic_is_its_operands_read_once(bench):
+    """The recorded DRAM bytes of one dense-teacher KL launch at 32K are its operands read
+    once (queries, indexer queries and weights, the compressed key and indexer-key rows),
+    within a few percent: the key prefix stays in L2 for the blocks that share it."""
+    from compressed_sparse_attention_compress_gb300 import inputs as I
+    wl = I.WORKLOADS["warmup32k"]
+    t = bench._traffic("indexer_kl", "warmup32k")
+    if t is None:
+        pytest.skip("no capture recorded for the current kernel")
+    n_c = wl.T // wl.ratio
+    algo = wl.T * (wl.H * wl.d + wl.H_I * wl.d_I + wl.H_I) * 2 + n_c * (wl.d + wl.d_I) * 2
+    assert 0.98 * algo <= t <= 1.05 * algo, (t, algo)
